@@ -1,0 +1,197 @@
+"""fp64 CPU oracle for selected-token log-probabilities.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path may import, call or
+execute this module: only ``tests/``, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` use it.  It shares no code, constant or helper with
+the CUDA library; the only thing the two sides share is the seeded input
+generator, which holds none of the method's arithmetic.
+
+What it computes (the plain definition, written out in float64):
+
+    z[n, v]   = x[n, v] / T
+    lse[n]    = max_v z[n, v] + log( sum_v exp(z[n, v] - max_v z[n, v]) )
+    logprob[n]= z[n, t_n] - lse[n]                       (= -cross_entropy(z, t) at
+                                                          label smoothing 0)
+    grad_x[n, v] = g[n] * (1[v == t_n] - exp(z[n, v] - lse[n])) / T
+
+Rows with loss_mask == 0 give logprob = lse = 0 and an all-zero gradient.
+
+Sources (page title, then the section):
+  * Megatron-LM issue #6700 "Avoid full-vocabulary TP gather for selected-token
+    logprobs", section "Proposed solution": the identity
+    log_softmax(logits)[target] == -cross_entropy(logits, target) at label
+    smoothing 0, and numerically stable normalisation.
+  * torchforge PR #608 "Reduce reference model memory with parallel logprob
+    computation", section "Implementation": the log-sum-exp trick (max, then sum
+    of exp(x - max)), and the target logit gathered once.
+  * NeMo-RL PR #4222 "chunk target logprobs without tensor parallelism", section
+    "Changes": backward writes (onehot - softmax) * grad_output into a buffer of
+    the logits' dtype, recomputing the softmax from the saved inputs.
+  * verl PR #7733 "memory-efficient chunked top-k KL", section "Design & Code
+    Changes": the per-token fp32 logZ is what the forward keeps for backward.
+  * slime issue #2253 "full-vocab fp32 logits over the packed sequence -> OOM",
+    maintainer analysis: only loss_mask == 1 rows are computed, before the
+    vocabulary projection; off-mask values are zero after the scatter.
+
+Readings where the pages are silent (each is also listed in the design notes):
+  * temperature divides the logits before the softmax (z = x / T); the gradient
+    is taken with respect to the raw logits, so it carries the factor 1/T;
+  * lse is the log-sum-exp of the scaled logits z;
+  * an all -inf row gives NaN (as log_softmax does); a target on a -inf column
+    gives logprob = -inf;
+  * the LM head has no bias; its logits are h @ W^T in float64.
+
+Every function here is pinned by ``tests/test_oracle_pins.py`` against closed
+forms, invariants, finite differences and independent library routines.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "decode_bf16",
+    "selected_logprob_forward",
+    "selected_logprob_backward",
+    "lmhead_logits",
+    "lmhead_forward",
+    "lmhead_backward",
+]
+
+
+def decode_bf16(bits) -> np.ndarray:
+    """Exact float64 values of bfloat16 numbers given as their 16-bit patterns.
+
+    A bfloat16 is the upper half of an IEEE binary32, so widening is a 16-bit
+    left shift of the pattern: no rounding is involved.
+    """
+    b = np.asarray(bits).astype(np.uint16).astype(np.uint32) << np.uint32(16)
+    with np.errstate(invalid="ignore"):
+        return b.view(np.float32).astype(np.float64)
+
+
+def _as_f64(a) -> np.ndarray:
+    return np.asarray(a, dtype=np.float64)
+
+
+def _active_rows(N: int, mask) -> np.ndarray:
+    if mask is None:
+        return np.ones(N, dtype=bool)
+    return np.asarray(mask).reshape(N) != 0
+
+
+def selected_logprob_forward(x, t, mask, T: float):
+    """Forward of the selected-token log-probability for every row.
+
+    x: [N, V] real logits (any float dtype; widened to float64).
+    t: [N] integer targets in [0, V).  mask: [N] (nonzero = compute) or None.
+    T: temperature > 0.
+
+    Returns (logprob[N], lse[N]) in float64; inactive rows are 0.
+
+    Follows torchforge PR #608, "Implementation" (max, sum of exp(x - max),
+    target logit), on the scaled logits x / T; the identity with
+    -cross_entropy is Megatron-LM issue #6700, "Proposed solution".
+    """
+    x = _as_f64(x)
+    N = x.shape[0]
+    t = np.asarray(t).reshape(N).astype(np.int64)
+    active = _active_rows(N, mask)
+    logprob = np.zeros(N, dtype=np.float64)
+    lse = np.zeros(N, dtype=np.float64)
+    with np.errstate(invalid="ignore", over="ignore", divide="ignore"):
+        for n in range(N):
+            if not active[n]:
+                continue
+            z = x[n] / T
+            M = np.max(z)
+            S = np.sum(np.exp(z - M))
+            lse[n] = M + np.log(S)
+            logprob[n] = z[t[n]] - lse[n]
+    return logprob, lse
+
+
+def selected_logprob_backward(x, t, mask, T: float, lse, grad_out):
+    """Gradient of sum_n grad_out[n] * logprob[n] with respect to the raw logits.
+
+    grad_x[n, v] = grad_out[n] * (1[v == t_n] - exp(x[n, v] / T - lse[n])) / T,
+    with the softmax recomputed from x and the saved lse (NeMo-RL PR #4222,
+    "Changes": (onehot - softmax) * grad_output; verl PR #7733, "Design & Code
+    Changes": recompute from the saved per-token logZ).  Inactive rows are 0.
+    """
+    x = _as_f64(x)
+    N, V = x.shape
+    t = np.asarray(t).reshape(N).astype(np.int64)
+    lse = _as_f64(lse).reshape(N)
+    g = _as_f64(grad_out).reshape(N)
+    active = _active_rows(N, mask)
+    grad = np.zeros((N, V), dtype=np.float64)
+    with np.errstate(invalid="ignore", over="ignore"):
+        for n in range(N):
+            if not active[n]:
+                continue
+            p = np.exp(x[n] / T - lse[n])
+            onehot = np.zeros(V, dtype=np.float64)
+            onehot[t[n]] = 1.0
+            grad[n] = g[n] * (onehot - p) / T
+    return grad
+
+
+def lmhead_logits(h, W) -> np.ndarray:
+    """LM-head logits h @ W^T in float64 (no bias).
+
+    h: [N, d], W: [V, d].  The products of two bfloat16 values are exact in
+    float64, so only the summation order is left to the library matmul.
+    """
+    return _as_f64(h) @ _as_f64(W).T
+
+
+def lmhead_forward(h, W, t, mask, T: float):
+    """Selected-token log-probabilities through the LM head.
+
+    Only rows with mask != 0 are projected to the vocabulary (slime issue
+    #2253, maintainer analysis: keep trainable rows before the vocabulary
+    projection, compute compact rows, scatter scalars back); the others return
+    logprob = lse = 0.
+    """
+    h = _as_f64(h)
+    N = h.shape[0]
+    active = _active_rows(N, mask)
+    t = np.asarray(t).reshape(N).astype(np.int64)
+    logprob = np.zeros(N, dtype=np.float64)
+    lse = np.zeros(N, dtype=np.float64)
+    rows = np.nonzero(active)[0]
+    if rows.size:
+        x = lmhead_logits(h[rows], W)
+        lp_c, lse_c = selected_logprob_forward(x, t[rows], None, T)
+        logprob[rows] = lp_c
+        lse[rows] = lse_c
+    return logprob, lse
+
+
+def lmhead_backward(h, W, t, mask, T: float, lse, grad_out):
+    """Gradients of sum_n grad_out[n] * logprob[n] with respect to h and W.
+
+    dz = selected_logprob_backward of the compact logits; then
+    dh = dz @ W and dW = dz^T @ h over the active rows only.  Inactive rows of
+    dh are 0 (Megatron-LM issue #6700, "Prototype correctness": masked
+    positions have exactly zero gradient).
+    Returns (dh [N, d], dW [V, d]) in float64.
+    """
+    h = _as_f64(h)
+    W = _as_f64(W)
+    N, d = h.shape
+    V = W.shape[0]
+    active = _active_rows(N, mask)
+    t = np.asarray(t).reshape(N).astype(np.int64)
+    lse = _as_f64(lse).reshape(N)
+    g = _as_f64(grad_out).reshape(N)
+    dh = np.zeros((N, d), dtype=np.float64)
+    dW = np.zeros((V, d), dtype=np.float64)
+    rows = np.nonzero(active)[0]
+    if rows.size:
+        x = lmhead_logits(h[rows], W)
+        dz = selected_logprob_backward(x, t[rows], None, T, lse[rows], g[rows])
+        dh[rows] = dz @ W
+        dW = dz.T @ h[rows]
+    return dh, dW
