@@ -1,0 +1,184 @@
+/*
+ * slp.h - selected-token log-probabilities over a large vocabulary, on one
+ * NVIDIA GB300 (sm_103a).  C ABI of libslp.so.
+ *
+ * For every row n of a logits matrix x[N, V], with target token t[n] and
+ * temperature T:
+ *
+ *     logprob[n] = x[n, t_n] / T - logsumexp_v( x[n, v] / T )
+ *     lse[n]     = logsumexp_v( x[n, v] / T )
+ *
+ * which is -cross_entropy(x / T, t) at label smoothing 0 (Megatron-LM issue
+ * #6700 "Avoid full-vocabulary TP gather for selected-token logprobs",
+ * "Proposed solution").  The backward pass writes
+ *
+ *     grad_x[n, v] = grad_out[n] * (1[v == t_n] - exp(x[n, v] / T - lse[n])) / T
+ *
+ * recomputing the softmax from x and the saved lse instead of keeping a float32
+ * [N, V] buffer (NeMo-RL PR #4222 "chunk target logprobs without tensor
+ * parallelism", "Changes"; verl PR #7733 "memory-efficient chunked top-k KL",
+ * "Design & Code Changes").  A second pair of calls fuses the LM-head
+ * projection x = h W^T with the same log-sum-exp, computing only rows whose
+ * loss mask is 1 (slime issue #2253 "full-vocab fp32 logits over the packed
+ * sequence -> OOM", maintainer analysis), so the logits are never stored.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - All array arguments are DEVICE pointers on the current CUDA device,
+ *    allocated and owned by the caller.  The library allocates no device
+ *    memory, keeps no pointer after a call returns and never synchronises:
+ *    every kernel is enqueued on `stream` (a cudaStream_t passed as void*;
+ *    NULL = the legacy default stream), so results are ready when the stream
+ *    reaches that point.  The calls contain no host-device synchronisation and
+ *    no allocation, so they may be captured in a CUDA graph.
+ *  - Matrices are row-major.  `ld` is the row stride in elements (ld >= V).
+ *  - Outputs are overwritten, never accumulated into.
+ *  - `mask` is optional (NULL = every row active).  mask[n] == 0 makes row n
+ *    inactive: its logprob and lse are +0.0 and its gradient row is +0.0,
+ *    bit for bit (Megatron-LM issue #6700, "Prototype correctness": masked
+ *    positions have exactly zero gradient).
+ *  - Argument errors are reported synchronously by the return value, before
+ *    anything is launched.  N == 0 is a successful no-op.
+ *  - Data errors are found on the device: a target outside [0, V) on an
+ *    active row ORs SLP_DATA_ERR_TARGET into *err (when err is not NULL) and
+ *    makes that row's outputs NaN.  No kernel traps or asserts.
+ *  - All offsets are 64-bit (N * ld may exceed 2^32).
+ */
+#ifndef SLP_H_
+#define SLP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type of the logits (and of their gradient). */
+typedef enum { SLP_BF16 = 0, SLP_F32 = 1 } slp_dtype;
+
+/* Return values. */
+typedef enum {
+  SLP_OK = 0,
+  SLP_ERR_INVALID_ARG = 1, /* NULL required pointer, N < 0, V <= 0, ld < V,
+                              T not finite or <= 0, unknown dtype, ...      */
+  SLP_ERR_UNSUPPORTED = 2, /* shape the kernels do not handle (see per call) */
+  SLP_ERR_MISALIGNED = 3,  /* pointer/stride alignment the call requires    */
+  SLP_ERR_WORKSPACE = 4,   /* workspace NULL or smaller than required       */
+  SLP_ERR_CUDA = 5         /* a CUDA runtime call or launch failed          */
+} slp_status;
+
+/* Bits OR-ed into the optional device error word. */
+#define SLP_DATA_ERR_TARGET 1 /* target outside [0, V) on an active row */
+
+/*
+ * slp_forward - selected-token log-probability and row log-sum-exp.
+ *
+ * Defined by: Megatron-LM issue #6700, "Proposed solution" (the identity with
+ * -cross_entropy, stable normalisation); torchforge PR #608 "Reduce reference
+ * model memory with parallel logprob computation", "Implementation" (max,
+ * sum of exp(x - max), target gather); NeMo-RL PR #4222, "Changes" (fp32
+ * log-sum-exp over low-precision logits that are never upcast as a whole).
+ *
+ *   x        [N, ld] logits of type `dtype` (bf16 or f32); columns >= V unread.
+ *   dtype    SLP_BF16 or SLP_F32.
+ *   N, V, ld rows, vocabulary size, row stride in elements (ld >= V).
+ *   t        [N] int32 targets.
+ *   mask     [N] uint8 loss mask or NULL.
+ *   T        temperature, finite and > 0.
+ *   logprob  [N] float32 out.
+ *   lse      [N] float32 out: log-sum-exp of x / T (kept for slp_backward).
+ *   err      optional int32 device error word (only ever OR-ed into).
+ *   stream   cudaStream_t.
+ *
+ * Any ld and alignment is accepted; rows whose base address is 16-byte
+ * aligned (x aligned and ld * sizeof(element) a multiple of 16) take the
+ * 128-bit vector path.  An all -inf row gives NaN; a target on a -inf column
+ * gives logprob = -inf.
+ */
+int slp_forward(const void* x, int dtype, int64_t N, int64_t V, int64_t ld,
+                const int32_t* t, const uint8_t* mask, float T,
+                float* logprob, float* lse, int32_t* err, void* stream);
+
+/*
+ * slp_backward - gradient of sum_n grad_out[n] * logprob[n] w.r.t. x.
+ *
+ * Defined by: NeMo-RL PR #4222, "Changes" ((onehot - softmax) * grad_output
+ * written into a buffer of the logits' dtype, softmax recomputed); verl PR
+ * #7733, "Design & Code Changes" (recompute from the saved per-token fp32
+ * logZ).  The factor 1/T is the derivative of x / T.
+ *
+ *   x, dtype, N, V, ld, t, mask, T   as for slp_forward (same values).
+ *   lse       [N] float32, as returned by slp_forward.
+ *   grad_out  [N] float32 upstream gradient of logprob.
+ *   grad_x    [N, ld_grad] out, same element type as x; columns >= V are not
+ *             written.  Float32 arithmetic, rounded to nearest-even into bf16.
+ *   ld_grad   row stride of grad_x in elements (>= V).
+ *   err       optional device error word.
+ */
+int slp_backward(const void* x, int dtype, int64_t N, int64_t V, int64_t ld,
+                 const int32_t* t, const uint8_t* mask, float T,
+                 const float* lse, const float* grad_out,
+                 void* grad_x, int64_t ld_grad, int32_t* err, void* stream);
+
+/*
+ * slp_lmhead_workspace_size - bytes of device workspace that
+ * slp_lmhead_forward and slp_lmhead_backward need for these sizes (the same
+ * value serves both; a larger workspace is fine).  Returns 0 for invalid sizes.
+ */
+size_t slp_lmhead_workspace_size(int64_t N, int64_t V, int64_t d);
+
+/*
+ * slp_lmhead_forward - selected-token log-probabilities through the LM head,
+ * logits never stored.
+ *
+ * Defined by: the slp_forward definition applied to x = h W^T (no bias),
+ * computing only rows with mask[n] != 0 before the vocabulary projection and
+ * scattering the per-row scalars back (slime issue #2253, maintainer
+ * analysis); Megatron-LM issue #6700, "Alternatives considered" (a fused
+ * LM-head / cross-entropy kernel).
+ *
+ *   h        [N, d] bf16 hidden states, row-major, 16-byte aligned.
+ *   W        [V, d] bf16 output embedding, row-major, 16-byte aligned.
+ *   N, V, d  d must be a positive multiple of 64.
+ *   t, mask, T, logprob, lse, err, stream   as for slp_forward.  The logits
+ *            are accumulated in float32 and not rounded before the
+ *            log-sum-exp.
+ *   ws, ws_bytes  device workspace of at least
+ *            slp_lmhead_workspace_size(N, V, d) bytes, 256-byte aligned;
+ *            its contents on entry do not matter.
+ */
+int slp_lmhead_forward(const void* h, const void* W, int64_t N, int64_t V, int64_t d,
+                       const int32_t* t, const uint8_t* mask, float T,
+                       float* logprob, float* lse,
+                       void* ws, size_t ws_bytes, int32_t* err, void* stream);
+
+/*
+ * slp_lmhead_backward - gradients of sum_n grad_out[n] * logprob[n] with
+ * respect to h and W for the fused LM head.
+ *
+ *   dz[n, v] = grad_out[n] * (1[v == t_n] - exp(z[n, v] - lse[n])) / T with
+ *   z = h W^T / T recomputed from the saved lse (as for slp_backward);
+ *   dh = dz W and dW = dz^T h over the active rows, float32 accumulation,
+ *   rounded to nearest-even into bf16.  Inactive rows of dh are +0.0.
+ *
+ *   h, W, N, V, d, t, mask, T   as for slp_lmhead_forward (same values).
+ *   lse       [N] float32 from slp_lmhead_forward.
+ *   grad_out  [N] float32.
+ *   dh        [N, d] bf16 out.      dW  [V, d] bf16 out (overwritten).
+ *   ws, ws_bytes, err, stream   as for slp_lmhead_forward.
+ */
+int slp_lmhead_backward(const void* h, const void* W, int64_t N, int64_t V, int64_t d,
+                        const int32_t* t, const uint8_t* mask, float T,
+                        const float* lse, const float* grad_out,
+                        void* dh, void* dW,
+                        void* ws, size_t ws_bytes, int32_t* err, void* stream);
+
+/* Static, human-readable text for a slp_status value. */
+const char* slp_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SLP_H_ */

@@ -1,0 +1,119 @@
+"""CPU-only: the C-ABI library loads, exports every function include/slp.h
+declares, and rejects bad arguments before touching the device."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from vocab_selected_token_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))
+           if f.endswith(".h")]
+
+
+def declared_functions():
+    names = set()
+    for h in HEADERS:
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\**\s+\**\s*(slp_\w+)\s*\(",
+                             src, flags=re.M):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from vocab_selected_token_gb300 import build
+    build.build()
+    return _lib.load()
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("slp_forward", "slp_backward", "slp_lmhead_workspace_size",
+              "slp_lmhead_forward", "slp_lmhead_backward", "slp_status_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+        assert n in _lib.SIGNATURES, f"{n} has no ctypes signature"
+
+
+def test_status_strings(lib):
+    assert _lib.status_string(0) == "ok"
+    assert "invalid" in _lib.status_string(1)
+    assert _lib.status_string(99) == "unknown status"
+
+
+FAKE = ctypes.c_void_p(0x1000)  # never dereferenced: validation fails first
+
+
+@pytest.mark.parametrize("args,expect", [
+    # (x, dtype, N, V, ld, t, mask, T, lp, lse, err, stream)
+    ((FAKE, 0, -1, 10, 10, FAKE, None, 1.0, FAKE, FAKE, None, None), _lib.SLP_ERR_INVALID_ARG),
+    ((FAKE, 0, 4, 0, 10, FAKE, None, 1.0, FAKE, FAKE, None, None), _lib.SLP_ERR_INVALID_ARG),
+    ((FAKE, 0, 4, 10, 9, FAKE, None, 1.0, FAKE, FAKE, None, None), _lib.SLP_ERR_INVALID_ARG),
+    ((FAKE, 7, 4, 10, 10, FAKE, None, 1.0, FAKE, FAKE, None, None), _lib.SLP_ERR_INVALID_ARG),
+    ((FAKE, 0, 4, 10, 10, FAKE, None, 0.0, FAKE, FAKE, None, None), _lib.SLP_ERR_INVALID_ARG),
+    ((FAKE, 0, 4, 10, 10, FAKE, None, float("nan"), FAKE, FAKE, None, None), _lib.SLP_ERR_INVALID_ARG),
+    ((FAKE, 0, 4, 10, 10, FAKE, None, float("inf"), FAKE, FAKE, None, None), _lib.SLP_ERR_INVALID_ARG),
+    ((None, 0, 4, 10, 10, FAKE, None, 1.0, FAKE, FAKE, None, None), _lib.SLP_ERR_INVALID_ARG),
+    ((FAKE, 0, 4, 10, 10, None, None, 1.0, FAKE, FAKE, None, None), _lib.SLP_ERR_INVALID_ARG),
+    ((FAKE, 0, 4, 10, 10, FAKE, None, 1.0, None, FAKE, None, None), _lib.SLP_ERR_INVALID_ARG),
+    ((None, 0, 0, 10, 10, None, None, 1.0, None, None, None, None), _lib.SLP_OK),  # N = 0: no-op
+])
+def test_forward_argument_errors(lib, args, expect):
+    assert lib.slp_forward(*args) == expect
+
+
+def test_backward_argument_errors(lib):
+    # ld_grad < V
+    assert lib.slp_backward(FAKE, 0, 4, 10, 10, FAKE, None, 1.0, FAKE, FAKE, FAKE, 9, None,
+                            None) == _lib.SLP_ERR_INVALID_ARG
+    # missing lse
+    assert lib.slp_backward(FAKE, 0, 4, 10, 10, FAKE, None, 1.0, None, FAKE, FAKE, 10, None,
+                            None) == _lib.SLP_ERR_INVALID_ARG
+    assert lib.slp_backward(None, 1, 0, 10, 10, None, None, 1.0, None, None, None, 10, None,
+                            None) == _lib.SLP_OK
+
+
+def test_lmhead_argument_errors(lib):
+    N, V, d = 64, 1000, 128
+    need = lib.slp_lmhead_workspace_size(N, V, d)
+    assert need > 0
+    assert lib.slp_lmhead_workspace_size(-1, V, d) == 0
+    f = lib.slp_lmhead_forward
+    # d not a multiple of 64
+    assert f(FAKE, FAKE, N, V, 100, FAKE, None, 1.0, FAKE, FAKE, FAKE, 1 << 40, None,
+             None) == _lib.SLP_ERR_UNSUPPORTED
+    # misaligned h
+    assert f(ctypes.c_void_p(0x1008), FAKE, N, V, d, FAKE, None, 1.0, FAKE, FAKE, FAKE, need,
+             None, None) == _lib.SLP_ERR_MISALIGNED
+    # workspace too small / missing
+    assert f(FAKE, FAKE, N, V, d, FAKE, None, 1.0, FAKE, FAKE, FAKE, need - 1, None,
+             None) == _lib.SLP_ERR_WORKSPACE
+    assert f(FAKE, FAKE, N, V, d, FAKE, None, 1.0, FAKE, FAKE, None, need, None,
+             None) == _lib.SLP_ERR_WORKSPACE
+    # bad temperature
+    assert f(FAKE, FAKE, N, V, d, FAKE, None, -1.0, FAKE, FAKE, FAKE, need, None,
+             None) == _lib.SLP_ERR_INVALID_ARG
+    b = lib.slp_lmhead_backward
+    assert b(FAKE, FAKE, N, V, d, FAKE, None, 1.0, FAKE, FAKE, None, FAKE, FAKE, need, None,
+             None) == _lib.SLP_ERR_INVALID_ARG
+    assert b(FAKE, FAKE, N, V, d, FAKE, None, 1.0, FAKE, FAKE, ctypes.c_void_p(0x1002), FAKE,
+             FAKE, need, None, None) == _lib.SLP_ERR_MISALIGNED
+
+
+def test_product_path_has_no_oracle_import():
+    pkg = os.path.join(ROOT, "vocab_selected_token_gb300")
+    pat = re.compile(r"^\s*(from|import)\s+(\.\.)?oracle\b|slp_oracle", re.M)
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                assert not pat.search(open(os.path.join(dirpath, f)).read()), f

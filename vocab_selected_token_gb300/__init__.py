@@ -1,0 +1,202 @@
+"""Selected-token log-probabilities over a large vocabulary on one GB300.
+
+Thin binding over the C ABI of ``libslp.so`` (``include/slp.h``): the
+functions below only check tensor properties, allocate outputs with torch
+when the caller passes none, and hand raw device pointers plus the current
+CUDA stream to the library.  Every step of the computation runs in the
+library's CUDA kernels; there is no CPU or PyTorch fallback.
+
+    logprob[n] = x[n, t_n] / T - logsumexp_v(x[n, v] / T)
+
+Low level (same names and arguments as the C ABI):
+    slp_forward, slp_backward, slp_lmhead_workspace_size,
+    slp_lmhead_forward, slp_lmhead_backward
+Autograd:
+    selected_logprob(x, t, mask=None, temperature=1.0)
+    lmhead_selected_logprob(h, W, t, mask=None, temperature=1.0)
+"""
+
+from __future__ import annotations
+
+import torch
+
+from . import _lib
+from ._lib import SlpError
+
+__all__ = [
+    "SlpError", "slp_forward", "slp_backward", "slp_lmhead_workspace_size",
+    "slp_lmhead_forward", "slp_lmhead_backward", "selected_logprob",
+    "lmhead_selected_logprob", "library_path",
+]
+
+_DTYPES = {torch.bfloat16: _lib.SLP_BF16, torch.float32: _lib.SLP_F32}
+
+
+def library_path() -> str:
+    _lib.load()
+    return _lib.LIB_PATH
+
+
+def _stream_handle(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _check_vec(name, v, N, dtype):
+    if v.dim() != 1 or v.shape[0] != N or v.dtype != dtype or not v.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous [{N}] {dtype} tensor")
+    return v
+
+
+def _logits_layout(x):
+    if x.dim() != 2 or x.dtype not in _DTYPES:
+        raise ValueError("x must be a 2-D bfloat16 or float32 tensor")
+    if not x.is_cuda:
+        raise ValueError("x must be a CUDA tensor")
+    N, V = x.shape
+    if N > 0 and V > 0 and x.stride(1) != 1:
+        raise ValueError("x must have unit column stride")
+    ld = x.stride(0) if N > 1 else max(V, 1)
+    return N, V, ld
+
+
+def slp_forward(x, t, mask=None, T: float = 1.0, logprob=None, lse=None, err=None, stream=None):
+    """Forward of the logits-input path.  Returns (logprob[N], lse[N]), float32."""
+    N, V, ld = _logits_layout(x)
+    _check_vec("t", t, N, torch.int32)
+    if mask is not None:
+        _check_vec("mask", mask, N, torch.uint8)
+    if logprob is None:
+        logprob = torch.empty(N, dtype=torch.float32, device=x.device)
+    if lse is None:
+        lse = torch.empty(N, dtype=torch.float32, device=x.device)
+    _check_vec("logprob", logprob, N, torch.float32)
+    _check_vec("lse", lse, N, torch.float32)
+    _lib.call("slp_forward", _ptr(x), _DTYPES[x.dtype], N, V, ld, _ptr(t), _ptr(mask), float(T),
+              _ptr(logprob), _ptr(lse), _ptr(err), _stream_handle(stream))
+    return logprob, lse
+
+
+def slp_backward(x, t, mask, T: float, lse, grad_out, grad_x=None, err=None, stream=None):
+    """Backward of the logits-input path.  Returns grad_x [N, V] (x's dtype)."""
+    N, V, ld = _logits_layout(x)
+    _check_vec("t", t, N, torch.int32)
+    if mask is not None:
+        _check_vec("mask", mask, N, torch.uint8)
+    _check_vec("lse", lse, N, torch.float32)
+    _check_vec("grad_out", grad_out, N, torch.float32)
+    if grad_x is None:
+        grad_x = torch.empty((N, V), dtype=x.dtype, device=x.device)
+    if grad_x.shape != (N, V) or grad_x.dtype != x.dtype or (N > 0 and V > 0 and grad_x.stride(1) != 1):
+        raise ValueError("grad_x must be [N, V] with x's dtype and unit column stride")
+    ldg = grad_x.stride(0) if N > 1 else max(V, 1)
+    _lib.call("slp_backward", _ptr(x), _DTYPES[x.dtype], N, V, ld, _ptr(t), _ptr(mask), float(T),
+              _ptr(lse), _ptr(grad_out), _ptr(grad_x), ldg, _ptr(err), _stream_handle(stream))
+    return grad_x
+
+
+def slp_lmhead_workspace_size(N: int, V: int, d: int) -> int:
+    return int(_lib.load().slp_lmhead_workspace_size(int(N), int(V), int(d)))
+
+
+def _lmhead_check(h, W):
+    if h.dim() != 2 or W.dim() != 2 or h.dtype != torch.bfloat16 or W.dtype != torch.bfloat16:
+        raise ValueError("h [N, d] and W [V, d] must be bfloat16 matrices")
+    if not (h.is_contiguous() and W.is_contiguous()) or h.shape[1] != W.shape[1]:
+        raise ValueError("h and W must be contiguous with the same inner size d")
+    return h.shape[0], W.shape[0], h.shape[1]
+
+
+def _workspace(N, V, d, ws, device):
+    need = slp_lmhead_workspace_size(N, V, d)
+    if ws is None:
+        ws = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
+    return ws, ws.numel()
+
+
+def slp_lmhead_forward(h, W, t, mask=None, T: float = 1.0, logprob=None, lse=None, ws=None,
+                       err=None, stream=None):
+    """Fused LM-head forward.  Returns (logprob[N], lse[N]), float32."""
+    N, V, d = _lmhead_check(h, W)
+    _check_vec("t", t, N, torch.int32)
+    if mask is not None:
+        _check_vec("mask", mask, N, torch.uint8)
+    if logprob is None:
+        logprob = torch.empty(N, dtype=torch.float32, device=h.device)
+    if lse is None:
+        lse = torch.empty(N, dtype=torch.float32, device=h.device)
+    ws, nbytes = _workspace(N, V, d, ws, h.device)
+    _lib.call("slp_lmhead_forward", _ptr(h), _ptr(W), N, V, d, _ptr(t), _ptr(mask), float(T),
+              _ptr(logprob), _ptr(lse), _ptr(ws), nbytes, _ptr(err), _stream_handle(stream))
+    return logprob, lse
+
+
+def slp_lmhead_backward(h, W, t, mask, T: float, lse, grad_out, dh=None, dW=None, ws=None,
+                        err=None, stream=None):
+    """Fused LM-head backward.  Returns (dh [N, d], dW [V, d]), bfloat16."""
+    N, V, d = _lmhead_check(h, W)
+    _check_vec("t", t, N, torch.int32)
+    if mask is not None:
+        _check_vec("mask", mask, N, torch.uint8)
+    _check_vec("lse", lse, N, torch.float32)
+    _check_vec("grad_out", grad_out, N, torch.float32)
+    if dh is None:
+        dh = torch.empty((N, d), dtype=torch.bfloat16, device=h.device)
+    if dW is None:
+        dW = torch.empty((V, d), dtype=torch.bfloat16, device=h.device)
+    ws, nbytes = _workspace(N, V, d, ws, h.device)
+    _lib.call("slp_lmhead_backward", _ptr(h), _ptr(W), N, V, d, _ptr(t), _ptr(mask), float(T),
+              _ptr(lse), _ptr(grad_out), _ptr(dh), _ptr(dW), _ptr(ws), nbytes, _ptr(err),
+              _stream_handle(stream))
+    return dh, dW
+
+
+class _SelectedLogprob(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, x, t, mask, T):
+        lp, lse = slp_forward(x, t, mask, T)
+        ctx.save_for_backward(x, t, mask, lse)
+        ctx.T = T
+        ctx.mark_non_differentiable(lse)
+        return lp, lse
+
+    @staticmethod
+    def backward(ctx, g, _g_lse):
+        x, t, mask, lse = ctx.saved_tensors
+        gx = slp_backward(x, t, mask, ctx.T, lse, g.float().contiguous())
+        return gx, None, None, None
+
+
+def selected_logprob(x, t, mask=None, temperature: float = 1.0):
+    """logprob[N] = log_softmax(x / T)[n, t_n] with an autograd backward that
+    recomputes the softmax from x and the saved lse (no [N, V] float buffer).
+    Rows with mask == 0 give 0 and a zero gradient."""
+    lp, _ = _SelectedLogprob.apply(x, t, mask, float(temperature))
+    return lp
+
+
+class _LMHeadSelectedLogprob(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, h, W, t, mask, T):
+        lp, lse = slp_lmhead_forward(h, W, t, mask, T)
+        ctx.save_for_backward(h, W, t, mask, lse)
+        ctx.T = T
+        ctx.mark_non_differentiable(lse)
+        return lp, lse
+
+    @staticmethod
+    def backward(ctx, g, _g_lse):
+        h, W, t, mask, lse = ctx.saved_tensors
+        dh, dW = slp_lmhead_backward(h, W, t, mask, ctx.T, lse, g.float().contiguous())
+        return dh, dW, None, None, None
+
+
+def lmhead_selected_logprob(h, W, t, mask=None, temperature: float = 1.0):
+    """Selected-token log-probabilities of the logits h W^T / T without storing
+    them; only rows with mask != 0 are projected."""
+    lp, _ = _LMHeadSelectedLogprob.apply(h, W, t, mask, float(temperature))
+    return lp

@@ -1,0 +1,128 @@
+// C-ABI entry points of libslp: argument validation (before any CUDA call, so
+// argument errors are reported without touching the device), then the kernel
+// launchers.  The library allocates nothing and never synchronises.
+
+#include "slp.h"
+#include "slp_internal.h"
+
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+namespace slp {
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 152;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+}  // namespace slp
+
+namespace {
+
+bool temperature_ok(float T) { return isfinite(T) && T > 0.f; }
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? SLP_OK : SLP_ERR_CUDA; }
+
+int check_logits_args(const void* x, int dtype, int64_t N, int64_t V, int64_t ld,
+                      const int32_t* t, float T) {
+  if (dtype != SLP_BF16 && dtype != SLP_F32) return SLP_ERR_INVALID_ARG;
+  if (N < 0 || V <= 0 || ld < V || V > INT32_MAX) return SLP_ERR_INVALID_ARG;
+  if (!temperature_ok(T)) return SLP_ERR_INVALID_ARG;
+  if (N > 0 && (x == nullptr || t == nullptr)) return SLP_ERR_INVALID_ARG;
+  return SLP_OK;
+}
+
+int check_lmhead_args(const void* h, const void* W, int64_t N, int64_t V, int64_t d,
+                      const int32_t* t, float T, void* ws, size_t ws_bytes) {
+  if (N < 0 || V <= 0 || d <= 0 || V > INT32_MAX || N > INT32_MAX) return SLP_ERR_INVALID_ARG;
+  if (!temperature_ok(T)) return SLP_ERR_INVALID_ARG;
+  if (N == 0) return SLP_OK;
+  if (h == nullptr || W == nullptr || t == nullptr) return SLP_ERR_INVALID_ARG;
+  if (d % 64 != 0) return SLP_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(h) & 15u) || (reinterpret_cast<uintptr_t>(W) & 15u))
+    return SLP_ERR_MISALIGNED;
+  if (ws == nullptr || ws_bytes < slp::lmhead_workspace_size(N, V, d)) return SLP_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(ws) & 255u) return SLP_ERR_MISALIGNED;
+  return SLP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int slp_forward(const void* x, int dtype, int64_t N, int64_t V, int64_t ld, const int32_t* t,
+                const uint8_t* mask, float T, float* logprob, float* lse, int32_t* err,
+                void* stream) {
+  int st = check_logits_args(x, dtype, N, V, ld, t, T);
+  if (st != SLP_OK) return st;
+  if (N == 0) return SLP_OK;
+  if (logprob == nullptr || lse == nullptr) return SLP_ERR_INVALID_ARG;
+  return cuda_status(slp::launch_forward(x, dtype, N, V, ld, t, mask, T, logprob, lse, err,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+int slp_backward(const void* x, int dtype, int64_t N, int64_t V, int64_t ld, const int32_t* t,
+                 const uint8_t* mask, float T, const float* lse, const float* grad_out,
+                 void* grad_x, int64_t ld_grad, int32_t* err, void* stream) {
+  int st = check_logits_args(x, dtype, N, V, ld, t, T);
+  if (st != SLP_OK) return st;
+  if (ld_grad < V) return SLP_ERR_INVALID_ARG;
+  if (N == 0) return SLP_OK;
+  if (lse == nullptr || grad_out == nullptr || grad_x == nullptr) return SLP_ERR_INVALID_ARG;
+  return cuda_status(slp::launch_backward(x, dtype, N, V, ld, t, mask, T, lse, grad_out, grad_x,
+                                          ld_grad, err, static_cast<cudaStream_t>(stream)));
+}
+
+size_t slp_lmhead_workspace_size(int64_t N, int64_t V, int64_t d) {
+  if (N < 0 || V <= 0 || d <= 0 || V > INT32_MAX || N > INT32_MAX) return 0;
+  return slp::lmhead_workspace_size(N, V, d);
+}
+
+int slp_lmhead_forward(const void* h, const void* W, int64_t N, int64_t V, int64_t d,
+                       const int32_t* t, const uint8_t* mask, float T, float* logprob,
+                       float* lse, void* ws, size_t ws_bytes, int32_t* err, void* stream) {
+  int st = check_lmhead_args(h, W, N, V, d, t, T, ws, ws_bytes);
+  if (st != SLP_OK) return st;
+  if (N == 0) return SLP_OK;
+  if (logprob == nullptr || lse == nullptr) return SLP_ERR_INVALID_ARG;
+  return cuda_status(slp::launch_lmhead_forward(h, W, N, V, d, t, mask, T, logprob, lse, ws, err,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
+int slp_lmhead_backward(const void* h, const void* W, int64_t N, int64_t V, int64_t d,
+                        const int32_t* t, const uint8_t* mask, float T, const float* lse,
+                        const float* grad_out, void* dh, void* dW, void* ws, size_t ws_bytes,
+                        int32_t* err, void* stream) {
+  int st = check_lmhead_args(h, W, N, V, d, t, T, ws, ws_bytes);
+  if (st != SLP_OK) return st;
+  if (N == 0) return SLP_OK;
+  if (lse == nullptr || grad_out == nullptr || dh == nullptr || dW == nullptr)
+    return SLP_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(dh) & 15u) || (reinterpret_cast<uintptr_t>(dW) & 15u))
+    return SLP_ERR_MISALIGNED;
+  return cuda_status(slp::launch_lmhead_backward(h, W, N, V, d, t, mask, T, lse, grad_out, dh,
+                                                 dW, ws, err, static_cast<cudaStream_t>(stream)));
+}
+
+const char* slp_status_string(int status) {
+  switch (status) {
+    case SLP_OK: return "ok";
+    case SLP_ERR_INVALID_ARG: return "invalid argument";
+    case SLP_ERR_UNSUPPORTED: return "unsupported shape";
+    case SLP_ERR_MISALIGNED: return "misaligned pointer or stride";
+    case SLP_ERR_WORKSPACE: return "workspace missing or too small";
+    case SLP_ERR_CUDA: return "CUDA runtime error";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

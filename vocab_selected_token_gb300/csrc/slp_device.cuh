@@ -1,0 +1,151 @@
+// Device-side helpers shared by the libslp kernels (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace slp {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Hardware base-2 exponential (MUFU.EX2); subnormal results flush to zero,
+// ex2(-inf) = 0.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// 128-bit streaming load: read once, do not keep in L1.
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 r;
+  asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p));
+  return r;
+}
+
+// 128-bit streaming store (evict-first).
+__device__ __forceinline__ void st_stream(void* p, const uint4& v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// Element traits: how many elements a 16-byte vector holds, how to widen them.
+template <typename Elt>
+struct Elem;
+
+template <>
+struct Elem<__nv_bfloat16> {
+  static constexpr int kVec = 8;
+  static constexpr uint32_t kNegInfWord = 0xFF80FF80u;  // two bf16 -inf
+  __device__ static __forceinline__ void unpack(const uint4& v, float (&f)[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = __uint_as_float(w[i] << 16);
+      f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  }
+  __device__ static __forceinline__ uint4 pack(const float (&f)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __nv_bfloat162 b = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+      w[i] = *reinterpret_cast<uint32_t*>(&b);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  __device__ static __forceinline__ float load1(const __nv_bfloat16* p) {
+    return __bfloat162float(*p);
+  }
+  __device__ static __forceinline__ void store1(__nv_bfloat16* p, float v) {
+    *p = __float2bfloat16_rn(v);
+  }
+};
+
+template <>
+struct Elem<float> {
+  static constexpr int kVec = 4;
+  static constexpr uint32_t kNegInfWord = 0xFF800000u;
+  __device__ static __forceinline__ void unpack(const uint4& v, float (&f)[4]) {
+    f[0] = __uint_as_float(v.x);
+    f[1] = __uint_as_float(v.y);
+    f[2] = __uint_as_float(v.z);
+    f[3] = __uint_as_float(v.w);
+  }
+  __device__ static __forceinline__ uint4 pack(const float (&f)[4]) {
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                      __float_as_uint(f[3]));
+  }
+  __device__ static __forceinline__ float load1(const float* p) { return *p; }
+  __device__ static __forceinline__ void store1(float* p, float v) { *p = v; }
+};
+
+// Running log-sum-exp state of a set of logits, kept in base 2.
+//   m  : the largest raw logit seen (-inf when none),
+//   mc : m * c rounded to float (c = log2(e) / T), the offset actually used,
+//   s  : sum of 2^(x*c - mc) over the set.
+// mc is a fixed function of m, so two states with the same m carry the same
+// offset and merge exactly.
+struct Lse2 {
+  float m, mc, s;
+};
+
+__device__ __forceinline__ Lse2 lse2_empty() { return Lse2{-INFINITY, -INFINITY, 0.f}; }
+
+// Merge b into a.  Empty states (m == -inf, s == 0) are neutral, so an all
+// -inf segment never produces -inf - -inf.
+__device__ __forceinline__ Lse2 lse2_merge(Lse2 a, Lse2 b) {
+  if (b.m > a.m) {
+    a.s = a.s * ex2(a.mc - b.mc) + b.s;  // ex2(-inf) = 0 when a is empty
+    a.m = b.m;
+    a.mc = b.mc;
+  } else if (b.m != -INFINITY) {
+    a.s = a.s + b.s * ex2(b.mc - a.mc);
+  }
+  return a;
+}
+
+__device__ __forceinline__ Lse2 lse2_shfl_xor(Lse2 v, int lane_mask) {
+  Lse2 o;
+  o.m = __shfl_xor_sync(0xFFFFFFFFu, v.m, lane_mask);
+  o.mc = __shfl_xor_sync(0xFFFFFFFFu, v.mc, lane_mask);
+  o.s = __shfl_xor_sync(0xFFFFFFFFu, v.s, lane_mask);
+  return o;
+}
+
+// Butterfly merge across the warp; every lane ends with the same state.
+// The merge order is fixed, so results are bitwise reproducible.
+__device__ __forceinline__ Lse2 lse2_warp_reduce(Lse2 v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = lse2_merge(v, lse2_shfl_xor(v, o));
+  return v;
+}
+
+// ---- thread-block cluster helpers (distributed shared memory) --------------
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release;\n\t"
+               "barrier.cluster.wait.acquire;" ::
+                   : "memory");
+}
+
+// Address of `smem_ptr` in the shared memory of CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t map_shared_rank(const void* smem_ptr, uint32_t rank) {
+  uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(smem_ptr));
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+}  // namespace slp

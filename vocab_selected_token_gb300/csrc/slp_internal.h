@@ -1,0 +1,37 @@
+// Internal interface between the C-ABI layer (slp_api.cu) and the kernel
+// launchers.  Arguments have been validated by the caller.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace slp {
+
+// Streaming multiprocessors of the current device (cached per device).
+int sm_count();
+
+// Logits-input path (slp_logits.cu).
+cudaError_t launch_forward(const void* x, int dtype, int64_t N, int64_t V, int64_t ld,
+                           const int32_t* t, const uint8_t* mask, float T, float* logprob,
+                           float* lse, int32_t* err, cudaStream_t stream);
+
+cudaError_t launch_backward(const void* x, int dtype, int64_t N, int64_t V, int64_t ld,
+                            const int32_t* t, const uint8_t* mask, float T, const float* lse,
+                            const float* grad_out, void* grad_x, int64_t ld_grad,
+                            int32_t* err, cudaStream_t stream);
+
+// Fused LM-head path (slp_lmhead.cu).
+size_t lmhead_workspace_size(int64_t N, int64_t V, int64_t d);
+
+cudaError_t launch_lmhead_forward(const void* h, const void* W, int64_t N, int64_t V, int64_t d,
+                                  const int32_t* t, const uint8_t* mask, float T,
+                                  float* logprob, float* lse, void* ws, int32_t* err,
+                                  cudaStream_t stream);
+
+cudaError_t launch_lmhead_backward(const void* h, const void* W, int64_t N, int64_t V, int64_t d,
+                                   const int32_t* t, const uint8_t* mask, float T,
+                                   const float* lse, const float* grad_out, void* dh, void* dW,
+                                   void* ws, int32_t* err, cudaStream_t stream);
+
+}  // namespace slp

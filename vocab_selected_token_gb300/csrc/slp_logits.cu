@@ -1,0 +1,358 @@
+// Logits-input path: forward (online log-sum-exp + target gather) and
+// backward ((onehot - softmax) * g / T with the softmax recomputed from the
+// saved lse), both streaming kernels bound by HBM bandwidth.
+//
+// Forward: one CTA (or a thread-block cluster of `splits` CTAs) per row.
+// Each thread streams 16-byte vectors with read-once loads and folds them into
+// a running base-2 (max, sum-exp) state; warps merge by butterfly shuffles,
+// CTAs of a cluster merge through distributed shared memory.  The cluster is
+// the single-GPU form of the vocabulary-parallel exchange (torchforge PR #608,
+// "Implementation": all-reduce MAX, all-reduce SUM of exp(x - max), target
+// gathered by its owner only), with no global workspace.
+//
+// Backward: a flat grid of (row, column-tile) CTAs; each thread handles
+// kBwdUnroll 16-byte vectors, recomputes p = 2^(x*c - lse*log2 e) and writes
+// g/T * (1[v == t] - p) with streaming stores.  Inactive rows only write zeros.
+
+#include "slp.h"
+#include "slp_device.cuh"
+#include "slp_internal.h"
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace slp {
+
+constexpr int kFwdThreads = 256;
+constexpr int kFwdUnroll = 4;  // 16-byte vectors in flight per thread per batch
+constexpr int kBwdThreads = 256;
+constexpr int kBwdUnroll = 4;
+constexpr int kMaxSplits = 8;  // portable cluster size
+
+// Fold K logits into the running state: one max over the batch, a rescale
+// only when the max grows, then K exponentials against the current offset.
+// Partial sums are kept per batch so the long running sum sees few additions.
+template <int K>
+__device__ __forceinline__ void lse2_fold(Lse2& st, const float* f, float c) {
+  float bm = f[0];
+#pragma unroll
+  for (int k = 1; k < K; ++k) bm = fmaxf(bm, f[k]);
+  if (bm > st.m) {
+    const float nmc = __fmul_rn(bm, c);  // rounded product: the stored offset
+    st.s *= ex2(st.mc - nmc);
+    st.m = bm;
+    st.mc = nmc;
+  }
+  if (st.m != -INFINITY) {
+    float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int k = 0; k < K; ++k) a[k & 3] += ex2(fmaf(f[k], c, -st.mc));
+    st.s += (a[0] + a[1]) + (a[2] + a[3]);
+  }
+}
+
+// Row result from the merged state.  ln sum_v exp((x_v - m)/T) is recovered
+// from the base-2 sum and the exact rounding residual of the offset.
+__device__ __forceinline__ void write_row_result(const Lse2& a, float xt, bool tvalid, float T,
+                                                 float c, float* logprob, float* lse,
+                                                 int32_t* err, int64_t row) {
+  float lp, l;
+  if (!tvalid) {
+    if (err) atomicOr(err, SLP_DATA_ERR_TARGET);
+    lp = l = __int_as_float(0x7FC00000);
+  } else if (!(a.s > 0.f) || a.m == -INFINITY) {
+    lp = l = __int_as_float(0x7FC00000);  // all -inf (or NaN) row
+  } else {
+    const float r = fmaf(a.m, c, -a.mc);  // m*c - mc, exact
+    const float ln_s = (log2f(a.s) - r) * kLn2;
+    l = a.m / T + ln_s;
+    lp = (xt - a.m) / T - ln_s;
+  }
+  logprob[row] = lp;
+  lse[row] = l;
+}
+
+template <typename Elt, bool kVecPath>
+__global__ void __launch_bounds__(kFwdThreads)
+    slp_fwd_kernel(const Elt* __restrict__ x, int64_t V, int64_t ld,
+                   const int32_t* __restrict__ t, const uint8_t* __restrict__ mask, float T,
+                   float c, float* __restrict__ logprob, float* __restrict__ lse,
+                   int32_t* __restrict__ err, int splits) {
+  using E = Elem<Elt>;
+  constexpr int kVec = E::kVec;
+  constexpr int kWarps = kFwdThreads / 32;
+  __shared__ Lse2 warp_part[kWarps];
+  __shared__ float cta_part[3];
+
+  const int64_t row = blockIdx.x / splits;
+  const int rank = static_cast<int>(blockIdx.x - row * splits);
+  // Every CTA of a cluster handles the same row, so all of them leave here
+  // together (no cluster barrier is left waiting).
+  if (mask != nullptr && mask[row] == 0) {
+    if (rank == 0 && threadIdx.x == 0) {
+      logprob[row] = 0.f;
+      lse[row] = 0.f;
+    }
+    return;
+  }
+  const Elt* xr = x + row * ld;
+  const int32_t tt = t[row];
+  const bool tvalid = tt >= 0 && static_cast<int64_t>(tt) < V;
+  float xt = 0.f;
+  if (rank == 0 && threadIdx.x == 0 && tvalid) xt = E::load1(xr + tt);
+
+  Lse2 st = lse2_empty();
+  if constexpr (kVecPath) {
+    const int64_t nvec = V / kVec;
+    const int64_t v0 = nvec * rank / splits;
+    const int64_t v1 = nvec * (rank + 1) / splits;
+    const uint4* p = reinterpret_cast<const uint4*>(xr) + v0;
+    const int64_t n = v1 - v0;
+    const uint4 pad = make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord, E::kNegInfWord);
+    for (int64_t i0 = threadIdx.x; i0 < n; i0 += kFwdThreads * kFwdUnroll) {
+      uint4 buf[kFwdUnroll];
+#pragma unroll
+      for (int u = 0; u < kFwdUnroll; ++u) {
+        const int64_t i = i0 + static_cast<int64_t>(u) * kFwdThreads;
+        buf[u] = (i < n) ? ld_stream(p + i) : pad;
+      }
+      float f[kFwdUnroll][kVec];
+#pragma unroll
+      for (int u = 0; u < kFwdUnroll; ++u) E::unpack(buf[u], f[u]);
+      lse2_fold<kFwdUnroll * kVec>(st, &f[0][0], c);
+    }
+    if (rank == splits - 1) {  // fewer than kVec trailing elements
+      const int64_t e = nvec * kVec + threadIdx.x;
+      if (e < V) {
+        float f1[1] = {E::load1(xr + e)};
+        lse2_fold<1>(st, f1, c);
+      }
+    }
+  } else {
+    const int64_t e0 = V * rank / splits;
+    const int64_t e1 = V * (rank + 1) / splits;
+    for (int64_t i0 = e0 + threadIdx.x; i0 < e1; i0 += kFwdThreads * 4) {
+      float f[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int64_t i = i0 + static_cast<int64_t>(u) * kFwdThreads;
+        f[u] = (i < e1) ? E::load1(xr + i) : -INFINITY;
+      }
+      lse2_fold<4>(st, f, c);
+    }
+  }
+
+  // CTA merge: warps, then the warp results in warp order.
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  st = lse2_warp_reduce(st);
+  if (lane == 0) warp_part[warp] = st;
+  __syncthreads();
+  if (warp == 0) {
+    Lse2 v = lane < kWarps ? warp_part[lane] : lse2_empty();
+    v = lse2_warp_reduce(v);
+    if (lane == 0) {
+      cta_part[0] = v.m;
+      cta_part[1] = v.mc;
+      cta_part[2] = v.s;
+      if (splits == 1) write_row_result(v, xt, tvalid, T, c, logprob, lse, err, row);
+    }
+  }
+  if (splits == 1) return;
+
+  // Cluster merge: CTA rank 0 reads the other ranks' states, in rank order,
+  // from their shared memory; the second barrier keeps every CTA resident
+  // until those reads are done.
+  cluster_sync_all();
+  if (rank == 0 && threadIdx.x == 0) {
+    Lse2 acc{cta_part[0], cta_part[1], cta_part[2]};
+    for (int r = 1; r < splits; ++r) {
+      Lse2 o;
+      o.m = ld_shared_cluster_f32(map_shared_rank(&cta_part[0], r));
+      o.mc = ld_shared_cluster_f32(map_shared_rank(&cta_part[1], r));
+      o.s = ld_shared_cluster_f32(map_shared_rank(&cta_part[2], r));
+      acc = lse2_merge(acc, o);
+    }
+    write_row_result(acc, xt, tvalid, T, c, logprob, lse, err, row);
+  }
+  cluster_sync_all();
+}
+
+template <typename Elt, bool kVecPath>
+__global__ void __launch_bounds__(kBwdThreads)
+    slp_bwd_kernel(const Elt* __restrict__ x, int64_t V, int64_t ld,
+                   const int32_t* __restrict__ t, const uint8_t* __restrict__ mask, float invT,
+                   float c, const float* __restrict__ lse, const float* __restrict__ g,
+                   Elt* __restrict__ gx, int64_t ldg, int32_t* __restrict__ err,
+                   int64_t tiles_per_row) {
+  using E = Elem<Elt>;
+  constexpr int kVec = E::kVec;
+  constexpr int64_t kTileElems = static_cast<int64_t>(kBwdThreads) * kBwdUnroll * kVec;
+
+  const int64_t row = blockIdx.x / tiles_per_row;
+  const int64_t tile = blockIdx.x - row * tiles_per_row;
+  const bool active = mask == nullptr || mask[row] != 0;
+  const Elt* xr = x + row * ld;
+  Elt* gr = gx + row * ldg;
+  const int64_t e_tile = tile * kTileElems;
+
+  float gT = 0.f, L2 = 0.f;
+  int64_t tt = -1;
+  if (active) {
+    tt = t[row];
+    gT = g[row] * invT;
+    L2 = lse[row] * kLog2e;
+    if (tt < 0 || tt >= V) {
+      if (err != nullptr && tile == 0 && threadIdx.x == 0) atomicOr(err, SLP_DATA_ERR_TARGET);
+      gT = __int_as_float(0x7FC00000);
+    }
+  }
+  const float a = -gT;
+
+  if constexpr (kVecPath) {
+    uint4* gv = reinterpret_cast<uint4*>(gr);
+    const uint4* xv = reinterpret_cast<const uint4*>(xr);
+    if (!active) {
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int u = 0; u < kBwdUnroll; ++u) {
+        const int64_t e = e_tile + (static_cast<int64_t>(u) * kBwdThreads + threadIdx.x) * kVec;
+        if (e + kVec <= V) {
+          st_stream(gv + e / kVec, z);
+        } else {
+          for (int64_t k = e; k < V; ++k) E::store1(gr + k, 0.f);
+        }
+      }
+      return;
+    }
+    uint4 buf[kBwdUnroll];
+#pragma unroll
+    for (int u = 0; u < kBwdUnroll; ++u) {
+      const int64_t e = e_tile + (static_cast<int64_t>(u) * kBwdThreads + threadIdx.x) * kVec;
+      if (e + kVec <= V) buf[u] = ld_stream(xv + e / kVec);
+    }
+#pragma unroll
+    for (int u = 0; u < kBwdUnroll; ++u) {
+      const int64_t e = e_tile + (static_cast<int64_t>(u) * kBwdThreads + threadIdx.x) * kVec;
+      if (e + kVec <= V) {
+        float f[kVec];
+        E::unpack(buf[u], f);
+        const int64_t rel = tt - e;
+#pragma unroll
+        for (int k = 0; k < kVec; ++k) {
+          const float p = ex2(fmaf(f[k], c, -L2));
+          f[k] = (rel == k) ? fmaf(a, p, gT) : a * p;
+        }
+        st_stream(gv + e / kVec, E::pack(f));
+      } else {
+        for (int64_t k = e; k < V; ++k) {
+          const float p = ex2(fmaf(E::load1(xr + k), c, -L2));
+          E::store1(gr + k, (k == tt) ? fmaf(a, p, gT) : a * p);
+        }
+      }
+    }
+  } else {
+    const int64_t e_end = min(V, e_tile + kTileElems);
+    for (int64_t e = e_tile + threadIdx.x; e < e_end; e += kBwdThreads) {
+      float out = 0.f;
+      if (active) {
+        const float p = ex2(fmaf(E::load1(xr + e), c, -L2));
+        out = (e == tt) ? fmaf(a, p, gT) : a * p;
+      }
+      E::store1(gr + e, out);
+    }
+  }
+}
+
+namespace {
+
+bool aligned16(const void* p, int64_t ld, int esize) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0 && ((ld * esize) & 15) == 0;
+}
+
+int choose_splits(int64_t N, int64_t V) {
+  // Aim for about four waves of eight resident CTAs per SM, but give every
+  // CTA at least 8K elements so the cluster merge stays negligible.
+  const int64_t want = static_cast<int64_t>(sm_count()) * 32;
+  int64_t s = (want + N - 1) / N;
+  const int64_t by_len = V / 8192;
+  if (s > by_len) s = by_len;
+  if (s > kMaxSplits) s = kMaxSplits;
+  if (s < 1) s = 1;
+  return static_cast<int>(s);
+}
+
+template <typename Elt>
+cudaError_t fwd_typed(const Elt* x, int64_t N, int64_t V, int64_t ld, const int32_t* t,
+                      const uint8_t* mask, float T, float* logprob, float* lse, int32_t* err,
+                      cudaStream_t stream) {
+  const int splits = choose_splits(N, V);
+  if (N * splits > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
+  const float c = static_cast<float>(1.4426950408889634 / static_cast<double>(T));
+  const bool vec = aligned16(x, ld, sizeof(Elt));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(N * splits), 1, 1);
+  cfg.blockDim = dim3(kFwdThreads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if (splits > 1) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(splits);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  if (vec)
+    return cudaLaunchKernelEx(&cfg, slp_fwd_kernel<Elt, true>, x, V, ld, t, mask, T, c, logprob,
+                              lse, err, splits);
+  return cudaLaunchKernelEx(&cfg, slp_fwd_kernel<Elt, false>, x, V, ld, t, mask, T, c, logprob,
+                            lse, err, splits);
+}
+
+template <typename Elt>
+cudaError_t bwd_typed(const Elt* x, int64_t N, int64_t V, int64_t ld, const int32_t* t,
+                      const uint8_t* mask, float T, const float* lse, const float* g, Elt* gx,
+                      int64_t ldg, int32_t* err, cudaStream_t stream) {
+  constexpr int64_t kTileElems =
+      static_cast<int64_t>(kBwdThreads) * kBwdUnroll * Elem<Elt>::kVec;
+  const int64_t tiles = (V + kTileElems - 1) / kTileElems;
+  const int64_t blocks = N * tiles;
+  if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
+  const float invT = 1.0f / T;
+  const float c = static_cast<float>(1.4426950408889634 / static_cast<double>(T));
+  const bool vec = aligned16(x, ld, sizeof(Elt)) && aligned16(gx, ldg, sizeof(Elt));
+  if (vec)
+    slp_bwd_kernel<Elt, true><<<static_cast<unsigned>(blocks), kBwdThreads, 0, stream>>>(
+        x, V, ld, t, mask, invT, c, lse, g, gx, ldg, err, tiles);
+  else
+    slp_bwd_kernel<Elt, false><<<static_cast<unsigned>(blocks), kBwdThreads, 0, stream>>>(
+        x, V, ld, t, mask, invT, c, lse, g, gx, ldg, err, tiles);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_forward(const void* x, int dtype, int64_t N, int64_t V, int64_t ld,
+                           const int32_t* t, const uint8_t* mask, float T, float* logprob,
+                           float* lse, int32_t* err, cudaStream_t stream) {
+  if (dtype == SLP_BF16)
+    return fwd_typed(static_cast<const __nv_bfloat16*>(x), N, V, ld, t, mask, T, logprob, lse,
+                     err, stream);
+  return fwd_typed(static_cast<const float*>(x), N, V, ld, t, mask, T, logprob, lse, err,
+                   stream);
+}
+
+cudaError_t launch_backward(const void* x, int dtype, int64_t N, int64_t V, int64_t ld,
+                            const int32_t* t, const uint8_t* mask, float T, const float* lse,
+                            const float* grad_out, void* grad_x, int64_t ld_grad,
+                            int32_t* err, cudaStream_t stream) {
+  if (dtype == SLP_BF16)
+    return bwd_typed(static_cast<const __nv_bfloat16*>(x), N, V, ld, t, mask, T, lse, grad_out,
+                     static_cast<__nv_bfloat16*>(grad_x), ld_grad, err, stream);
+  return bwd_typed(static_cast<const float*>(x), N, V, ld, t, mask, T, lse, grad_out,
+                   static_cast<float*>(grad_x), ld_grad, err, stream);
+}
+
+}  // namespace slp
