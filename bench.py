@@ -1,0 +1,437 @@
+#!/usr/bin/env python
+"""Benchmark of selected-token log-probabilities on one GB300 (or N replicas).
+
+A step is one pass of the hot path over one batch of synthetic input: the
+forward (online log-sum-exp + target gather) and the backward ((onehot -
+softmax) * g / T) of the logits-input path on the c151k workload
+(N=4096 tokens, V=151936, bf16 logits), through the C ABI of libslp.so.
+Prints ONE JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl slp|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica of the same
+workload on its own GPU (rows are independent: no data-path collective); the
+timed region is bracketed by barriers and the max time over ranks is used.
+``--impl reference`` times the CPU oracle on a bounded sample of the same
+workload instead (rank 0 only).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "selected-logprob fwd+bwd tokens/s and HBM GB/s (% of roofline) at V=151936, 1 GB300"
+UNIT = "tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=3000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["slp", "reference"], default="slp")
+    p.add_argument("--config", default="c151k", choices=["c151k", "packed", "stability", "tiny"])
+    p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--no-extra", action="store_true", help="skip the other workloads' lines")
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--rows", type=int, default=None,
+                   help="override N (same recipe), e.g. for a small profiling case")
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def traffic_table():
+    """Per-launch DRAM bytes from the committed ncu summary (kernel, workload,
+    bytes, source hash of the kernel file when captured)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    out = {}
+    if os.path.exists(path):
+        for line in open(path):
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            k, w, b, h = line.split()[:4]
+            out[(k, w)] = (float(b), h)
+    return out
+
+
+def source_hash(fname):
+    import hashlib
+    p = os.path.join(ROOT, "vocab_selected_token_gb300", "csrc", fname)
+    return hashlib.sha1(open(p, "rb").read()).hexdigest()[:12]
+
+
+# ---------------------------------------------------------------- distributed
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "slp" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif args.impl == "slp":
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world, device):
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        self.proc = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+            ident = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            ident = os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0]
+        self.ident = ident
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.ident, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax.append(float(f[1]))
+                power.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- workloads
+def logits_bytes(x, mask):
+    N, V = x.shape
+    es = x.element_size()
+    na = N if mask is None else int(mask.sum().item())
+    fwd = na * V * es + N * (4 + 4 + 4 + (0 if mask is None else 1))
+    bwd = na * V * es + N * V * es + N * (4 * 3 + (0 if mask is None else 1))
+    return fwd, bwd, na
+
+
+def time_logits(inp, steps, warmup, world, device, clocks=None):
+    """Device-timed forward+backward steps through the C ABI.  Returns a dict
+    with ms/step and the average duration of each kernel (CUDA events on the
+    launching stream)."""
+    from vocab_selected_token_gb300 import _lib
+    lib = _lib.load()
+    x, t, mask, T, g = inp.x, inp.t, inp.mask, inp.T, inp.g
+    N, V = x.shape
+    dt = _lib.SLP_BF16 if x.dtype == torch.bfloat16 else _lib.SLP_F32
+    lp = torch.empty(N, dtype=torch.float32, device=device)
+    lse = torch.empty_like(lp)
+    gx = torch.empty_like(x)
+    stream = torch.cuda.current_stream(device)
+    sh = stream.cuda_stream
+    mp = None if mask is None else mask.data_ptr()
+    fargs = (x.data_ptr(), dt, N, V, x.stride(0), t.data_ptr(), mp, float(T), lp.data_ptr(),
+             lse.data_ptr(), None, sh)
+    bargs = (x.data_ptr(), dt, N, V, x.stride(0), t.data_ptr(), mp, float(T), lse.data_ptr(),
+             g.data_ptr(), gx.data_ptr(), gx.stride(0), None, sh)
+
+    def step():
+        assert lib.slp_forward(*fargs) == 0
+        assert lib.slp_backward(*bargs) == 0
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(device)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize(device)
+    if clocks:
+        clocks.start()
+    for i in range(steps):
+        ev[i][0].record(stream)
+        assert lib.slp_forward(*fargs) == 0
+        ev[i][1].record(stream)
+        assert lib.slp_backward(*bargs) == 0
+        ev[i][2].record(stream)
+    torch.cuda.synchronize(device)
+    barrier(world)
+    clk = clocks.stop() if clocks else None
+    total_ms = ev[0][0].elapsed_time(ev[-1][2])
+    fwd = [e[0].elapsed_time(e[1]) for e in ev]
+    bwd = [e[1].elapsed_time(e[2]) for e in ev]
+    total_ms = max_over_ranks(total_ms, world, device)
+    return {"ms_per_step": total_ms / steps, "fwd_ms": sum(fwd) / steps,
+            "bwd_ms": sum(bwd) / steps, "clocks": clk, "launches": 2 * steps,
+            "outputs": (lp, lse, gx)}
+
+
+def e2e_logits(inp, steps, device):
+    """Same metric through the public Python API with host (pinned) buffers:
+    every step copies the step's inputs host->device, runs forward and
+    backward, and reads logprob, lse and grad_x back to the host."""
+    import vocab_selected_token_gb300 as slp
+    xh = inp.x.cpu().pin_memory()
+    th = inp.t.cpu().pin_memory()
+    gh = inp.g.cpu().pin_memory()
+    mh = None if inp.mask is None else inp.mask.cpu().pin_memory()
+    N, V = xh.shape
+    xd = torch.empty_like(inp.x)
+    td = torch.empty_like(inp.t)
+    gd = torch.empty_like(inp.g)
+    md = None if mh is None else torch.empty_like(inp.mask)
+    lp_h = torch.empty(N, dtype=torch.float32).pin_memory()
+    lse_h = torch.empty(N, dtype=torch.float32).pin_memory()
+    gx_h = torch.empty((N, V), dtype=xh.dtype).pin_memory()
+    gxd = torch.empty_like(inp.x)
+    h2d = xh.numel() * xh.element_size() + th.numel() * 4 + gh.numel() * 4 + (0 if mh is None else N)
+    d2h = 2 * N * 4 + gx_h.numel() * gx_h.element_size()
+
+    def step():
+        xd.copy_(xh, non_blocking=True)
+        td.copy_(th, non_blocking=True)
+        gd.copy_(gh, non_blocking=True)
+        if md is not None:
+            md.copy_(mh, non_blocking=True)
+        lp, lse = slp.slp_forward(xd, td, md, inp.T)
+        slp.slp_backward(xd, td, md, inp.T, lse, gd, grad_x=gxd)
+        lp_h.copy_(lp, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+        gx_h.copy_(gxd, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize(device)
+    s = torch.cuda.current_stream(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(steps):
+        step()
+    e1.record(s)
+    torch.cuda.synchronize(device)
+    ms = e0.elapsed_time(e1) / steps
+    return {"value": N * 1000.0 / ms, "unit": UNIT, "ms_per_step": ms,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+# ---------------------------------------------------------------- oracle arm
+def oracle_rows_per_second(inp, seconds, max_rows=4096):
+    """The CPU oracle as it stands (fp64 numpy, one core), forward+backward on
+    consecutive rows of the workload until `seconds` of CPU work are done."""
+    from oracle import slp_oracle as O
+    N = inp.x.shape[0]
+    rows_done, t_total, r = 0, 0.0, 0
+    while (t_total < seconds and rows_done < max_rows) or rows_done == 0:
+        blk = slice(r, min(r + 4, N))
+        x64 = inp.x[blk].double().cpu().numpy()
+        tt = inp.t[blk].cpu().numpy()
+        mm = None if inp.mask is None else inp.mask[blk].cpu().numpy()
+        gg = inp.g[blk].double().cpu().numpy()
+        t0 = time.perf_counter()
+        lp, lse = O.selected_logprob_forward(x64, tt, mm, inp.T)
+        O.selected_logprob_backward(x64, tt, mm, inp.T, lse, gg)
+        t_total += time.perf_counter() - t0
+        rows_done += x64.shape[0]
+        r = (r + 4) % N
+    return rows_done / t_total, rows_done, t_total
+
+
+def workload_desc(name, inp, na):
+    N, V = inp.x.shape
+    from vocab_selected_token_gb300.workloads import WORKLOADS
+    dt = "bf16" if inp.x.dtype == torch.bfloat16 else "f32"
+    return {"workload": f"{name}: N={N} tokens, V={V}, {dt} logits, T={inp.T}; "
+                        + WORKLOADS[name]["recipe"],
+            "N": N, "V": V, "active_rows": na, "temperature": inp.T,
+            "l2": f"inputs exceed L2 (logits {N * V * inp.x.element_size() / 1e9:.3f} GB > 129 MB); no flush"}
+
+
+def run_reference(args, world, rank):
+    from vocab_selected_token_gb300 import workloads as W
+    if rank != 0:
+        return
+    inp = W.make_logits_inputs(args.config, device="cpu", N=args.rows)
+    # size one step so the whole run stays within about two minutes
+    r1, _, t1 = oracle_rows_per_second(inp, 0.0, max_rows=4)
+    per_row = 1.0 / r1
+    rows = max(1, min(64, int(120.0 / max(1, args.steps + args.warmup) / per_row)))
+    from oracle import slp_oracle as O
+    N = inp.x.shape[0]
+
+    def step(i):
+        blk = slice((i * rows) % N, (i * rows) % N + rows)
+        x64 = inp.x[blk].double().numpy()
+        tt = inp.t[blk].numpy()
+        mm = None if inp.mask is None else inp.mask[blk].numpy()
+        lp, lse = O.selected_logprob_forward(x64, tt, mm, inp.T)
+        O.selected_logprob_backward(x64, tt, mm, inp.T, lse, inp.g[blk].double().numpy())
+        return x64.shape[0]
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    done = sum(step(i) for i in range(args.steps))
+    el = time.perf_counter() - t0
+    v = done / el
+    _, _, na = logits_bytes(inp.x, inp.mask)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1000 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded generators, CPU)",
+            "config": workload_desc(args.config, inp, na),
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"{rows} consecutive rows per step, fp64 numpy forward+backward"},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- main
+def main():
+    args = parse()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    import __graft_entry__
+    __graft_entry__.build()
+    from vocab_selected_token_gb300 import workloads as W
+    device = torch.device("cuda", torch.cuda.current_device())
+    hbm, bf16_burst, bf16_sus, peak_src = peaks()
+
+    inp = W.make_logits_inputs(args.config, device=device, N=args.rows)
+    fwd_b, bwd_b, na = logits_bytes(inp.x, inp.mask)
+    N, V = inp.x.shape
+    torch.cuda.reset_peak_memory_stats(device)
+    base_mem = torch.cuda.memory_allocated(device)
+    res = time_logits(inp, args.steps, args.warmup, world, device, ClockSampler(device))
+    extra_mem = torch.cuda.max_memory_allocated(device) - base_mem
+    value = world * N * 1000.0 / res["ms_per_step"]
+
+    kern = "slp_bwd_kernel" if res["bwd_ms"] >= res["fwd_ms"] else "slp_fwd_kernel"
+    k_bytes, k_ms = (bwd_b, res["bwd_ms"]) if kern == "slp_bwd_kernel" else (fwd_b, res["fwd_ms"])
+    achieved = k_bytes / (k_ms * 1e-3) / 1e9
+    tt = traffic_table().get((kern, args.config))
+    traffic = None
+    if tt is not None and tt[1] == source_hash("slp_logits.cu"):
+        traffic = tt[0]
+    step_gbs = (fwd_b + bwd_b) / (res["ms_per_step"] * 1e-3) / 1e9
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": res["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if inp.x.dtype == torch.bfloat16 else "f32",
+        "data": "synthetic (seeded generators on the device)",
+        "config": {**workload_desc(args.config, inp, na),
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "hbm": {"step_gbs": step_gbs, "step_frac_of_measured": step_gbs / hbm,
+                "step_frac_of_8tbs": step_gbs / 8000.0,
+                "fwd_ms": res["fwd_ms"], "bwd_ms": res["bwd_ms"],
+                "fwd_gbs": fwd_b / (res["fwd_ms"] * 1e-3) / 1e9,
+                "bwd_gbs": bwd_b / (res["bwd_ms"] * 1e-3) / 1e9,
+                "bytes_per_step": fwd_b + bwd_b},
+        "roofline": {"kernel": kern, "bound": "hbm", "achieved": achieved, "peak": hbm,
+                     "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": k_bytes, "peak_source": peak_src},
+        "clocks": res["clocks"],
+        "gpu_launches": res["launches"],
+        "peak_extra_device_bytes": int(extra_mem),
+    }
+    if rank == 0:
+        line["e2e"] = e2e_logits(inp, args.e2e_steps, device)
+        if world == 1:
+            v, rows, secs = oracle_rows_per_second(inp, args.cpu_seconds)
+            line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                    "sample": f"{rows} rows of {args.config} (forward+backward, "
+                                              f"fp64 numpy, {secs:.1f} s)"}
+        if not args.no_extra:
+            del inp
+            torch.cuda.empty_cache()
+            line["other_workloads"] = other_workloads(device, hbm)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def other_workloads(device, hbm):
+    """Shorter timings of the other logits-input workloads (and the fused LM
+    head once present), for the record."""
+    from vocab_selected_token_gb300 import workloads as W
+    out = {}
+    for name in ("packed", "stability"):
+        inp = W.make_logits_inputs(name, device=device)
+        fwd_b, bwd_b, na = logits_bytes(inp.x, inp.mask)
+        r = time_logits(inp, 30, 3, 1, device)
+        out[name] = {"N": inp.x.shape[0], "V": inp.x.shape[1], "active_rows": na,
+                     "ms_per_step": r["ms_per_step"], "fwd_ms": r["fwd_ms"], "bwd_ms": r["bwd_ms"],
+                     "tokens_per_s": inp.x.shape[0] * 1000.0 / r["ms_per_step"],
+                     "step_gbs": (fwd_b + bwd_b) / (r["ms_per_step"] * 1e-3) / 1e9,
+                     "fwd_gbs": fwd_b / (r["fwd_ms"] * 1e-3) / 1e9,
+                     "bwd_gbs": bwd_b / (r["bwd_ms"] * 1e-3) / 1e9}
+        out[name]["step_frac_of_measured"] = out[name]["step_gbs"] / hbm
+        del inp, r
+        torch.cuda.empty_cache()
+    return out
+
+
+if __name__ == "__main__":
+    main()

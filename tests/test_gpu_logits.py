@@ -1,0 +1,237 @@
+"""GPU parity of the logits-input path (slp_forward / slp_backward through the
+C ABI) against the CPU oracle."""
+
+from __future__ import annotations
+
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import vocab_selected_token_gb300 as slp
+from oracle import slp_oracle as O
+from tests.gpu_util import (TOL_LP, assert_close_nan, assert_grad_close, check_rows, device,
+                            to64)
+from vocab_selected_token_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+GOLDEN = json.load(open(os.path.join(os.path.dirname(__file__), "golden",
+                                     "oracle_cases.json")))["cases"]
+
+
+def run(x, t, mask, T, g, stream=None):
+    lp, lse = slp.slp_forward(x, t, mask, T, stream=stream)
+    gx = slp.slp_backward(x, t, mask, T, lse, g, stream=stream)
+    torch.cuda.synchronize()
+    return lp, lse, gx
+
+
+@pytest.mark.parametrize("case", GOLDEN, ids=lambda c: c["name"])
+def test_golden_cases(case):
+    dev = device()
+    x = torch.tensor(case["x"], dtype=torch.float32, device=dev)
+    t = torch.tensor(case["t"], dtype=torch.int32, device=dev)
+    g = torch.tensor(case["g"], dtype=torch.float32, device=dev)
+    lp, lse, gx = run(x, t, None, case["T"], g)
+    assert_close_nan(to64(lp), case["logprob"], TOL_LP, "logprob")
+    assert_close_nan(to64(lse), case["lse"], TOL_LP, "lse")
+    assert_grad_close(to64(gx), np.array(case["grad_x"]))
+
+
+def test_tiny_all_rows():
+    dev = device()
+    a = W.make_logits_inputs("tiny", device=dev)
+    lp, lse, gx = run(a.x, a.t, a.mask, a.T, a.g)
+    check_rows(a.x, a.t, a.mask, a.T, a.g, lp, lse, gx, range(a.x.shape[0]))
+
+
+# Same recipes at sizes the oracle handles in seconds, spanning many tiles
+# and ragged tails.
+SCALED = [
+    ("c151k", 48, 151936),
+    ("c151k", 33, 151936 - 5),     # V not a multiple of the vector width
+    ("packed", 3000, 20016),
+    ("stability", 256, 131072),
+    ("stability", 64, 4099),
+    ("tiny", 300, 2047),           # odd V, rows not 16-byte aligned
+]
+
+
+@pytest.mark.parametrize("name,N,V", SCALED, ids=lambda v: str(v))
+def test_scaled_workloads_all_rows(name, N, V):
+    dev = device()
+    a = W.make_logits_inputs(name, device=dev, N=N, V=V)
+    lp, lse, gx = run(a.x, a.t, a.mask, a.T, a.g)
+    check_rows(a.x, a.t, a.mask, a.T, a.g, lp, lse, gx, range(N))
+
+
+def test_ragged_tail_on_vector_path():
+    """V not a multiple of 8 but the row stride is: 128-bit body plus scalar
+    tail, and the padding columns of grad_x are left untouched."""
+    dev = device()
+    a = W.make_logits_inputs("c151k", device=dev, N=40, V=20016)
+    V = 20011
+    x = a.x[:, :V]
+    gx = torch.full((40, 20016), 7.0, dtype=torch.bfloat16, device=dev)
+    lp, lse = slp.slp_forward(x, a.t % V, None, a.T)
+    slp.slp_backward(x, a.t % V, None, a.T, lse, a.g, grad_x=gx[:, :V])
+    torch.cuda.synchronize()
+    assert bool((gx[:, V:] == 7.0).all()), "columns >= V of grad_x were written"
+    check_rows(x, a.t % V, None, a.T, a.g, lp, lse, gx[:, :V], range(40))
+
+
+FULL = ["c151k", "packed", "stability"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled_rows(name):
+    """Full workload sizes, in the launch configuration the bench times:
+    sampled rows against the oracle, every row against properties."""
+    dev = device()
+    a = W.make_logits_inputs(name, device=dev)
+    N, V = a.x.shape
+    lp, lse, gx = run(a.x, a.t, a.mask, a.T, a.g)
+    gen = np.random.default_rng(17)
+    rows = set(gen.choice(N, 40, replace=False).tolist()) | {0, N - 1}
+    if name == "stability":
+        inf_rows = torch.nonzero(torch.isinf(a.x).any(dim=1))[:, 0].cpu().numpy()
+        rows |= set(inf_rows[:8].tolist())
+    if a.mask is not None:
+        m = a.mask.cpu().numpy()
+        edges = np.flatnonzero(np.diff(m.astype(np.int8)))
+        rows |= set(edges[:8].tolist()) | set((edges[:8] + 1).tolist())
+    check_rows(a.x, a.t, a.mask, a.T, a.g, lp, lse, gx, rows)
+    active = torch.ones(N, dtype=torch.bool, device=dev) if a.mask is None else a.mask != 0
+    assert bool(torch.isfinite(lp[active]).all()) and bool((lp[active] <= 1e-6).all())
+    assert bool(torch.isfinite(lse[active]).all())
+    if a.mask is not None:
+        off = ~active
+        assert bool((lp[off] == 0).all()) and bool((lse[off] == 0).all())
+        assert bool((gx[off].view(torch.int16) == 0).all()), "masked rows not +0.0"
+    # every active row of the gradient sums to ~0 (softmax sums to one), up to
+    # the rounding of each stored element (at most 2^-8 of it in bf16)
+    ga = gx[active].double()
+    rs = ga.sum(dim=1).abs()
+    bound = 2.0 ** -8 * ga.abs().sum(dim=1) + 1e-5
+    assert bool((rs <= bound).all())
+
+
+def test_split_invariance():
+    """The same rows computed under different cluster splits (chosen from N)
+    agree with each other and with the oracle."""
+    dev = device()
+    big = W.make_logits_inputs("c151k", device=dev, N=5000)
+    outs = []
+    for N in (4, 600, 1000, 2000, 5000):
+        x, t = big.x[:N], big.t[:N]
+        lp, lse = slp.slp_forward(x, t, None, 1.0)
+        torch.cuda.synchronize()
+        outs.append((to64(lp[:4]), to64(lse[:4])))
+    for lp, lse in outs[1:]:
+        assert np.abs(lp - outs[0][0]).max() <= TOL_LP
+        assert np.abs(lse - outs[0][1]).max() <= TOL_LP
+    check_rows(big.x[:4], big.t[:4], None, 1.0, big.g[:4],
+               *slp.slp_forward(big.x[:4], big.t[:4], None, 1.0), None, range(4))
+
+
+def test_deterministic():
+    dev = device()
+    a = W.make_logits_inputs("c151k", device=dev, N=512)
+    r1 = run(a.x, a.t, a.mask, a.T, a.g)
+    r2 = run(a.x, a.t, a.mask, a.T, a.g)
+    for u, v in zip(r1, r2):
+        assert torch.equal(u.view(torch.int16) if u.dtype == torch.bfloat16 else u.view(torch.int32),
+                           v.view(torch.int16) if v.dtype == torch.bfloat16 else v.view(torch.int32))
+
+
+def test_empty_and_degenerate():
+    dev = device()
+    # N = 0
+    x = torch.empty((0, 100), dtype=torch.bfloat16, device=dev)
+    t = torch.empty(0, dtype=torch.int32, device=dev)
+    lp, lse = slp.slp_forward(x, t, None, 1.0)
+    gx = slp.slp_backward(x, t, None, 1.0, lse, torch.empty(0, device=dev))
+    assert lp.numel() == 0 and gx.shape == (0, 100)
+    # V = 1: logprob 0, gradient 0
+    x = torch.randn(5, 1, device=dev)
+    t = torch.zeros(5, dtype=torch.int32, device=dev)
+    g = torch.ones(5, device=dev)
+    lp, lse, gx = run(x, t, None, 0.9, g)
+    assert float(lp.abs().max()) <= TOL_LP
+    assert float(gx.abs().max()) <= 1e-5
+    # all-zero mask, all-one mask, mask None
+    a = W.make_logits_inputs("tiny", device=dev, N=64, V=4096)
+    z = torch.zeros(64, dtype=torch.uint8, device=dev)
+    lp0, lse0, gx0 = run(a.x, a.t, z, a.T, a.g)
+    assert bool((lp0 == 0).all()) and bool((lse0 == 0).all())
+    assert bool((gx0.view(torch.int16) == 0).all())
+    lp1, lse1, gx1 = run(a.x, a.t, torch.ones_like(z), a.T, a.g)
+    lpn, lsen, gxn = run(a.x, a.t, None, a.T, a.g)
+    assert torch.equal(lp1, lpn) and torch.equal(gx1, gxn)
+
+
+def test_target_on_neg_inf_and_all_neg_inf_rows():
+    dev = device()
+    x = torch.randn(3, 1000, device=dev)
+    x[0, 5] = float("-inf")
+    x[1, :] = float("-inf")
+    t = torch.tensor([5, 0, 7], dtype=torch.int32, device=dev)
+    lp, lse = slp.slp_forward(x, t, None, 1.0)
+    torch.cuda.synchronize()
+    assert float(lp[0]) == float("-inf")
+    assert np.isnan(float(lp[1])) and np.isnan(float(lse[1]))
+    r, _ = O.selected_logprob_forward(to64(x[2:]), [7], None, 1.0)
+    assert abs(float(lp[2]) - r[0]) <= TOL_LP
+
+
+def test_bad_target_sets_error_word():
+    dev = device()
+    a = W.make_logits_inputs("tiny", device=dev, N=16, V=512)
+    t = a.t.clone()
+    t[3] = 512
+    t[9] = -1
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    lp, lse = slp.slp_forward(a.x, t, None, 1.0, err=err)
+    gx = slp.slp_backward(a.x, t, None, 1.0, lse, a.g, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & 1
+    assert np.isnan(float(lp[3])) and np.isnan(float(lp[9]))
+    assert bool(torch.isnan(gx[3].float()).all())
+    good = [i for i in range(16) if i not in (3, 9)]
+    check_rows(a.x, t, None, 1.0, a.g, lp, lse, gx, good)
+    # masked-off bad targets are not errors
+    err.zero_()
+    m = torch.ones(16, dtype=torch.uint8, device=dev)
+    m[3] = m[9] = 0
+    slp.slp_forward(a.x, t, m, 1.0, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+
+
+def test_strided_unaligned_rows_fp32():
+    dev = device()
+    base = torch.randn(20, 1003, device=dev) * 3
+    x = base[:, 1:1002]                  # ld = 1003 floats, rows not 16-byte aligned
+    t = torch.randint(0, 1001, (20,), dtype=torch.int32, device=dev)
+    g = torch.rand(20, device=dev) * 2 - 1
+    lp, lse, gx = run(x, t, None, 1.3, g)
+    check_rows(x, t, None, 1.3, g, lp, lse, gx, range(20))
+
+
+def test_autograd_and_side_stream():
+    dev = device()
+    a = W.make_logits_inputs("tiny", device=dev, N=128, V=3000)
+    x = a.x.clone().requires_grad_(True)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        lp = slp.selected_logprob(x, a.t, None, a.T)
+        (lp * a.g).sum().backward()
+    s.synchronize()
+    _, lse = slp.slp_forward(a.x, a.t, None, a.T)
+    ref = slp.slp_backward(a.x, a.t, None, a.T, lse, a.g)
+    torch.cuda.synchronize()
+    assert torch.equal(x.grad, ref)
+    check_rows(a.x, a.t, None, a.T, a.g, lp.detach(), lse, x.grad, range(0, 128, 7))
