@@ -69,7 +69,10 @@ typedef enum {
 } slp_status;
 
 /* Bits OR-ed into the optional device error word. */
-#define SLP_DATA_ERR_TARGET 1 /* target outside [0, V) on an active row */
+#define SLP_DATA_ERR_TARGET 1    /* target outside [0, V) on an active row          */
+#define SLP_DEVICE_ERR_TIMEOUT 2 /* a pipeline wait inside an LM-head kernel gave up
+                                    after about two seconds; that call's outputs are
+                                    undefined (the kernel returned instead of hanging) */
 
 /*
  * slp_forward - selected-token log-probability and row log-sum-exp.
@@ -123,10 +126,17 @@ int slp_backward(const void* x, int dtype, int64_t N, int64_t V, int64_t ld,
 
 /*
  * slp_lmhead_workspace_size - bytes of device workspace that
- * slp_lmhead_forward and slp_lmhead_backward need for these sizes (the same
- * value serves both; a larger workspace is fine).  Returns 0 for invalid sizes.
+ * slp_lmhead_backward needs for these sizes (enough for slp_lmhead_forward
+ * too; a larger workspace is fine).  Returns 0 for invalid sizes.
+ *
+ * slp_lmhead_forward_workspace_size - the smaller amount slp_lmhead_forward
+ * alone needs (compacted hidden rows and per-slab log-sum-exp partials).
+ *
+ * The backward workspace holds the compacted rows, a bf16 dz buffer of
+ * roundup(N,128) x roundup(V,64) elements and float32 split-K partials of dh.
  */
 size_t slp_lmhead_workspace_size(int64_t N, int64_t V, int64_t d);
+size_t slp_lmhead_forward_workspace_size(int64_t N, int64_t V, int64_t d);
 
 /*
  * slp_lmhead_forward - selected-token log-probabilities through the LM head,
@@ -145,8 +155,8 @@ size_t slp_lmhead_workspace_size(int64_t N, int64_t V, int64_t d);
  *            are accumulated in float32 and not rounded before the
  *            log-sum-exp.
  *   ws, ws_bytes  device workspace of at least
- *            slp_lmhead_workspace_size(N, V, d) bytes, 256-byte aligned;
- *            its contents on entry do not matter.
+ *            slp_lmhead_forward_workspace_size(N, V, d) bytes, 256-byte
+ *            aligned; its contents on entry do not matter.
  */
 int slp_lmhead_forward(const void* h, const void* W, int64_t N, int64_t V, int64_t d,
                        const int32_t* t, const uint8_t* mask, float T,
@@ -166,7 +176,11 @@ int slp_lmhead_forward(const void* h, const void* W, int64_t N, int64_t V, int64
  *   lse       [N] float32 from slp_lmhead_forward.
  *   grad_out  [N] float32.
  *   dh        [N, d] bf16 out.      dW  [V, d] bf16 out (overwritten).
- *   ws, ws_bytes, err, stream   as for slp_lmhead_forward.
+ *   ws, ws_bytes  at least slp_lmhead_workspace_size(N, V, d) bytes,
+ *             256-byte aligned; contents on entry do not matter.
+ *   err, stream   as for slp_lmhead_forward.
+ * A row whose target is outside [0, V) is flagged in *err, gets a NaN dh row
+ * and contributes nothing to dW.
  */
 int slp_lmhead_backward(const void* h, const void* W, int64_t N, int64_t V, int64_t d,
                         const int32_t* t, const uint8_t* mask, float T,

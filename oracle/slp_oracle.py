@@ -56,6 +56,8 @@ __all__ = [
     "lmhead_logits",
     "lmhead_forward",
     "lmhead_backward",
+    "lmhead_dh_rows",
+    "lmhead_dW_rows",
 ]
 
 
@@ -195,3 +197,46 @@ def lmhead_backward(h, W, t, mask, T: float, lse, grad_out):
         dh[rows] = dz @ W
         dW = dz.T @ h[rows]
     return dh, dW
+
+
+def lmhead_dh_rows(h, W, t, mask, T: float, lse, grad_out, rows):
+    """Rows `rows` of dh from lmhead_backward, one at a time: for an active row
+    n, dh[n] = dz[n] @ W with dz[n, v] = g_n (1[v = t_n] - exp(h_n.W_v / T -
+    lse_n)) / T; an inactive row is 0.  Needs only row n's own lse."""
+    W = _as_f64(W)
+    h = _as_f64(h)
+    N = h.shape[0]
+    active = _active_rows(N, mask)
+    t = np.asarray(t).reshape(N).astype(np.int64)
+    lse = _as_f64(lse).reshape(N)
+    g = _as_f64(grad_out).reshape(N)
+    out = np.zeros((len(rows), W.shape[1]), dtype=np.float64)
+    for k, n in enumerate(rows):
+        if not active[n]:
+            continue
+        x = lmhead_logits(h[n:n + 1], W)
+        dz = selected_logprob_backward(x, t[n:n + 1], None, T, lse[n:n + 1], g[n:n + 1])
+        out[k] = dz[0] @ W
+    return out
+
+
+def lmhead_dW_rows(h, W, t, mask, T: float, lse, grad_out, vrows):
+    """Rows `vrows` of dW from lmhead_backward: dW[v] = sum over active rows n
+    of dz[n, v] h[n], with dz[n, v] = g_n (1[v = t_n] - exp(h_n.W_v / T -
+    lse_n)) / T.  Needs lse of every active row (from lmhead_forward)."""
+    h = _as_f64(h)
+    W = _as_f64(W)
+    N = h.shape[0]
+    active = _active_rows(N, mask)
+    rows = np.nonzero(active)[0]
+    t = np.asarray(t).reshape(N).astype(np.int64)[rows]
+    lse = _as_f64(lse).reshape(N)[rows]
+    g = _as_f64(grad_out).reshape(N)[rows]
+    hr = h[rows]
+    out = np.zeros((len(vrows), h.shape[1]), dtype=np.float64)
+    with np.errstate(over="ignore", invalid="ignore"):
+        for k, v in enumerate(vrows):
+            z = hr @ W[v] / T
+            dz = g * ((t == v).astype(np.float64) - np.exp(z - lse)) / T
+            out[k] = dz @ hr
+    return out

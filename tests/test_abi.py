@@ -85,9 +85,11 @@ def test_backward_argument_errors(lib):
 
 def test_lmhead_argument_errors(lib):
     N, V, d = 64, 1000, 128
-    need = lib.slp_lmhead_workspace_size(N, V, d)
-    assert need > 0
+    need_b = lib.slp_lmhead_workspace_size(N, V, d)
+    need = lib.slp_lmhead_forward_workspace_size(N, V, d)
+    assert 0 < need <= need_b
     assert lib.slp_lmhead_workspace_size(-1, V, d) == 0
+    assert lib.slp_lmhead_forward_workspace_size(N, 0, d) == 0
     f = lib.slp_lmhead_forward
     # d not a multiple of 64
     assert f(FAKE, FAKE, N, V, 100, FAKE, None, 1.0, FAKE, FAKE, FAKE, 1 << 40, None,
@@ -104,10 +106,13 @@ def test_lmhead_argument_errors(lib):
     assert f(FAKE, FAKE, N, V, d, FAKE, None, -1.0, FAKE, FAKE, FAKE, need, None,
              None) == _lib.SLP_ERR_INVALID_ARG
     b = lib.slp_lmhead_backward
-    assert b(FAKE, FAKE, N, V, d, FAKE, None, 1.0, FAKE, FAKE, None, FAKE, FAKE, need, None,
+    assert b(FAKE, FAKE, N, V, d, FAKE, None, 1.0, FAKE, FAKE, None, FAKE, FAKE, need_b, None,
              None) == _lib.SLP_ERR_INVALID_ARG
     assert b(FAKE, FAKE, N, V, d, FAKE, None, 1.0, FAKE, FAKE, ctypes.c_void_p(0x1002), FAKE,
-             FAKE, need, None, None) == _lib.SLP_ERR_MISALIGNED
+             FAKE, need_b, None, None) == _lib.SLP_ERR_MISALIGNED
+    # the backward needs the larger workspace
+    assert b(FAKE, FAKE, N, V, d, FAKE, None, 1.0, FAKE, FAKE, FAKE, FAKE, FAKE, need_b - 1,
+             None, None) == _lib.SLP_ERR_WORKSPACE
 
 
 def test_product_path_has_no_oracle_import():

@@ -1,0 +1,152 @@
+"""GPU parity of the fused LM-head path (slp_lmhead_forward / _backward through
+the C ABI) against the CPU oracle.
+
+Tolerances: |logprob - oracle| <= 5e-3; gradients reach cosine >= 0.999 and
+relative Frobenius error <= 1e-2 against the fp64 oracle; masked rows of dh
+are exactly +0.0."""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import vocab_selected_token_gb300 as slp
+from oracle import slp_oracle as O
+from tests.gpu_util import assert_close_nan, device, to64
+from vocab_selected_token_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+TOL_LP = 5e-3
+COS_MIN = 0.999
+FROB_MAX = 1e-2
+
+
+def grad_ok(got, ref, what):
+    got = np.asarray(got, np.float64).ravel()
+    ref = np.asarray(ref, np.float64).ravel()
+    nr = np.linalg.norm(ref)
+    if nr == 0:
+        assert np.all(got == 0), f"{what}: expected all zeros"
+        return
+    cos = float(got @ ref / (np.linalg.norm(got) * nr + 1e-300))
+    frob = float(np.linalg.norm(got - ref) / nr)
+    assert cos >= COS_MIN and frob <= FROB_MAX, f"{what}: cosine {cos:.6f} frob {frob:.3e}"
+
+
+def run_fwd_bwd(a, err=None):
+    lp, lse = slp.slp_lmhead_forward(a.h, a.W, a.t, a.mask, a.T, err=err)
+    dh, dW = slp.slp_lmhead_backward(a.h, a.W, a.t, a.mask, a.T, lse, a.g, err=err)
+    torch.cuda.synchronize()
+    return lp, lse, dh, dW
+
+
+SMALL = [
+    # N, V, d, T, p_mask
+    (300, 1000, 128, 1.0, 0.5),     # ragged row block and vocabulary tile
+    (256, 512, 64, 0.7, 1.0),       # one k-block, all rows active
+    (1024, 20000, 512, 0.8, 0.5),   # many slabs
+    (130, 4096, 2560, 1.0, 0.9),    # the workload's hidden size
+]
+
+
+@pytest.mark.parametrize("N,V,d,T,pm", SMALL, ids=lambda v: str(v))
+def test_small_all_outputs(N, V, d, T, pm):
+    dev = device()
+    a = W.make_lmhead_inputs(device=dev, N=N, V=V, d=d, p_mask=pm)
+    a.T = T
+    lp, lse, dh, dW = run_fwd_bwd(a)
+    h64, W64 = to64(a.h), to64(a.W)
+    t, m, g = a.t.cpu().numpy(), a.mask.cpu().numpy(), to64(a.g)
+    rlp, rlse = O.lmhead_forward(h64, W64, t, m, T)
+    assert_close_nan(to64(lp), rlp, TOL_LP, "logprob")
+    assert_close_nan(to64(lse), rlse, TOL_LP, "lse")
+    rdh, rdW = O.lmhead_backward(h64, W64, t, m, T, rlse, g)
+    grad_ok(to64(dh), rdh, "dh")
+    grad_ok(to64(dW), rdW, "dW")
+    off = torch.as_tensor(m == 0, device=dev)
+    assert bool((dh[off].view(torch.int16) == 0).all()), "masked dh rows not +0.0"
+    assert bool((lp[off] == 0).all()) and bool((lse[off] == 0).all())
+
+
+def test_full_size_sampled():
+    """The lmhead workload at full size (N=8192, V=151936, d=2560): sampled rows
+    of logprob / dh and sampled rows of dW against the oracle."""
+    dev = device()
+    a = W.make_lmhead_inputs(device=dev)
+    lp, lse, dh, dW = run_fwd_bwd(a)
+    h64, W64 = to64(a.h), to64(a.W)
+    t, m, g = a.t.cpu().numpy(), a.mask.cpu().numpy(), to64(a.g)
+    act = np.nonzero(m)[0]
+    gen = np.random.default_rng(5)
+    rows = sorted(set(gen.choice(act, 12, replace=False).tolist()) | {int(act[0]), int(act[-1])})
+    # oracle forward for every active row (dW needs every row's lse)
+    rlp, rlse = O.lmhead_forward(h64, W64, t, m, a.T)
+    assert_close_nan(to64(lp), rlp, TOL_LP, "logprob (all rows)")
+    rdh = O.lmhead_dh_rows(h64, W64, t, m, a.T, rlse, g, rows)
+    grad_ok(to64(dh[rows]), rdh, "dh (sampled rows)")
+    vrows = sorted(set(gen.choice(a.W.shape[0], 12, replace=False).tolist()) |
+                   {0, a.W.shape[0] - 1, int(t[act[0]])})
+    rdW = O.lmhead_dW_rows(h64, W64, t, m, a.T, rlse, g, vrows)
+    grad_ok(to64(dW[vrows]), rdW, "dW (sampled rows)")
+    off = torch.as_tensor(m == 0, device=dev)
+    assert bool((dh[off].view(torch.int16) == 0).all())
+    assert bool(torch.isfinite(dW.float()).all()) and bool(torch.isfinite(dh.float()).all())
+
+
+def test_no_mask_and_all_masked():
+    dev = device()
+    a = W.make_lmhead_inputs(device=dev, N=200, V=3000, d=256)
+    # mask None == all-one mask
+    lp1, lse1 = slp.slp_lmhead_forward(a.h, a.W, a.t, None, a.T)
+    lp2, lse2 = slp.slp_lmhead_forward(a.h, a.W, a.t, torch.ones_like(a.mask), a.T)
+    torch.cuda.synchronize()
+    assert torch.equal(lp1, lp2) and torch.equal(lse1, lse2)
+    # nothing active: zeros everywhere, dW fully overwritten with zeros
+    z = torch.zeros_like(a.mask)
+    lp, lse = slp.slp_lmhead_forward(a.h, a.W, a.t, z, a.T)
+    dh = torch.full((200, 256), 3.0, dtype=torch.bfloat16, device=dev)
+    dW = torch.full((3000, 256), 3.0, dtype=torch.bfloat16, device=dev)
+    slp.slp_lmhead_backward(a.h, a.W, a.t, z, a.T, lse, a.g, dh=dh, dW=dW)
+    torch.cuda.synchronize()
+    assert bool((lp == 0).all()) and bool((lse == 0).all())
+    assert bool((dh.view(torch.int16) == 0).all()) and bool((dW.view(torch.int16) == 0).all())
+
+
+def test_bad_target_flagged():
+    dev = device()
+    a = W.make_lmhead_inputs(device=dev, N=64, V=1000, d=128, p_mask=1.0)
+    a.t[5] = 1000
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    lp, lse, dh, dW = run_fwd_bwd(a, err=err)
+    assert int(err.item()) & 1
+    assert np.isnan(float(lp[5])) and bool(torch.isnan(dh[5].float()).all())
+    good = [i for i in range(64) if i != 5]
+    m = np.ones(64, np.uint8)
+    m[5] = 0  # the flagged row contributes nothing: same as masking it out
+    rlp, rlse = O.lmhead_forward(to64(a.h), to64(a.W), a.t.cpu().numpy(), m, a.T)
+    assert_close_nan(to64(lp[good]), rlp[good], TOL_LP, "logprob")
+    _, rdW = O.lmhead_backward(to64(a.h), to64(a.W), a.t.cpu().numpy(), m, a.T, rlse, to64(a.g))
+    grad_ok(to64(dW), rdW, "dW without the flagged row")
+
+
+def test_deterministic():
+    dev = device()
+    a = W.make_lmhead_inputs(device=dev, N=700, V=9000, d=256)
+    r1 = run_fwd_bwd(a)
+    r2 = run_fwd_bwd(a)
+    for u, v in zip(r1, r2):
+        assert torch.equal(u, v)
+
+
+def test_autograd():
+    dev = device()
+    a = W.make_lmhead_inputs(device=dev, N=128, V=2000, d=128)
+    h = a.h.clone().requires_grad_(True)
+    Wt = a.W.clone().requires_grad_(True)
+    lp = slp.lmhead_selected_logprob(h, Wt, a.t, a.mask, a.T)
+    (lp * a.g).sum().backward()
+    lp2, lse2, dh, dW = run_fwd_bwd(a)
+    assert torch.equal(lp.detach(), lp2)
+    assert torch.equal(h.grad, dh) and torch.equal(Wt.grad, dW)

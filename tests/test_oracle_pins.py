@@ -117,3 +117,21 @@ def test_decode_bf16_all_patterns_match_torch():
     theirs = torch.from_numpy(pats.view(np.int16)).view(torch.bfloat16).double().numpy()
     same = (ours == theirs) | (np.isnan(ours) & np.isnan(theirs))
     assert same.all()
+
+
+def test_sampled_lmhead_gradients_match_full_backward():
+    """The one-row-at-a-time dh / dW helpers equal the finite-difference-pinned
+    full backward."""
+    r = np.random.default_rng(12)
+    N, d, V, T = 9, 8, 30, 0.8
+    h = r.normal(0, 1, (N, d))
+    W = r.normal(0, 0.4, (V, d))
+    t = r.integers(0, V, N)
+    g = r.uniform(-1, 1, N)
+    mask = (r.random(N) < 0.6).astype(np.uint8)
+    _, lse = O.lmhead_forward(h, W, t, mask, T)
+    dh, dW = O.lmhead_backward(h, W, t, mask, T, lse, g)
+    rows = [0, 3, 8, 5]
+    assert np.allclose(O.lmhead_dh_rows(h, W, t, mask, T, lse, g, rows), dh[rows], rtol=1e-12, atol=1e-14)
+    vr = [0, 7, 29, 13]
+    assert np.allclose(O.lmhead_dW_rows(h, W, t, mask, T, lse, g, vr), dW[vr], rtol=1e-12, atol=1e-14)

@@ -25,6 +25,7 @@ from ._lib import SlpError
 
 __all__ = [
     "SlpError", "slp_forward", "slp_backward", "slp_lmhead_workspace_size",
+    "slp_lmhead_forward_workspace_size",
     "slp_lmhead_forward", "slp_lmhead_backward", "selected_logprob",
     "lmhead_selected_logprob", "library_path",
 ]
@@ -100,7 +101,13 @@ def slp_backward(x, t, mask, T: float, lse, grad_out, grad_x=None, err=None, str
 
 
 def slp_lmhead_workspace_size(N: int, V: int, d: int) -> int:
+    """Bytes of workspace slp_lmhead_backward needs (enough for the forward too)."""
     return int(_lib.load().slp_lmhead_workspace_size(int(N), int(V), int(d)))
+
+
+def slp_lmhead_forward_workspace_size(N: int, V: int, d: int) -> int:
+    """Bytes of workspace slp_lmhead_forward alone needs."""
+    return int(_lib.load().slp_lmhead_forward_workspace_size(int(N), int(V), int(d)))
 
 
 def _lmhead_check(h, W):
@@ -111,8 +118,8 @@ def _lmhead_check(h, W):
     return h.shape[0], W.shape[0], h.shape[1]
 
 
-def _workspace(N, V, d, ws, device):
-    need = slp_lmhead_workspace_size(N, V, d)
+def _workspace(N, V, d, ws, device, forward_only=False):
+    need = (slp_lmhead_forward_workspace_size if forward_only else slp_lmhead_workspace_size)(N, V, d)
     if ws is None:
         ws = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
     return ws, ws.numel()
@@ -129,7 +136,7 @@ def slp_lmhead_forward(h, W, t, mask=None, T: float = 1.0, logprob=None, lse=Non
         logprob = torch.empty(N, dtype=torch.float32, device=h.device)
     if lse is None:
         lse = torch.empty(N, dtype=torch.float32, device=h.device)
-    ws, nbytes = _workspace(N, V, d, ws, h.device)
+    ws, nbytes = _workspace(N, V, d, ws, h.device, forward_only=True)
     _lib.call("slp_lmhead_forward", _ptr(h), _ptr(W), N, V, d, _ptr(t), _ptr(mask), float(T),
               _ptr(logprob), _ptr(lse), _ptr(ws), nbytes, _ptr(err), _stream_handle(stream))
     return logprob, lse

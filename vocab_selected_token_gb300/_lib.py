@@ -18,6 +18,7 @@ SLP_ERR_MISALIGNED = 3
 SLP_ERR_WORKSPACE = 4
 SLP_ERR_CUDA = 5
 SLP_DATA_ERR_TARGET = 1
+SLP_DEVICE_ERR_TIMEOUT = 2
 
 _vp = ctypes.c_void_p
 _i64 = ctypes.c_int64
@@ -31,6 +32,7 @@ SIGNATURES = {
     "slp_backward": (_int, [_vp, _int, _i64, _i64, _i64, _vp, _vp, _f32, _vp, _vp, _vp, _i64,
                             _vp, _vp]),
     "slp_lmhead_workspace_size": (_sz, [_i64, _i64, _i64]),
+    "slp_lmhead_forward_workspace_size": (_sz, [_i64, _i64, _i64]),
     "slp_lmhead_forward": (_int, [_vp, _vp, _i64, _i64, _i64, _vp, _vp, _f32, _vp, _vp, _vp,
                                   _sz, _vp, _vp]),
     "slp_lmhead_backward": (_int, [_vp, _vp, _i64, _i64, _i64, _vp, _vp, _f32, _vp, _vp, _vp,

@@ -42,7 +42,7 @@ int check_logits_args(const void* x, int dtype, int64_t N, int64_t V, int64_t ld
 }
 
 int check_lmhead_args(const void* h, const void* W, int64_t N, int64_t V, int64_t d,
-                      const int32_t* t, float T, void* ws, size_t ws_bytes) {
+                      const int32_t* t, float T, void* ws, size_t ws_bytes, size_t ws_need) {
   if (N < 0 || V <= 0 || d <= 0 || V > INT32_MAX || N > INT32_MAX) return SLP_ERR_INVALID_ARG;
   if (!temperature_ok(T)) return SLP_ERR_INVALID_ARG;
   if (N == 0) return SLP_OK;
@@ -50,7 +50,7 @@ int check_lmhead_args(const void* h, const void* W, int64_t N, int64_t V, int64_
   if (d % 64 != 0) return SLP_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(h) & 15u) || (reinterpret_cast<uintptr_t>(W) & 15u))
     return SLP_ERR_MISALIGNED;
-  if (ws == nullptr || ws_bytes < slp::lmhead_workspace_size(N, V, d)) return SLP_ERR_WORKSPACE;
+  if (ws == nullptr || ws_bytes < ws_need) return SLP_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(ws) & 255u) return SLP_ERR_MISALIGNED;
   return SLP_OK;
 }
@@ -83,14 +83,20 @@ int slp_backward(const void* x, int dtype, int64_t N, int64_t V, int64_t ld, con
 }
 
 size_t slp_lmhead_workspace_size(int64_t N, int64_t V, int64_t d) {
-  if (N < 0 || V <= 0 || d <= 0 || V > INT32_MAX || N > INT32_MAX) return 0;
+  if (N < 0 || V <= 0 || d <= 0 || V > INT32_MAX || N > INT32_MAX || d > INT32_MAX) return 0;
   return slp::lmhead_workspace_size(N, V, d);
+}
+
+size_t slp_lmhead_forward_workspace_size(int64_t N, int64_t V, int64_t d) {
+  if (N < 0 || V <= 0 || d <= 0 || V > INT32_MAX || N > INT32_MAX || d > INT32_MAX) return 0;
+  return slp::lmhead_forward_workspace_size(N, V, d);
 }
 
 int slp_lmhead_forward(const void* h, const void* W, int64_t N, int64_t V, int64_t d,
                        const int32_t* t, const uint8_t* mask, float T, float* logprob,
                        float* lse, void* ws, size_t ws_bytes, int32_t* err, void* stream) {
-  int st = check_lmhead_args(h, W, N, V, d, t, T, ws, ws_bytes);
+  int st = check_lmhead_args(h, W, N, V, d, t, T, ws, ws_bytes,
+                             slp::lmhead_forward_workspace_size(N, V, d));
   if (st != SLP_OK) return st;
   if (N == 0) return SLP_OK;
   if (logprob == nullptr || lse == nullptr) return SLP_ERR_INVALID_ARG;
@@ -102,7 +108,8 @@ int slp_lmhead_backward(const void* h, const void* W, int64_t N, int64_t V, int6
                         const int32_t* t, const uint8_t* mask, float T, const float* lse,
                         const float* grad_out, void* dh, void* dW, void* ws, size_t ws_bytes,
                         int32_t* err, void* stream) {
-  int st = check_lmhead_args(h, W, N, V, d, t, T, ws, ws_bytes);
+  int st = check_lmhead_args(h, W, N, V, d, t, T, ws, ws_bytes,
+                             slp::lmhead_workspace_size(N, V, d));
   if (st != SLP_OK) return st;
   if (N == 0) return SLP_OK;
   if (lse == nullptr || grad_out == nullptr || dh == nullptr || dW == nullptr)

@@ -5,6 +5,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include "slp.h"
+
 namespace slp {
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -124,6 +126,49 @@ __device__ __forceinline__ Lse2 lse2_warp_reduce(Lse2 v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = lse2_merge(v, lse2_shfl_xor(v, o));
   return v;
+}
+
+// Fold K logits into the running state: one max over the batch, a rescale
+// only when the max grows, then K exponentials against the current offset.
+// Partial sums are kept per batch so the long running sum sees few additions.
+template <int K>
+__device__ __forceinline__ void lse2_fold(Lse2& st, const float* f, float c) {
+  float bm = f[0];
+#pragma unroll
+  for (int k = 1; k < K; ++k) bm = fmaxf(bm, f[k]);
+  if (bm > st.m) {
+    const float nmc = __fmul_rn(bm, c);  // rounded product: the stored offset
+    st.s *= ex2(st.mc - nmc);
+    st.m = bm;
+    st.mc = nmc;
+  }
+  if (st.m != -INFINITY) {
+    float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int k = 0; k < K; ++k) a[k & 3] += ex2(fmaf(f[k], c, -st.mc));
+    st.s += (a[0] + a[1]) + (a[2] + a[3]);
+  }
+}
+
+// Row result from the merged state.  ln sum_v exp((x_v - m)/T) is recovered
+// from the base-2 sum and the exact rounding residual of the offset.
+__device__ __forceinline__ void write_row_result(const Lse2& a, float xt, bool tvalid, float T,
+                                                 float c, float* logprob, float* lse,
+                                                 int32_t* err, int64_t row) {
+  float lp, l;
+  if (!tvalid) {
+    if (err) atomicOr(err, SLP_DATA_ERR_TARGET);
+    lp = l = __int_as_float(0x7FC00000);
+  } else if (!(a.s > 0.f) || a.m == -INFINITY) {
+    lp = l = __int_as_float(0x7FC00000);  // all -inf (or NaN) row
+  } else {
+    const float r = fmaf(a.m, c, -a.mc);  // m*c - mc, exact
+    const float ln_s = (log2f(a.s) - r) * kLn2;
+    l = a.m / T + ln_s;
+    lp = (xt - a.m) / T - ln_s;
+  }
+  logprob[row] = lp;
+  lse[row] = l;
 }
 
 // ---- thread-block cluster helpers (distributed shared memory) --------------

@@ -23,6 +23,7 @@ cudaError_t launch_backward(const void* x, int dtype, int64_t N, int64_t V, int6
 
 // Fused LM-head path (slp_lmhead.cu).
 size_t lmhead_workspace_size(int64_t N, int64_t V, int64_t d);
+size_t lmhead_forward_workspace_size(int64_t N, int64_t V, int64_t d);
 
 cudaError_t launch_lmhead_forward(const void* h, const void* W, int64_t N, int64_t V, int64_t d,
                                   const int32_t* t, const uint8_t* mask, float T,

@@ -1,20 +1,765 @@
-// Fused LM-head path (not built yet).
+// Fused LM-head path: selected-token log-probabilities of z = h W^T / T
+// without storing the logits, computing only rows whose loss mask is 1 (slime
+// issue #2253, maintainer analysis: keep trainable rows before the vocabulary
+// projection, compute compact rows, scatter scalars back).
+//
+// Forward
+//   1. scan    : mask -> pos[N] (compact index or -1), idx[Na], Na     (1 CTA)
+//   2. gather  : h_c[i] = h[idx[i]], rows Na..roundup(Na,128) zeroed
+//   3. GEMM    : persistent tcgen05 kernel, 128 x 256 tiles of h_c W^T with
+//                fp32 accumulators in TMEM; the epilogue warps keep an online
+//                (max, sum-exp) per row over a slab of vocabulary tiles and
+//                catch the target logit; one partial per (slab, row)
+//   4. combine : merge the slab partials of each row in slab order, scatter
+//                logprob/lse to the original rows (inactive rows -> 0)
+// Backward
+//   1-2. scan + gather as above
+//   3. GEMM (recompute): same tiles; the epilogue writes
+//        dz = g/T (1[v == t] - 2^(x*c - lse*log2 e)) as bf16 (rows >= Na: 0)
+//   4. GEMM dh_part[ks] = dz[:, K-slice] W[K-slice, :]  (split-K, fp32)
+//   5. reduce  : dh[r] = bf16(sum_ks dh_part[ks][pos[r]]) (inactive rows 0)
+//   6. GEMM dW = dz^T h_c (K = compact rows), bf16 stores
+//
+// GEMM kernel layout (one CTA per SM, 256 threads): warp 0 issues TMA loads
+// into a 4-stage shared-memory ring (128-byte swizzle), warp 1 issues
+// tcgen05.mma (M=128, N=256, K=16) into one of two TMEM accumulators, warp 2
+// owns the TMEM allocation, warps 4-7 are the epilogue (TMEM lane = row, so
+// every row reduction is thread-local).  Every mbarrier wait gives up after
+// about two seconds, sets SLP_DEVICE_ERR_TIMEOUT and lets the CTA drain and
+// free its TMEM instead of hanging.
+
+#include "slp.h"
+#include "slp_device.cuh"
 #include "slp_internal.h"
+#include "slp_sm100.cuh"
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
 
 namespace slp {
+namespace lmh {
 
-size_t lmhead_workspace_size(int64_t, int64_t, int64_t) { return 256; }
+constexpr int BM = 128;   // rows of a tile (TMEM lanes)
+constexpr int BN = 256;   // columns of a tile (TMEM columns per accumulator)
+constexpr int BK = 64;    // K per stage: 64 bf16 = one 128-byte swizzle row
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int kThreads = 256;
+constexpr uint32_t kTmemCols = 2 * BN;
+constexpr int kSmemBytes = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr int kSlabCap = 256;  // most vocabulary slabs per row (forward partials)
+constexpr int kKSplitCap = 24;  // most K splits of the dh GEMM
 
-cudaError_t launch_lmhead_forward(const void*, const void*, int64_t, int64_t, int64_t,
-                                  const int32_t*, const uint8_t*, float, float*, float*, void*,
-                                  int32_t*, cudaStream_t) {
-  return cudaErrorNotSupported;
+enum Epi { EPI_LSE = 0, EPI_DZ = 1, EPI_F32 = 2, EPI_BF16 = 3 };
+
+__host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+// Work decomposition of one GEMM launch, a pure function of the sizes and of
+// the grid, evaluated identically by every CTA and by the follow-up kernels.
+struct Sched {
+  int m_tiles, n_tiles, k_blocks, S, units;
+};
+
+// Slabs of vocabulary tiles per row block: the S minimising the tile count of
+// the busiest CTA (ties -> fewer slabs, i.e. fewer partials).
+__host__ __device__ inline int choose_slabs(int m_tiles, int n_tiles, int G) {
+  int best = 1;
+  long long best_cost = -1;
+  const int smax = n_tiles < kSlabCap ? n_tiles : kSlabCap;
+  for (int S = 1; S <= smax; ++S) {
+    const long long cost = static_cast<long long>(cdiv(m_tiles * S, G)) * cdiv(n_tiles, S);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = S;
+    }
+  }
+  return best;
 }
 
-cudaError_t launch_lmhead_backward(const void*, const void*, int64_t, int64_t, int64_t,
-                                   const int32_t*, const uint8_t*, float, const float*,
-                                   const float*, void*, void*, void*, int32_t*, cudaStream_t) {
-  return cudaErrorNotSupported;
+// K splits of the dh GEMM: balance the busiest CTA, with at least s_min
+// splits so that one K-slice of W (V/S rows x d) stays in L2 while every row
+// block reads it.
+__host__ __device__ inline int choose_ksplits(int tiles, int k_blocks, int G, int s_min) {
+  int best = 1;
+  long long best_cost = -1;
+  int lo = s_min < 1 ? 1 : s_min;
+  if (lo > kKSplitCap) lo = kKSplitCap;
+  if (lo > k_blocks) lo = k_blocks > 0 ? k_blocks : 1;
+  const int hi = k_blocks < kKSplitCap ? (k_blocks > 0 ? k_blocks : 1) : kKSplitCap;
+  for (int S = lo; S <= hi; ++S) {
+    const long long cost = static_cast<long long>(cdiv(tiles * S, G)) * cdiv(k_blocks, S);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = S;
+    }
+  }
+  return best;
+}
+
+__host__ __device__ inline int ksplit_min(int V, int d) {
+  // keep a K-slice of W under ~48 MB (a third of L2)
+  const long long bytes = static_cast<long long>(V) * d * 2;
+  return static_cast<int>((bytes + (48ll << 20) - 1) / (48ll << 20));
+}
+
+__host__ __device__ inline Sched make_sched(int epi, int Na, int V, int d, int G) {
+  Sched s{};
+  if (epi == EPI_LSE || epi == EPI_DZ) {
+    s.m_tiles = cdiv(Na, BM);
+    s.n_tiles = cdiv(V, BN);
+    s.k_blocks = d / BK;
+    s.S = choose_slabs(s.m_tiles, s.n_tiles, G);
+    s.units = s.m_tiles * s.S;
+  } else if (epi == EPI_F32) {
+    s.m_tiles = cdiv(Na, BM);
+    s.n_tiles = cdiv(d, BN);
+    s.k_blocks = cdiv(V, BK);
+    s.S = choose_ksplits(s.m_tiles * s.n_tiles, s.k_blocks, G, ksplit_min(V, d));
+    s.units = s.m_tiles * s.n_tiles * s.S;
+  } else {
+    s.m_tiles = cdiv(V, BM);
+    s.n_tiles = cdiv(d, BN);
+    s.k_blocks = cdiv(Na, BM) * (BM / BK);
+    s.S = 1;
+    s.units = s.m_tiles * s.n_tiles;
+  }
+  return s;
+}
+
+struct Unit {
+  int m, n0, n1, k0, k1, slab;
+};
+
+__device__ __forceinline__ Unit decode(const Sched& s, int epi, int u) {
+  Unit w;
+  if (epi == EPI_LSE || epi == EPI_DZ) {
+    w.slab = u / s.m_tiles;
+    w.m = u - w.slab * s.m_tiles;
+    w.n0 = static_cast<int>(static_cast<long long>(w.slab) * s.n_tiles / s.S);
+    w.n1 = static_cast<int>(static_cast<long long>(w.slab + 1) * s.n_tiles / s.S);
+    w.k0 = 0;
+    w.k1 = s.k_blocks;
+  } else if (epi == EPI_F32) {
+    const int mn = s.m_tiles * s.n_tiles;
+    w.slab = u / mn;  // K split
+    const int r = u - w.slab * mn;
+    w.m = r / s.n_tiles;
+    w.n0 = r - w.m * s.n_tiles;
+    w.n1 = w.n0 + 1;
+    w.k0 = static_cast<int>(static_cast<long long>(w.slab) * s.k_blocks / s.S);
+    w.k1 = static_cast<int>(static_cast<long long>(w.slab + 1) * s.k_blocks / s.S);
+  } else {
+    w.slab = 0;
+    w.m = u / s.n_tiles;
+    w.n0 = u - w.m * s.n_tiles;
+    w.n1 = w.n0 + 1;
+    w.k0 = 0;
+    w.k1 = s.k_blocks;
+  }
+  return w;
+}
+
+struct Params {
+  int V, d, N, Mcap;
+  int G;                      // grid size the schedule was made for
+  const int32_t* counters;    // [0] = Na
+  const int32_t* idx;         // compact row -> original row
+  const int32_t* t;           // [N] targets
+  const float* g;             // [N] upstream gradient (backward)
+  const float* lse;           // [N] saved lse (backward)
+  float c;                    // log2(e) / T
+  float invT;
+  float* part_m;              // [kSlabCap][Mcap] forward partials
+  float* part_mc;
+  float* part_s;
+  float* part_xt;
+  __nv_bfloat16* dz;          // [Mcap][ld_dz]
+  long long ld_dz;
+  float* part_f32;            // [kKSplitCap][Mcap][d]
+  __nv_bfloat16* out;         // dW [V][d]
+  int32_t* err;
+};
+
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float (&v)[32]) {
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    float f[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) f[j] = v[q * 8 + j];
+    d4[q] = Elem<__nv_bfloat16>::pack(f);
+  }
+}
+
+// v[i] for a run-time i in [0, 32) as a tree of selects on the bits of i, so
+// the 32 values stay in registers (no indexed local-memory copy).
+__device__ __forceinline__ float select32(const float (&v)[32], int i) {
+  float a[16], b[8], c[4], d[2];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) a[j] = (i & 16) ? v[j + 16] : v[j];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) b[j] = (i & 8) ? a[j + 8] : a[j];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) c[j] = (i & 4) ? b[j + 4] : b[j];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) d[j] = (i & 2) ? c[j + 2] : c[j];
+  return (i & 1) ? d[1] : d[0];
+}
+
+template <int kEpi, bool kAmn, bool kBmn>
+__global__ void __launch_bounds__(kThreads, 1)
+    lmh_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                    const __grid_constant__ CUtensorMap tmB, const Params p) {
+  using namespace sm100;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 4);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t bar_full = smem_u32(bars);
+  const uint32_t bar_empty = bar_full + 8 * STAGES;
+  const uint32_t bar_accf = bar_full + 16 * STAGES;
+  const uint32_t bar_acce = bar_accf + 16;
+  const uint32_t ring = smem_u32(smem);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_accf + 8 * b, 1);
+      mbar_init(bar_acce + 8 * b, 4);  // one arrival per epilogue warp
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 2) tmem_alloc(smem_u32(tmem_holder), kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  const int Na = p.counters[0];
+  const Sched sc = make_sched(kEpi, Na, p.V, p.d, p.G);
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      int it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < sc.units && ok; u += gridDim.x) {
+        const Unit w = decode(sc, kEpi, u);
+        for (int n = w.n0; n < w.n1 && ok; ++n) {
+          for (int kb = w.k0; kb < w.k1; ++kb, ++it) {
+            const int s = it % STAGES;
+            const uint32_t ph = (it / STAGES) & 1;
+            if (!mbar_wait_bounded(bar_empty + 8 * s, ph ^ 1, abort_flag, kWaitLimitNs)) {
+              ok = false;
+              break;
+            }
+            const uint32_t fb = bar_full + 8 * s;
+            mbar_arrive_expect_tx(fb, STAGE_BYTES);
+            const uint32_t a_dst = ring + s * STAGE_BYTES;
+            const uint32_t b_dst = a_dst + A_BYTES;
+            if (!kAmn) {
+              tma_load_2d(a_dst, &tmA, kb * BK, w.m * BM, fb);
+            } else {
+#pragma unroll
+              for (int j = 0; j < BM / 64; ++j)
+                tma_load_2d(a_dst + j * 8192, &tmA, w.m * BM + 64 * j, kb * BK, fb);
+            }
+            if (!kBmn) {
+              tma_load_2d(b_dst, &tmB, kb * BK, n * BN, fb);
+            } else {
+#pragma unroll
+              for (int j = 0; j < BN / 64; ++j)
+                tma_load_2d(b_dst + j * 8192, &tmB, n * BN + 64 * j, kb * BK, fb);
+            }
+          }
+        }
+      }
+      if (!ok) {
+        // drain: wait (bounded, ignoring the abort flag) for the copies issued
+        // into the last STAGES slots before the CTA may exit
+        for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
+          mbar_wait_bounded(bar_full + 8 * (j % STAGES), (j / STAGES) & 1, nullptr,
+                            kWaitLimitNs);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t idesc = umma_idesc_bf16(BM, BN, kAmn, kBmn);
+      int it = 0, tc = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < sc.units && ok; u += gridDim.x) {
+        const Unit w = decode(sc, kEpi, u);
+        for (int n = w.n0; n < w.n1 && ok; ++n, ++tc) {
+          const int buf = tc & 1;
+          if (!mbar_wait_bounded(bar_acce + 8 * buf, ((tc >> 1) & 1) ^ 1, abort_flag,
+                                 kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + buf * BN;
+          for (int kb = w.k0; kb < w.k1; ++kb, ++it) {
+            const int s = it % STAGES;
+            if (!mbar_wait_bounded(bar_full + 8 * s, (it / STAGES) & 1, abort_flag,
+                                   kWaitLimitNs)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_addr = ring + s * STAGE_BYTES;
+            const uint32_t b_addr = a_addr + A_BYTES;
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k) {
+              const uint64_t ad = kAmn ? umma_desc_sw128(a_addr + k * 2048, 8192, 1024)
+                                       : umma_desc_sw128(a_addr + k * 32, 16, 1024);
+              const uint64_t bd = kBmn ? umma_desc_sw128(b_addr + k * 2048, 8192, 1024)
+                                       : umma_desc_sw128(b_addr + k * 32, 16, 1024);
+              mma_bf16(d_tmem, ad, bd, idesc, (kb > w.k0 || k > 0) ? 1u : 0u);
+            }
+            mma_commit(bar_empty + 8 * s);  // frees the stage once these MMAs finish
+          }
+          if (!ok) break;
+          mma_commit(bar_accf + 8 * buf);  // accumulator ready for the epilogue
+        }
+      }
+    }
+  } else if (warp >= 4) {
+    // ---------------- epilogue ----------------
+    const int q = warp & 3;
+    const int rit = q * 32 + lane;  // row within the tile = TMEM lane
+    int tc = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < sc.units && ok; u += gridDim.x) {
+      const Unit w = decode(sc, kEpi, u);
+      const int row = w.m * BM + rit;
+      // per-row constants
+      bool valid = false;
+      int tr = -1;
+      float coef = 0.f, L2 = 0.f;
+      Lse2 st = lse2_empty();
+      float xt = __int_as_float(0x7FC00000);
+      if (kEpi == EPI_LSE || kEpi == EPI_DZ) {
+        valid = row < Na;
+        if (valid) {
+          const int orig = p.idx[row];
+          tr = p.t[orig];
+          if (tr < 0 || tr >= p.V) {
+            tr = -1;  // invalid target: no gradient contribution, flagged elsewhere
+          } else if (kEpi == EPI_DZ) {
+            coef = p.g[orig] * p.invT;
+            L2 = p.lse[orig] * kLog2e;
+          }
+        }
+      }
+      for (int n = w.n0; n < w.n1; ++n, ++tc) {
+        const int buf = tc & 1;
+        // every lane waits; the warp then agrees, so no lane reaches the
+        // warp-wide tcgen05.ld alone
+        const bool got = mbar_wait_bounded(bar_accf + 8 * buf, (tc >> 1) & 1, abort_flag,
+                                           kWaitLimitNs);
+        if (!__all_sync(0xFFFFFFFFu, got)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN;
+        const bool empty_k = w.k1 <= w.k0;
+#pragma unroll 1
+        for (int ch = 0; ch < BN / 32; ++ch) {
+          uint32_t r[32];
+          tmem_ld_32cols(taddr + ch * 32, r);
+          tmem_ld_wait();
+          float v[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = empty_k ? 0.f : __uint_as_float(r[j]);
+          const int col0 = n * BN + ch * 32;
+          if (kEpi == EPI_LSE) {
+            if (col0 + 32 > p.V) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (col0 + j >= p.V) v[j] = -INFINITY;
+            }
+            if (tr >= col0 && tr < col0 + 32) xt = select32(v, tr - col0);
+            if (col0 < p.V) lse2_fold<32>(st, v, p.c);
+          } else if (kEpi == EPI_DZ) {
+            if (col0 < p.V) {
+              float o[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const float pr = ex2(fmaf(v[j], p.c, -L2));
+                o[j] = (col0 + j == tr) ? fmaf(-coef, pr, coef) : -coef * pr;
+                if (!valid || tr < 0) o[j] = 0.f;
+              }
+              __nv_bfloat16* dst = p.dz + static_cast<long long>(row) * p.ld_dz + col0;
+              if (col0 + 32 <= p.V) {
+                store_bf16x32(dst, o);
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  if (col0 + j < p.V) dst[j] = __float2bfloat16_rn(o[j]);
+              }
+            }
+          } else if (kEpi == EPI_F32) {
+            if (row < Na && col0 < p.d) {
+              float* dst = p.part_f32 +
+                           (static_cast<long long>(w.slab) * p.Mcap + row) * p.d + col0;
+              float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                d4[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            }
+          } else {  // EPI_BF16
+            if (row < p.V && col0 < p.d)
+              store_bf16x32(p.out + static_cast<long long>(row) * p.d + col0, v);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_acce + 8 * buf);
+      }
+      if (kEpi == EPI_LSE && ok && valid) {
+        const long long o = static_cast<long long>(w.slab) * p.Mcap + row;
+        p.part_m[o] = st.m;
+        p.part_mc[o] = st.mc;
+        p.part_s[o] = st.s;
+        p.part_xt[o] = xt;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+  if (threadIdx.x == 0 && *abort_flag && p.err != nullptr) atomicOr(p.err, SLP_DEVICE_ERR_TIMEOUT);
+}
+
+// ---- compaction ---------------------------------------------------------------
+
+__global__ void __launch_bounds__(1024)
+    lmh_scan_kernel(const uint8_t* __restrict__ mask, int N, int32_t* __restrict__ counters,
+                    int32_t* __restrict__ pos, int32_t* __restrict__ idx) {
+  __shared__ int warp_sums[32];
+  __shared__ int carry;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  for (int base = 0; base < N; base += 1024) {
+    const int r = base + threadIdx.x;
+    const int f = (r < N) && (mask == nullptr || mask[r] != 0) ? 1 : 0;
+    int v = f;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, v, o);
+      if (lane >= o) v += y;
+    }
+    if (lane == 31) warp_sums[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+      int w = warp_sums[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, w, o);
+        if (lane >= o) w += y;
+      }
+      warp_sums[lane] = w;
+    }
+    __syncthreads();
+    const int excl = carry + (warp > 0 ? warp_sums[warp - 1] : 0) + v - f;
+    if (r < N) {
+      pos[r] = f ? excl : -1;
+      if (f) idx[excl] = r;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) carry += warp_sums[31];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) counters[0] = carry;
+}
+
+// CTA b < N copies active row b of h to its compact slot; CTA N + j zeroes
+// compact row Na + j when it lies below roundup(Na, BM).
+__global__ void __launch_bounds__(256)
+    lmh_gather_kernel(const __nv_bfloat16* __restrict__ h, int N, int d,
+                      const int32_t* __restrict__ counters, const int32_t* __restrict__ pos,
+                      __nv_bfloat16* __restrict__ hc) {
+  const int b = blockIdx.x;
+  const int nv = d / 8;  // 16-byte vectors per row
+  int dst_row;
+  const uint4* src = nullptr;
+  if (b < N) {
+    dst_row = pos[b];
+    if (dst_row < 0) return;
+    src = reinterpret_cast<const uint4*>(h + static_cast<long long>(b) * d);
+  } else {
+    const int Na = counters[0];
+    dst_row = Na + (b - N);
+    if (dst_row >= cdiv(Na, BM) * BM) return;
+  }
+  uint4* dst = reinterpret_cast<uint4*>(hc + static_cast<long long>(dst_row) * d);
+  for (int i = threadIdx.x; i < nv; i += blockDim.x)
+    dst[i] = src ? src[i] : make_uint4(0u, 0u, 0u, 0u);
+}
+
+// ---- forward combine ------------------------------------------------------------
+
+__global__ void __launch_bounds__(256)
+    lmh_fwd_combine_kernel(const Params p, const int32_t* __restrict__ pos, float T,
+                           float* __restrict__ logprob, float* __restrict__ lse) {
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= p.N) return;
+  const int i = pos[r];
+  if (i < 0) {
+    logprob[r] = 0.f;
+    lse[r] = 0.f;
+    return;
+  }
+  const Sched sc = make_sched(EPI_LSE, p.counters[0], p.V, p.d, p.G);
+  const int tt = p.t[r];
+  const bool tvalid = tt >= 0 && tt < p.V;
+  Lse2 acc = lse2_empty();
+  float xt = 0.f;
+  const int ttile = tvalid ? tt / BN : -1;
+  for (int s = 0; s < sc.S; ++s) {
+    const long long o = static_cast<long long>(s) * p.Mcap + i;
+    acc = lse2_merge(acc, Lse2{p.part_m[o], p.part_mc[o], p.part_s[o]});
+    const int n0 = static_cast<int>(static_cast<long long>(s) * sc.n_tiles / sc.S);
+    const int n1 = static_cast<int>(static_cast<long long>(s + 1) * sc.n_tiles / sc.S);
+    if (ttile >= n0 && ttile < n1) xt = p.part_xt[o];
+  }
+  write_row_result(acc, xt, tvalid, T, p.c, logprob, lse, p.err, r);
+}
+
+// ---- dh reduction -------------------------------------------------------------
+
+__global__ void __launch_bounds__(256)
+    lmh_dh_reduce_kernel(const Params p, const int32_t* __restrict__ pos,
+                         __nv_bfloat16* __restrict__ dh) {
+  const int r = blockIdx.x;
+  const int i = pos[r];
+  __nv_bfloat16* out = dh + static_cast<long long>(r) * p.d;
+  const int tt = p.t[r];
+  const bool bad = i >= 0 && (tt < 0 || tt >= p.V);
+  if (bad && threadIdx.x == 0 && p.err != nullptr) atomicOr(p.err, SLP_DATA_ERR_TARGET);
+  const Sched sc = make_sched(EPI_F32, p.counters[0], p.V, p.d, p.G);
+  for (int j = threadIdx.x * 4; j < p.d; j += blockDim.x * 4) {
+    float a[4] = {0.f, 0.f, 0.f, 0.f};
+    if (i >= 0) {
+      for (int s = 0; s < sc.S; ++s) {
+        const float4 v = *reinterpret_cast<const float4*>(
+            p.part_f32 + (static_cast<long long>(s) * p.Mcap + i) * p.d + j);
+        a[0] += v.x;
+        a[1] += v.y;
+        a[2] += v.z;
+        a[3] += v.w;
+      }
+      if (bad) a[0] = a[1] = a[2] = a[3] = __int_as_float(0x7FC00000);
+    }
+    __nv_bfloat162 lo = __floats2bfloat162_rn(a[0], a[1]);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(a[2], a[3]);
+    uint2 w;
+    w.x = *reinterpret_cast<uint32_t*>(&lo);
+    w.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(out + j) = w;
+  }
+}
+
+// ---- host side ------------------------------------------------------------------
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor [outer][inner] (row stride row_bytes), 128-byte swizzled box
+// of box_inner x box_outer elements; reads outside the tensor return zeros.
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+              uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct Layout {
+  int Mcap;
+  long long ld_dz;
+  size_t off_counters, off_pos, off_idx, off_hc, off_pm, off_pmc, off_ps, off_pxt, fwd_end;
+  size_t off_dz, off_pf32, bwd_end;
+};
+
+Layout layout(int64_t N, int64_t V, int64_t d) {
+  Layout L{};
+  L.Mcap = static_cast<int>(cdiv(static_cast<int>(N), BM) * BM);
+  L.ld_dz = (V + 63) / 64 * 64;
+  size_t o = 0;
+  L.off_counters = o; o += 256;
+  L.off_pos = o; o = align256(o + 4 * static_cast<size_t>(N));
+  L.off_idx = o; o = align256(o + 4 * static_cast<size_t>(L.Mcap));
+  L.off_hc = o; o = align256(o + 2 * static_cast<size_t>(L.Mcap) * d);
+  const size_t part = 4 * static_cast<size_t>(kSlabCap) * L.Mcap;
+  L.off_pm = o; o = align256(o + part);
+  L.off_pmc = o; o = align256(o + part);
+  L.off_ps = o; o = align256(o + part);
+  L.off_pxt = o; o = align256(o + part);
+  L.fwd_end = o;
+  L.off_dz = o; o = align256(o + 2 * static_cast<size_t>(L.Mcap) * L.ld_dz);
+  L.off_pf32 = o; o = align256(o + 4 * static_cast<size_t>(kKSplitCap) * L.Mcap * d);
+  L.bwd_end = o;
+  return L;
+}
+
+template <int kEpi, bool kAmn, bool kBmn>
+cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const Params& p,
+                        cudaStream_t stream) {
+  auto k = lmh_gemm_kernel<kEpi, kAmn, kBmn>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  k<<<p.G, kThreads, kSmemBytes, stream>>>(a, b, p);
+  return cudaGetLastError();
+}
+
+struct Prepared {
+  Layout L;
+  Params p;
+  int32_t* pos;
+  __nv_bfloat16* hc;
+};
+
+cudaError_t prepare(const void* h, int64_t N, int64_t V, int64_t d, const int32_t* t,
+                    const uint8_t* mask, float T, void* ws, int32_t* err, cudaStream_t stream,
+                    Prepared* out) {
+  Prepared& P = *out;
+  P.L = layout(N, V, d);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  int32_t* counters = reinterpret_cast<int32_t*>(w + P.L.off_counters);
+  P.pos = reinterpret_cast<int32_t*>(w + P.L.off_pos);
+  int32_t* idx = reinterpret_cast<int32_t*>(w + P.L.off_idx);
+  P.hc = reinterpret_cast<__nv_bfloat16*>(w + P.L.off_hc);
+  Params& p = P.p;
+  p = Params{};
+  p.V = static_cast<int>(V);
+  p.d = static_cast<int>(d);
+  p.N = static_cast<int>(N);
+  p.Mcap = P.L.Mcap;
+  p.G = sm_count();
+  p.counters = counters;
+  p.idx = idx;
+  p.t = t;
+  p.c = static_cast<float>(1.4426950408889634 / static_cast<double>(T));
+  p.invT = 1.0f / T;
+  p.part_m = reinterpret_cast<float*>(w + P.L.off_pm);
+  p.part_mc = reinterpret_cast<float*>(w + P.L.off_pmc);
+  p.part_s = reinterpret_cast<float*>(w + P.L.off_ps);
+  p.part_xt = reinterpret_cast<float*>(w + P.L.off_pxt);
+  p.dz = reinterpret_cast<__nv_bfloat16*>(w + P.L.off_dz);
+  p.ld_dz = P.L.ld_dz;
+  p.part_f32 = reinterpret_cast<float*>(w + P.L.off_pf32);
+  p.err = err;
+  lmh_scan_kernel<<<1, 1024, 0, stream>>>(mask, p.N, counters, P.pos, idx);
+  lmh_gather_kernel<<<p.N + BM, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(h), p.N,
+                                                 p.d, counters, P.pos, P.hc);
+  return cudaGetLastError();
+}
+
+}  // namespace lmh
+
+size_t lmhead_forward_workspace_size(int64_t N, int64_t V, int64_t d) {
+  return lmh::layout(N, V, d).fwd_end;
+}
+
+size_t lmhead_workspace_size(int64_t N, int64_t V, int64_t d) {
+  return lmh::layout(N, V, d).bwd_end;
+}
+
+cudaError_t launch_lmhead_forward(const void* h, const void* W, int64_t N, int64_t V, int64_t d,
+                                  const int32_t* t, const uint8_t* mask, float T, float* logprob,
+                                  float* lse, void* ws, int32_t* err, cudaStream_t stream) {
+  using namespace lmh;
+  Prepared P;
+  cudaError_t e = prepare(h, N, V, d, t, mask, T, ws, err, stream, &P);
+  if (e != cudaSuccess) return e;
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, P.hc, d, P.L.Mcap, d * 2, BK, BM) ||
+      !make_map(&mb, W, d, V, d * 2, BK, BN))
+    return cudaErrorInvalidValue;
+  e = launch_gemm<EPI_LSE, false, false>(ma, mb, P.p, stream);
+  if (e != cudaSuccess) return e;
+  lmh_fwd_combine_kernel<<<cdiv(static_cast<int>(N), 256), 256, 0, stream>>>(P.p, P.pos, T,
+                                                                              logprob, lse);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lmhead_backward(const void* h, const void* W, int64_t N, int64_t V, int64_t d,
+                                   const int32_t* t, const uint8_t* mask, float T,
+                                   const float* lse, const float* grad_out, void* dh, void* dW,
+                                   void* ws, int32_t* err, cudaStream_t stream) {
+  using namespace lmh;
+  Prepared P;
+  cudaError_t e = prepare(h, N, V, d, t, mask, T, ws, err, stream, &P);
+  if (e != cudaSuccess) return e;
+  P.p.g = grad_out;
+  P.p.lse = lse;
+  P.p.out = static_cast<__nv_bfloat16*>(dW);
+  CUtensorMap m_hc_k, m_w_k, m_dz_k, m_w_mn, m_dz_mn, m_hc_mn;
+  const uint64_t dz_row = static_cast<uint64_t>(P.L.ld_dz) * 2;
+  if (!make_map(&m_hc_k, P.hc, d, P.L.Mcap, d * 2, BK, BM) ||     // A of recompute
+      !make_map(&m_w_k, W, d, V, d * 2, BK, BN) ||                // B of recompute
+      !make_map(&m_dz_k, P.p.dz, V, P.L.Mcap, dz_row, BK, BM) ||  // A of dh (K = V)
+      !make_map(&m_w_mn, W, d, V, d * 2, 64, BK) ||               // B of dh (N = d)
+      !make_map(&m_dz_mn, P.p.dz, V, P.L.Mcap, dz_row, 64, BK) || // A of dW (M = V)
+      !make_map(&m_hc_mn, P.hc, d, P.L.Mcap, d * 2, 64, BK))      // B of dW (N = d)
+    return cudaErrorInvalidValue;
+  e = launch_gemm<EPI_DZ, false, false>(m_hc_k, m_w_k, P.p, stream);
+  if (e != cudaSuccess) return e;
+  e = launch_gemm<EPI_F32, false, true>(m_dz_k, m_w_mn, P.p, stream);
+  if (e != cudaSuccess) return e;
+  lmh_dh_reduce_kernel<<<static_cast<int>(N), 256, 0, stream>>>(P.p, P.pos,
+                                                               static_cast<__nv_bfloat16*>(dh));
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_gemm<EPI_BF16, true, true>(m_dz_mn, m_hc_mn, P.p, stream);
 }
 
 }  // namespace slp
