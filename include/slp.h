@@ -188,6 +188,34 @@ int slp_lmhead_backward(const void* h, const void* W, int64_t N, int64_t V, int6
                         void* dh, void* dW,
                         void* ws, size_t ws_bytes, int32_t* err, void* stream);
 
+/*
+ * slp_lmhead_forward_noalloc - slp_lmhead_forward without a caller workspace.
+ *
+ * The source pages have no counterpart to this call; it exists for callers
+ * that cannot allocate device memory on demand: their framework owns every
+ * byte of device memory through its own pool or budget, or they call from a
+ * place where cudaMalloc (which synchronises the whole device) is not
+ * acceptable, so they cannot supply the workspace slp_lmhead_forward needs.
+ *
+ * Same arguments, results and errors as slp_lmhead_forward, minus ws and
+ * ws_bytes.  The scratch is one 16 MiB array inside the library's device
+ * image, present on every GPU that loads the library until the process
+ * exits.  Sizes whose forward workspace
+ * (slp_lmhead_forward_workspace_size(N, V, d)) exceeds 16 MiB are rejected
+ * with SLP_ERR_WORKSPACE before anything is launched; at d = 2560 and
+ * V = 151936 that allows up to N = 1792 rows.
+ *
+ * The call allocates nothing.  Its first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress, with that device current);
+ * make that first call before any stream capture.  All calls on a device
+ * share the array and leave their contents in it (no part has to start
+ * zeroed); calls whose work overlaps on the GPU race on it, so serialise
+ * them (for example on one stream).
+ */
+int slp_lmhead_forward_noalloc(const void* h, const void* W, int64_t N, int64_t V, int64_t d,
+                               const int32_t* t, const uint8_t* mask, float T,
+                               float* logprob, float* lse, int32_t* err, void* stream);
+
 /* Static, human-readable text for a slp_status value. */
 const char* slp_status_string(int status);
 

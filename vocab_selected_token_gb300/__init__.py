@@ -25,7 +25,7 @@ from ._lib import SlpError
 
 __all__ = [
     "SlpError", "slp_forward", "slp_backward", "slp_lmhead_workspace_size",
-    "slp_lmhead_forward_workspace_size",
+    "slp_lmhead_forward_workspace_size", "slp_lmhead_forward_noalloc",
     "slp_lmhead_forward", "slp_lmhead_backward", "selected_logprob",
     "lmhead_selected_logprob", "library_path",
 ]
@@ -139,6 +139,21 @@ def slp_lmhead_forward(h, W, t, mask=None, T: float = 1.0, logprob=None, lse=Non
     ws, nbytes = _workspace(N, V, d, ws, h.device, forward_only=True)
     _lib.call("slp_lmhead_forward", _ptr(h), _ptr(W), N, V, d, _ptr(t), _ptr(mask), float(T),
               _ptr(logprob), _ptr(lse), _ptr(ws), nbytes, _ptr(err), _stream_handle(stream))
+    return logprob, lse
+
+
+def slp_lmhead_forward_noalloc(h, W, t, mask, T: float, logprob, lse, err=None, stream=None):
+    """Fused LM-head forward into caller-provided outputs, using the library's
+    fixed 16 MiB device scratch instead of a workspace (for callers that cannot
+    allocate).  Calls that overlap on the GPU race on that scratch."""
+    N, V, d = _lmhead_check(h, W)
+    _check_vec("t", t, N, torch.int32)
+    if mask is not None:
+        _check_vec("mask", mask, N, torch.uint8)
+    _check_vec("logprob", logprob, N, torch.float32)
+    _check_vec("lse", lse, N, torch.float32)
+    _lib.call("slp_lmhead_forward_noalloc", _ptr(h), _ptr(W), N, V, d, _ptr(t), _ptr(mask),
+              float(T), _ptr(logprob), _ptr(lse), _ptr(err), _stream_handle(stream))
     return logprob, lse
 
 
