@@ -47,6 +47,9 @@ def parse():
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--no-extra", action="store_true", help="skip the other workloads' lines")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--lmhead-only", action="store_true",
+                   help="time only the fused LM-head path and print its numbers")
+    p.add_argument("--lmhead-rows", type=int, default=None)
     p.add_argument("--rows", type=int, default=None,
                    help="override N (same recipe), e.g. for a small profiling case")
     return p.parse_args()
@@ -355,6 +358,11 @@ def main():
     from vocab_selected_token_gb300 import workloads as W
     device = torch.device("cuda", torch.cuda.current_device())
     hbm, bf16_burst, bf16_sus, peak_src = peaks()
+    if args.lmhead_only:
+        r = time_lmhead(device, steps=args.steps, warmup=args.warmup, N=args.lmhead_rows)
+        if rank == 0:
+            print(json.dumps({"lmhead": r}), flush=True)
+        return
 
     inp = W.make_logits_inputs(args.config, device=device, N=args.rows)
     fwd_b, bwd_b, na = logits_bytes(inp.x, inp.mask)
@@ -430,7 +438,62 @@ def other_workloads(device, hbm):
         out[name]["step_frac_of_measured"] = out[name]["step_gbs"] / hbm
         del inp, r
         torch.cuda.empty_cache()
+    out["lmhead"] = time_lmhead(device)
     return out
+
+
+def time_lmhead(device, steps=10, warmup=3, N=None):
+    """Fused LM-head forward and backward on the lmhead workload (N=8192,
+    d=2560, V=151936, Bernoulli(0.5) mask), each call timed whole with CUDA
+    events; TFLOP/s counts 2*Na*V*d for the forward and 6*Na*V*d for the
+    backward (logits recompute, dh and dW GEMMs)."""
+    from vocab_selected_token_gb300 import _lib
+    from vocab_selected_token_gb300 import workloads as W
+    lib = _lib.load()
+    a = W.make_lmhead_inputs(device=device, N=N)
+    Nn, d = a.h.shape
+    V = a.W.shape[0]
+    na = int(a.mask.sum().item())
+    ws_b = lib.slp_lmhead_workspace_size(Nn, V, d)
+    ws = torch.empty(ws_b, dtype=torch.uint8, device=device)
+    lp = torch.empty(Nn, device=device)
+    lse = torch.empty(Nn, device=device)
+    dh = torch.empty((Nn, d), dtype=torch.bfloat16, device=device)
+    dW = torch.empty((V, d), dtype=torch.bfloat16, device=device)
+    sh = torch.cuda.current_stream(device).cuda_stream
+    s = torch.cuda.current_stream(device)
+    fa = (a.h.data_ptr(), a.W.data_ptr(), Nn, V, d, a.t.data_ptr(), a.mask.data_ptr(), float(a.T),
+          lp.data_ptr(), lse.data_ptr(), ws.data_ptr(), ws_b, None, sh)
+    ba = (a.h.data_ptr(), a.W.data_ptr(), Nn, V, d, a.t.data_ptr(), a.mask.data_ptr(), float(a.T),
+          lse.data_ptr(), a.g.data_ptr(), dh.data_ptr(), dW.data_ptr(), ws.data_ptr(), ws_b, None, sh)
+    for _ in range(warmup):
+        assert lib.slp_lmhead_forward(*fa) == 0
+        assert lib.slp_lmhead_backward(*ba) == 0
+    torch.cuda.synchronize(device)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for i in range(steps):
+        ev[i][0].record(s)
+        assert lib.slp_lmhead_forward(*fa) == 0
+        ev[i][1].record(s)
+        assert lib.slp_lmhead_backward(*ba) == 0
+        ev[i][2].record(s)
+    torch.cuda.synchronize(device)
+    f_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
+    b_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / steps
+    flop_f = 2.0 * na * V * d
+    _, peak, peak_sus, src = peaks()
+    res = {"N": Nn, "V": V, "d": d, "active_rows": na, "fwd_ms": f_ms, "bwd_ms": b_ms,
+           "fwd_tflops": flop_f / (f_ms * 1e-3) / 1e12,
+           "bwd_tflops": 3 * flop_f / (b_ms * 1e-3) / 1e12,
+           "step_tflops": 4 * flop_f / ((f_ms + b_ms) * 1e-3) / 1e12,
+           "peak_bf16_tflops": peak, "peak_source": src,
+           "workspace_bytes": int(ws_b)}
+    res["fwd_frac"] = res["fwd_tflops"] / peak
+    res["bwd_frac"] = res["bwd_tflops"] / peak
+    res["step_frac"] = res["step_tflops"] / peak
+    del a, ws, dh, dW
+    torch.cuda.empty_cache()
+    return res
 
 
 if __name__ == "__main__":
