@@ -2,13 +2,16 @@
 // backward ((onehot - softmax) * g / T with the softmax recomputed from the
 // saved lse), both streaming kernels bound by HBM bandwidth.
 //
-// Forward: one CTA (or a thread-block cluster of `splits` CTAs) per row.
-// Each thread streams 16-byte vectors with read-once loads and folds them into
-// a running base-2 (max, sum-exp) state; warps merge by butterfly shuffles,
-// CTAs of a cluster merge through distributed shared memory.  The cluster is
-// the single-GPU form of the vocabulary-parallel exchange (torchforge PR #608,
-// "Implementation": all-reduce MAX, all-reduce SUM of exp(x - max), target
-// gathered by its owner only), with no global workspace.
+// Forward: one CTA per row (a thread-block cluster of `splits` CTAs per row
+// when there are too few rows to fill the GPU).  For 16-byte-aligned rows,
+// thread 0 streams the row segment into a 4 x 16 KB shared-memory ring with
+// cp.async.bulk copies completing on mbarriers, so ~64 KB per CTA is always
+// in flight while all 256 threads fold the landed chunks into a running
+// base-2 (max, sum-exp) state.  Warps merge by butterfly shuffles, CTAs of a
+// cluster through distributed shared memory: the single-GPU form of the
+// vocabulary-parallel exchange (torchforge PR #608, "Implementation":
+// all-reduce MAX, all-reduce SUM of exp(x - max), target gathered by its
+// owner only), with no global workspace.
 //
 // Backward: a flat grid of (row, column-tile) CTAs; each thread handles
 // kBwdUnroll 16-byte vectors, recomputes p = 2^(x*c - lse*log2 e) and writes
@@ -17,6 +20,7 @@
 #include "slp.h"
 #include "slp_device.cuh"
 #include "slp_internal.h"
+#include "slp_sm100.cuh"
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
@@ -25,7 +29,11 @@
 namespace slp {
 
 constexpr int kFwdThreads = 256;
-constexpr int kFwdUnroll = 4;  // 16-byte vectors in flight per thread per batch
+constexpr int kFwdUnroll = 4;  // elements per thread per batch on the scalar path
+constexpr int kFwdStages = 4;  // shared-memory ring of the vector path
+constexpr int kFwdChunk = 16384;  // bytes per bulk copy (4 vectors per thread)
+constexpr int kFwdSmem = kFwdStages * kFwdChunk;
+constexpr uint64_t kFwdWaitNs = 2000000000ull;
 constexpr int kBwdThreads = 256;
 constexpr int kBwdUnroll = 4;
 constexpr int kMaxSplits = 8;  // portable cluster size
@@ -61,23 +69,67 @@ __global__ void __launch_bounds__(kFwdThreads)
 
   Lse2 st = lse2_empty();
   if constexpr (kVecPath) {
+    extern __shared__ __align__(128) uint8_t ring[];
+    __shared__ __align__(8) uint64_t full[kFwdStages];
+    __shared__ int abort_flag;
     const int64_t nvec = V / kVec;
     const int64_t v0 = nvec * rank / splits;
     const int64_t v1 = nvec * (rank + 1) / splits;
-    const uint4* p = reinterpret_cast<const uint4*>(xr) + v0;
-    const int64_t n = v1 - v0;
+    const char* src = reinterpret_cast<const char*>(reinterpret_cast<const uint4*>(xr) + v0);
+    const int64_t nbytes = (v1 - v0) * 16;
+    const int64_t nch = (nbytes + kFwdChunk - 1) / kFwdChunk;
+    const uint32_t sbase = sm100::smem_u32(ring);
+    const uint32_t bbase = sm100::smem_u32(full);
+    if (threadIdx.x == 0) {
+      for (int s = 0; s < kFwdStages; ++s) sm100::mbar_init(bbase + 8 * s, 1);
+      abort_flag = 0;
+      sm100::fence_mbar_init();
+    }
+    __syncthreads();
+    // thread 0 keeps kFwdStages chunks of the segment in flight
+    auto issue = [&](int64_t ch) {
+      const int s = static_cast<int>(ch % kFwdStages);
+      const int64_t off = ch * kFwdChunk;
+      const uint32_t bytes = static_cast<uint32_t>(
+          nbytes - off < kFwdChunk ? nbytes - off : static_cast<int64_t>(kFwdChunk));
+      sm100::mbar_arrive_expect_tx(bbase + 8 * s, bytes);
+      sm100::bulk_load(sbase + s * kFwdChunk, src + off, bytes, bbase + 8 * s);
+    };
+    if (threadIdx.x == 0)
+      for (int64_t ch = 0; ch < kFwdStages && ch < nch; ++ch) issue(ch);
+    constexpr int kPer = kFwdChunk / 16 / kFwdThreads;
     const uint4 pad = make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord, E::kNegInfWord);
-    for (int64_t i0 = threadIdx.x; i0 < n; i0 += kFwdThreads * kFwdUnroll) {
-      uint4 buf[kFwdUnroll];
+    int64_t ch = 0;
+    for (; ch < nch; ++ch) {
+      const int s = static_cast<int>(ch % kFwdStages);
+      const bool got = sm100::mbar_wait_bounded(bbase + 8 * s, (ch / kFwdStages) & 1,
+                                                &abort_flag, kFwdWaitNs);
+      if (__syncthreads_or(!got)) break;
+      const int64_t off = ch * kFwdChunk;
+      const int nv = static_cast<int>(
+          (nbytes - off < kFwdChunk ? nbytes - off : static_cast<int64_t>(kFwdChunk)) / 16);
+      const uint4* q = reinterpret_cast<const uint4*>(ring + s * kFwdChunk);
+      float f[kPer][kVec];
 #pragma unroll
-      for (int u = 0; u < kFwdUnroll; ++u) {
-        const int64_t i = i0 + static_cast<int64_t>(u) * kFwdThreads;
-        buf[u] = (i < n) ? ld_stream(p + i) : pad;
+      for (int u = 0; u < kPer; ++u) {
+        const int i = u * kFwdThreads + threadIdx.x;
+        E::unpack(i < nv ? q[i] : pad, f[u]);
       }
-      float f[kFwdUnroll][kVec];
-#pragma unroll
-      for (int u = 0; u < kFwdUnroll; ++u) E::unpack(buf[u], f[u]);
-      lse2_fold<kFwdUnroll * kVec>(st, &f[0][0], c);
+      __syncthreads();  // stage s fully read: thread 0 may refill it
+      if (threadIdx.x == 0 && ch + kFwdStages < nch) issue(ch + kFwdStages);
+      lse2_fold<kPer * kVec>(st, &f[0][0], c);
+    }
+    if (ch < nch) {
+      // a copy never landed: report it and wait (bounded) for the copies in
+      // flight so the CTA does not exit under them
+      if (threadIdx.x == 0) {
+        if (err != nullptr) atomicOr(err, SLP_DEVICE_ERR_TIMEOUT);
+        const int64_t last = (ch + kFwdStages < nch ? ch + kFwdStages : nch);
+        for (int64_t j = ch; j < last; ++j)
+          sm100::mbar_wait_bounded(bbase + 8 * (j % kFwdStages), (j / kFwdStages) & 1, nullptr,
+                                   kFwdWaitNs);
+      }
+      __syncthreads();
     }
     if (rank == splits - 1) {  // fewer than kVec trailing elements
       const int64_t e = nvec * kVec + threadIdx.x;
@@ -228,11 +280,13 @@ bool aligned16(const void* p, int64_t ld, int esize) {
 }
 
 int choose_splits(int64_t N, int64_t V) {
-  // Aim for about four waves of eight resident CTAs per SM, but give every
-  // CTA at least 8K elements so the cluster merge stays negligible.
-  const int64_t want = static_cast<int64_t>(sm_count()) * 32;
+  // One CTA per row whenever the rows alone give about two waves of resident
+  // CTAs (three per SM: 64 KB of ring each); splitting a row into a cluster
+  // costs more than it gains there.  Fewer rows: split, giving every CTA at
+  // least 16K elements.
+  const int64_t want = static_cast<int64_t>(sm_count()) * 3 * 2;
   int64_t s = (want + N - 1) / N;
-  const int64_t by_len = V / 8192;
+  const int64_t by_len = V / 16384;
   if (s > by_len) s = by_len;
   if (s > kMaxSplits) s = kMaxSplits;
   if (s < 1) s = 1;
@@ -250,8 +304,13 @@ cudaError_t fwd_typed(const Elt* x, int64_t N, int64_t V, int64_t ld, const int3
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(N * splits), 1, 1);
   cfg.blockDim = dim3(kFwdThreads, 1, 1);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = vec ? kFwdSmem : 0;
   cfg.stream = stream;
+  if (vec) {
+    cudaError_t e = cudaFuncSetAttribute(slp_fwd_kernel<Elt, true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kFwdSmem);
+    if (e != cudaSuccess) return e;
+  }
   cudaLaunchAttribute attr[1];
   if (splits > 1) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
