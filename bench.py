@@ -438,7 +438,48 @@ def other_workloads(device, hbm):
         out[name]["step_frac_of_measured"] = out[name]["step_gbs"] / hbm
         del inp, r
         torch.cuda.empty_cache()
+    out["fused_fwd_bwd"] = time_fused(device, hbm)
     out["lmhead"] = time_lmhead(device)
+    return out
+
+
+def time_fused(device, hbm, steps=30, warmup=3):
+    """slp_forward_backward (upstream gradient known at forward time): one
+    read of the active rows and one write of the gradient per step."""
+    from vocab_selected_token_gb300 import _lib
+    from vocab_selected_token_gb300 import workloads as W
+    lib = _lib.load()
+    out = {}
+    for name in ("c151k", "packed", "stability"):
+        inp = W.make_logits_inputs(name, device=device)
+        x = inp.x
+        N, V = x.shape
+        es = x.element_size()
+        na = N if inp.mask is None else int(inp.mask.sum().item())
+        nbytes = na * V * es + N * V * es
+        lp = torch.empty(N, device=device)
+        lse = torch.empty(N, device=device)
+        gx = torch.empty_like(x)
+        s = torch.cuda.current_stream(device)
+        args = (x.data_ptr(), _lib.SLP_BF16 if x.dtype == torch.bfloat16 else _lib.SLP_F32, N, V,
+                x.stride(0), inp.t.data_ptr(), None if inp.mask is None else inp.mask.data_ptr(),
+                float(inp.T), inp.g.data_ptr(), lp.data_ptr(), lse.data_ptr(), gx.data_ptr(),
+                gx.stride(0), None, s.cuda_stream)
+        for _ in range(warmup):
+            assert lib.slp_forward_backward(*args) == 0
+        torch.cuda.synchronize(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(steps):
+            assert lib.slp_forward_backward(*args) == 0
+        e1.record(s)
+        torch.cuda.synchronize(device)
+        ms = e0.elapsed_time(e1) / steps
+        out[name] = {"ms_per_step": ms, "tokens_per_s": N * 1000.0 / ms,
+                     "algorithmic_bytes": nbytes, "gbs": nbytes / (ms * 1e-3) / 1e9,
+                     "frac_of_measured": nbytes / (ms * 1e-3) / 1e9 / hbm}
+        del inp, x, gx
+        torch.cuda.empty_cache()
     return out
 
 

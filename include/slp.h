@@ -125,6 +125,29 @@ int slp_backward(const void* x, int dtype, int64_t N, int64_t V, int64_t ld,
                  void* grad_x, int64_t ld_grad, int32_t* err, void* stream);
 
 /*
+ * slp_forward_backward - slp_forward and slp_backward in one pass, for the
+ * training case where grad_out is known when the forward runs (for example
+ * g = -advantage for a plain policy-gradient loss).
+ *
+ * Defined by: the two calls above (same definitions, same results within
+ * their tolerances).  Each row is read from HBM once and kept on chip (a
+ * thread-block cluster splits it across up to 8 CTAs' shared memory) between
+ * the log-sum-exp and the gradient pass, so the row's bytes are read once
+ * instead of twice (NeMo-RL PR #4222, "Changes": recompute the softmax rather
+ * than store it).  Rows that are not 16-byte aligned, or longer than
+ * 8 x 96 KB, are served by slp_forward followed by slp_backward.
+ *
+ *   x, dtype, N, V, ld, t, mask, T   as for slp_forward.
+ *   grad_out  [N] float32 upstream gradient of logprob.
+ *   logprob, lse  [N] float32 out, as from slp_forward.
+ *   grad_x, ld_grad, err, stream     as for slp_backward.
+ */
+int slp_forward_backward(const void* x, int dtype, int64_t N, int64_t V, int64_t ld,
+                         const int32_t* t, const uint8_t* mask, float T,
+                         const float* grad_out, float* logprob, float* lse,
+                         void* grad_x, int64_t ld_grad, int32_t* err, void* stream);
+
+/*
  * slp_lmhead_workspace_size - bytes of device workspace that
  * slp_lmhead_backward needs for these sizes (enough for slp_lmhead_forward
  * too; a larger workspace is fine).  Returns 0 for invalid sizes.

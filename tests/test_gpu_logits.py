@@ -235,3 +235,78 @@ def test_autograd_and_side_stream():
     torch.cuda.synchronize()
     assert torch.equal(x.grad, ref)
     check_rows(a.x, a.t, None, a.T, a.g, lp.detach(), lse, x.grad, range(0, 128, 7))
+
+
+# ---- fused forward + backward (slp_forward_backward) -------------------------
+
+FB_SCALED = [
+    ("tiny", None, None),             # one CTA per row
+    ("c151k", 48, 151936),            # cluster of 4
+    ("c151k", 33, 151936 - 5),        # ragged tail: rows not 16-byte aligned -> separate kernels
+    ("packed", 3000, 20016),
+    ("stability", 256, 131072),       # fp32, cluster of 6
+    ("tiny", 300, 2047),              # unaligned rows -> separate kernels
+]
+
+
+@pytest.mark.parametrize("name,N,V", FB_SCALED, ids=lambda v: str(v))
+def test_fused_forward_backward_all_rows(name, N, V):
+    dev = device()
+    a = W.make_logits_inputs(name, device=dev, N=N, V=V)
+    lp, lse, gx = slp.slp_forward_backward(a.x, a.t, a.mask, a.T, a.g)
+    torch.cuda.synchronize()
+    check_rows(a.x, a.t, a.mask, a.T, a.g, lp, lse, gx, range(a.x.shape[0]))
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_fused_forward_backward_full_size(name):
+    dev = device()
+    a = W.make_logits_inputs(name, device=dev)
+    N = a.x.shape[0]
+    lp, lse, gx = slp.slp_forward_backward(a.x, a.t, a.mask, a.T, a.g)
+    lp2, lse2 = slp.slp_forward(a.x, a.t, a.mask, a.T)
+    torch.cuda.synchronize()
+    rows = set(np.random.default_rng(23).choice(N, 24, replace=False).tolist()) | {0, N - 1}
+    check_rows(a.x, a.t, a.mask, a.T, a.g, lp, lse, gx, rows)
+    # same quantity as the separate forward, every row
+    assert float((lp - lp2).abs().max()) <= TOL_LP and float((lse - lse2).abs().max()) <= TOL_LP
+    if a.mask is not None:
+        off = a.mask == 0
+        assert bool((gx[off].view(torch.int16) == 0).all())
+
+
+def test_fused_forward_backward_long_rows_fall_back():
+    """Rows longer than one cluster can hold (8 x 96 KB) take the separate
+    kernels and still match the oracle."""
+    dev = device()
+    a = W.make_logits_inputs("tiny", device=dev, N=3, V=400008)
+    lp, lse, gx = slp.slp_forward_backward(a.x, a.t, a.mask, a.T, a.g)
+    torch.cuda.synchronize()
+    check_rows(a.x, a.t, a.mask, a.T, a.g, lp, lse, gx, range(3))
+
+
+def test_fused_forward_backward_bad_target():
+    dev = device()
+    a = W.make_logits_inputs("c151k", device=dev, N=8, V=151936)
+    t = a.t.clone()
+    t[2] = -5
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    lp, lse, gx = slp.slp_forward_backward(a.x, t, None, 1.0, a.g, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & 1
+    assert np.isnan(float(lp[2])) and bool(torch.isnan(gx[2].float()).all())
+    check_rows(a.x, t, None, 1.0, a.g, lp, lse, gx, [0, 1, 3, 4, 5, 6, 7])
+
+
+def test_fused_forward_backward_ragged_tail():
+    """V not a multiple of 8 with a 16-byte-aligned stride: the cluster path's
+    scalar tail, and grad_x's padding columns left untouched."""
+    dev = device()
+    a = W.make_logits_inputs("c151k", device=dev, N=40, V=20016)
+    V = 20011
+    x = a.x[:, :V]
+    gx = torch.full((40, 20016), 7.0, dtype=torch.bfloat16, device=dev)
+    lp, lse, _ = slp.slp_forward_backward(x, a.t % V, None, a.T, a.g, grad_x=gx[:, :V])
+    torch.cuda.synchronize()
+    assert bool((gx[:, V:] == 7.0).all())
+    check_rows(x, a.t % V, None, a.T, a.g, lp, lse, gx[:, :V], range(40))

@@ -24,7 +24,8 @@ from . import _lib
 from ._lib import SlpError
 
 __all__ = [
-    "SlpError", "slp_forward", "slp_backward", "slp_lmhead_workspace_size",
+    "SlpError", "slp_forward", "slp_backward", "slp_forward_backward",
+    "slp_lmhead_workspace_size",
     "slp_lmhead_forward_workspace_size", "slp_lmhead_forward_noalloc",
     "slp_lmhead_forward", "slp_lmhead_backward", "selected_logprob",
     "lmhead_selected_logprob", "library_path",
@@ -98,6 +99,32 @@ def slp_backward(x, t, mask, T: float, lse, grad_out, grad_x=None, err=None, str
     _lib.call("slp_backward", _ptr(x), _DTYPES[x.dtype], N, V, ld, _ptr(t), _ptr(mask), float(T),
               _ptr(lse), _ptr(grad_out), _ptr(grad_x), ldg, _ptr(err), _stream_handle(stream))
     return grad_x
+
+
+def slp_forward_backward(x, t, mask, T: float, grad_out, logprob=None, lse=None, grad_x=None,
+                         err=None, stream=None):
+    """Forward and backward of the logits-input path in one pass, for an
+    upstream gradient known at forward time.  Returns (logprob, lse, grad_x)."""
+    N, V, ld = _logits_layout(x)
+    _check_vec("t", t, N, torch.int32)
+    if mask is not None:
+        _check_vec("mask", mask, N, torch.uint8)
+    _check_vec("grad_out", grad_out, N, torch.float32)
+    if logprob is None:
+        logprob = torch.empty(N, dtype=torch.float32, device=x.device)
+    if lse is None:
+        lse = torch.empty(N, dtype=torch.float32, device=x.device)
+    _check_vec("logprob", logprob, N, torch.float32)
+    _check_vec("lse", lse, N, torch.float32)
+    if grad_x is None:
+        grad_x = torch.empty((N, V), dtype=x.dtype, device=x.device)
+    if grad_x.shape != (N, V) or grad_x.dtype != x.dtype or (N > 0 and V > 0 and grad_x.stride(1) != 1):
+        raise ValueError("grad_x must be [N, V] with x's dtype and unit column stride")
+    ldg = grad_x.stride(0) if N > 1 else max(V, 1)
+    _lib.call("slp_forward_backward", _ptr(x), _DTYPES[x.dtype], N, V, ld, _ptr(t), _ptr(mask),
+              float(T), _ptr(grad_out), _ptr(logprob), _ptr(lse), _ptr(grad_x), ldg, _ptr(err),
+              _stream_handle(stream))
+    return logprob, lse, grad_x
 
 
 def slp_lmhead_workspace_size(N: int, V: int, d: int) -> int:

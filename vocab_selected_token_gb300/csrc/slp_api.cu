@@ -82,6 +82,21 @@ int slp_backward(const void* x, int dtype, int64_t N, int64_t V, int64_t ld, con
                                           ld_grad, err, static_cast<cudaStream_t>(stream)));
 }
 
+int slp_forward_backward(const void* x, int dtype, int64_t N, int64_t V, int64_t ld,
+                         const int32_t* t, const uint8_t* mask, float T, const float* grad_out,
+                         float* logprob, float* lse, void* grad_x, int64_t ld_grad, int32_t* err,
+                         void* stream) {
+  int st = check_logits_args(x, dtype, N, V, ld, t, T);
+  if (st != SLP_OK) return st;
+  if (ld_grad < V) return SLP_ERR_INVALID_ARG;
+  if (N == 0) return SLP_OK;
+  if (grad_out == nullptr || logprob == nullptr || lse == nullptr || grad_x == nullptr)
+    return SLP_ERR_INVALID_ARG;
+  return cuda_status(slp::launch_forward_backward(x, dtype, N, V, ld, t, mask, T, grad_out,
+                                                  logprob, lse, grad_x, ld_grad, err,
+                                                  static_cast<cudaStream_t>(stream)));
+}
+
 size_t slp_lmhead_workspace_size(int64_t N, int64_t V, int64_t d) {
   if (N < 0 || V <= 0 || d <= 0 || V > INT32_MAX || N > INT32_MAX || d > INT32_MAX) return 0;
   return slp::lmhead_workspace_size(N, V, d);

@@ -21,6 +21,12 @@ cudaError_t launch_backward(const void* x, int dtype, int64_t N, int64_t V, int6
                             const float* grad_out, void* grad_x, int64_t ld_grad,
                             int32_t* err, cudaStream_t stream);
 
+cudaError_t launch_forward_backward(const void* x, int dtype, int64_t N, int64_t V, int64_t ld,
+                                    const int32_t* t, const uint8_t* mask, float T,
+                                    const float* grad_out, float* logprob, float* lse,
+                                    void* grad_x, int64_t ld_grad, int32_t* err,
+                                    cudaStream_t stream);
+
 // Fused LM-head path (slp_lmhead.cu).
 size_t lmhead_workspace_size(int64_t N, int64_t V, int64_t d);
 size_t lmhead_forward_workspace_size(int64_t N, int64_t V, int64_t d);

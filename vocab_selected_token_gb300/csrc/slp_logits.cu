@@ -273,6 +273,186 @@ __global__ void __launch_bounds__(kBwdThreads)
   }
 }
 
+
+// ---- fused forward + backward (upstream gradient known at forward time) ----
+//
+// A cluster of C CTAs holds one row in shared memory (each CTA a contiguous
+// segment of at most kFbMaxSeg bytes), loaded once with bulk copies.  The
+// log-sum-exp is folded as the chunks land and merged across the cluster
+// through distributed shared memory: every CTA merges all partials in rank
+// order, so all of them hold the same state.  Each CTA then writes its
+// segment of g/T * (1[v == t] - p) straight from shared memory.  That is one
+// HBM read of the active rows plus one write of the gradient, instead of the
+// two reads of a separate forward and backward (NeMo-RL PR #4222, "Changes":
+// recompute the softmax instead of storing it; here the row stays on chip
+// between the two passes).
+
+constexpr int kFbThreads = 256;
+constexpr int kFbChunk = 16384;
+constexpr int kFbMaxChunks = 6;
+constexpr int kFbMaxSeg = kFbChunk * kFbMaxChunks;  // 96 KB per CTA
+constexpr int kFbMaxCluster = 8;
+
+template <typename Elt>
+__global__ void __launch_bounds__(kFbThreads)
+    slp_fwd_bwd_kernel(const Elt* __restrict__ x, int64_t V, int64_t ld,
+                       const int32_t* __restrict__ t, const uint8_t* __restrict__ mask, float T,
+                       float c, float invT, const float* __restrict__ g,
+                       float* __restrict__ logprob, float* __restrict__ lse,
+                       Elt* __restrict__ gx, int64_t ldg, int32_t* __restrict__ err, int C) {
+  using E = Elem<Elt>;
+  constexpr int kVec = E::kVec;
+  constexpr int kWarps = kFbThreads / 32;
+  extern __shared__ __align__(128) uint8_t seg[];
+  __shared__ __align__(8) uint64_t full[kFbMaxChunks];
+  __shared__ Lse2 warp_part[kWarps];
+  __shared__ float cta_part[3];
+  __shared__ int abort_flag;
+
+  const int64_t row = blockIdx.x / C;
+  const int rank = static_cast<int>(blockIdx.x - row * C);
+  const int64_t nvec = V / kVec;
+  const int64_t v0 = nvec * rank / C;
+  const int64_t v1 = nvec * (rank + 1) / C;
+  const int nv = static_cast<int>(v1 - v0);  // vectors of this segment
+  uint4* gv = reinterpret_cast<uint4*>(gx + row * ldg) + v0;
+
+  // Inactive rows: every CTA of the cluster writes zeros and leaves; none of
+  // them touches a cluster barrier.
+  if (mask != nullptr && mask[row] == 0) {
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = threadIdx.x; i < nv; i += kFbThreads) st_stream(gv + i, z);
+    if (rank == C - 1)
+      for (int64_t e = nvec * kVec + threadIdx.x; e < V; e += kFbThreads)
+        E::store1(gx + row * ldg + e, 0.f);
+    if (rank == 0 && threadIdx.x == 0) {
+      logprob[row] = 0.f;
+      lse[row] = 0.f;
+    }
+    return;
+  }
+
+  const Elt* xr = x + row * ld;
+  const int32_t tt = t[row];
+  const bool tvalid = tt >= 0 && static_cast<int64_t>(tt) < V;
+  float xt = 0.f;
+  if (rank == 0 && threadIdx.x == 0 && tvalid) xt = E::load1(xr + tt);
+  const float gT = tvalid ? g[row] * invT : __int_as_float(0x7FC00000);
+
+  const int seg_bytes = nv * 16;
+  const int nch = (seg_bytes + kFbChunk - 1) / kFbChunk;
+  const uint32_t sbase = sm100::smem_u32(seg);
+  const uint32_t bbase = sm100::smem_u32(full);
+  if (threadIdx.x == 0) {
+    for (int k = 0; k < nch; ++k) sm100::mbar_init(bbase + 8 * k, 1);
+    abort_flag = 0;
+    sm100::fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const char* src = reinterpret_cast<const char*>(reinterpret_cast<const uint4*>(xr) + v0);
+    for (int k = 0; k < nch; ++k) {
+      const int off = k * kFbChunk;
+      const uint32_t bytes = static_cast<uint32_t>(seg_bytes - off < kFbChunk ? seg_bytes - off
+                                                                                : kFbChunk);
+      sm100::mbar_arrive_expect_tx(bbase + 8 * k, bytes);
+      sm100::bulk_load(sbase + off, src + off, bytes, bbase + 8 * k);
+    }
+  }
+
+  // pass 1: online log-sum-exp over the segment as its chunks land
+  Lse2 st = lse2_empty();
+  const uint4* q = reinterpret_cast<const uint4*>(seg);
+  constexpr int kPer = kFbChunk / 16 / kFbThreads;
+  const uint4 pad = make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord, E::kNegInfWord);
+  bool ok = true;
+  for (int k = 0; k < nch; ++k) {
+    const bool got =
+        sm100::mbar_wait_bounded(bbase + 8 * k, 0, &abort_flag, kFwdWaitNs);
+    if (__syncthreads_or(!got)) {
+      ok = false;
+      break;
+    }
+    float f[kPer][kVec];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int i = k * (kFbChunk / 16) + u * kFbThreads + threadIdx.x;
+      E::unpack(i < nv ? q[i] : pad, f[u]);
+    }
+    lse2_fold<kPer * kVec>(st, &f[0][0], c);
+  }
+  if (!ok && threadIdx.x == 0) {
+    if (err != nullptr) atomicOr(err, SLP_DEVICE_ERR_TIMEOUT);
+    for (int k = 0; k < nch; ++k)  // let every copy land before the CTA moves on
+      sm100::mbar_wait_bounded(bbase + 8 * k, 0, nullptr, kFwdWaitNs);
+  }
+  if (rank == C - 1) {
+    const int64_t e = nvec * kVec + threadIdx.x;
+    if (e < V) {
+      float f1[1] = {E::load1(xr + e)};
+      lse2_fold<1>(st, f1, c);
+    }
+  }
+
+  // CTA merge, then cluster merge (every CTA reads all partials)
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  st = lse2_warp_reduce(st);
+  if (lane == 0) warp_part[warp] = st;
+  __syncthreads();
+  if (warp == 0) {
+    Lse2 v = lane < kWarps ? warp_part[lane] : lse2_empty();
+    v = lse2_warp_reduce(v);
+    if (lane == 0) {
+      cta_part[0] = v.m;
+      cta_part[1] = v.mc;
+      cta_part[2] = v.s;
+    }
+  }
+  cluster_sync_all();
+  __shared__ Lse2 row_state;
+  if (threadIdx.x == 0) {
+    Lse2 acc = lse2_empty();
+    for (int r = 0; r < C; ++r) {
+      Lse2 o;
+      o.m = ld_shared_cluster_f32(map_shared_rank(&cta_part[0], r));
+      o.mc = ld_shared_cluster_f32(map_shared_rank(&cta_part[1], r));
+      o.s = ld_shared_cluster_f32(map_shared_rank(&cta_part[2], r));
+      acc = lse2_merge(acc, o);
+    }
+    row_state = acc;
+    if (rank == 0) write_row_result(acc, xt, tvalid, T, c, logprob, lse, err, row);
+  }
+  // no CTA may leave before the others have read its partial: arrive now,
+  // wait at the end
+  asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+  __syncthreads();
+  const Lse2 rs = row_state;
+
+  // pass 2: gradient from shared memory.  p = 2^(x*c - mc) / s.
+  const float off = (rs.m == -INFINITY || !(rs.s > 0.f)) ? __int_as_float(0x7FC00000)
+                                                          : rs.mc + log2f(rs.s);
+  const float a = -gT;
+  const int64_t rel0 = static_cast<int64_t>(tt) - v0 * kVec;  // target offset in segment
+  for (int i = threadIdx.x; i < nv; i += kFbThreads) {
+    float f[kVec];
+    E::unpack(q[i], f);
+    const int64_t rel = rel0 - static_cast<int64_t>(i) * kVec;
+#pragma unroll
+    for (int k2 = 0; k2 < kVec; ++k2) {
+      const float p = ex2(fmaf(f[k2], c, -off));
+      f[k2] = (rel == k2) ? fmaf(a, p, gT) : a * p;
+    }
+    st_stream(gv + i, E::pack(f));
+  }
+  if (rank == C - 1) {
+    for (int64_t e = nvec * kVec + threadIdx.x; e < V; e += kFbThreads) {
+      const float p = ex2(fmaf(E::load1(xr + e), c, -off));
+      E::store1(gx + row * ldg + e, (e == tt) ? fmaf(a, p, gT) : a * p);
+    }
+  }
+  asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+
 namespace {
 
 bool aligned16(const void* p, int64_t ld, int esize) {
@@ -348,6 +528,43 @@ cudaError_t bwd_typed(const Elt* x, int64_t N, int64_t V, int64_t ld, const int3
   return cudaGetLastError();
 }
 
+// Fused forward + backward: needs 16-byte-aligned rows and rows short enough
+// to fit a cluster of at most 8 CTAs x 96 KB; returns cudaErrorNotSupported
+// otherwise (the caller then runs the separate kernels).
+template <typename Elt>
+cudaError_t fwd_bwd_typed(const Elt* x, int64_t N, int64_t V, int64_t ld, const int32_t* t,
+                          const uint8_t* mask, float T, const float* g, float* logprob,
+                          float* lse, Elt* gx, int64_t ldg, int32_t* err, cudaStream_t stream) {
+  constexpr int kVec = Elem<Elt>::kVec;
+  if (!aligned16(x, ld, sizeof(Elt)) || !aligned16(gx, ldg, sizeof(Elt)))
+    return cudaErrorNotSupported;
+  const int64_t nvec = V / kVec;
+  int64_t C = (nvec * 16 + kFbMaxSeg - 1) / kFbMaxSeg;
+  if (C < 1) C = 1;
+  if (C > kFbMaxCluster) return cudaErrorNotSupported;
+  if (N * C > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
+  const int smem = static_cast<int>((nvec + C - 1) / C) * 16;
+  cudaError_t e = cudaFuncSetAttribute(slp_fwd_bwd_kernel<Elt>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kFbMaxSeg);
+  if (e != cudaSuccess) return e;
+  const float c = static_cast<float>(1.4426950408889634 / static_cast<double>(T));
+  const float invT = 1.0f / T;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(N * C), 1, 1);
+  cfg.blockDim = dim3(kFbThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(C);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, slp_fwd_bwd_kernel<Elt>, x, V, ld, t, mask, T, c, invT, g,
+                            logprob, lse, gx, ldg, err, static_cast<int>(C));
+}
+
 }  // namespace
 
 cudaError_t launch_forward(const void* x, int dtype, int64_t N, int64_t V, int64_t ld,
@@ -369,6 +586,26 @@ cudaError_t launch_backward(const void* x, int dtype, int64_t N, int64_t V, int6
                      static_cast<__nv_bfloat16*>(grad_x), ld_grad, err, stream);
   return bwd_typed(static_cast<const float*>(x), N, V, ld, t, mask, T, lse, grad_out,
                    static_cast<float*>(grad_x), ld_grad, err, stream);
+}
+
+cudaError_t launch_forward_backward(const void* x, int dtype, int64_t N, int64_t V, int64_t ld,
+                                    const int32_t* t, const uint8_t* mask, float T,
+                                    const float* grad_out, float* logprob, float* lse,
+                                    void* grad_x, int64_t ld_grad, int32_t* err,
+                                    cudaStream_t stream) {
+  cudaError_t e;
+  if (dtype == SLP_BF16)
+    e = fwd_bwd_typed(static_cast<const __nv_bfloat16*>(x), N, V, ld, t, mask, T, grad_out,
+                      logprob, lse, static_cast<__nv_bfloat16*>(grad_x), ld_grad, err, stream);
+  else
+    e = fwd_bwd_typed(static_cast<const float*>(x), N, V, ld, t, mask, T, grad_out, logprob, lse,
+                      static_cast<float*>(grad_x), ld_grad, err, stream);
+  if (e != cudaErrorNotSupported) return e;
+  // rows unaligned or too long for one cluster: the separate kernels
+  e = launch_forward(x, dtype, N, V, ld, t, mask, T, logprob, lse, err, stream);
+  if (e != cudaSuccess) return e;
+  return launch_backward(x, dtype, N, V, ld, t, mask, T, lse, grad_out, grad_x, ld_grad, err,
+                         stream);
 }
 
 }  // namespace slp
