@@ -58,6 +58,8 @@ __all__ = [
     "lmhead_backward",
     "lmhead_dh_rows",
     "lmhead_dW_rows",
+    "entropy_forward",
+    "entropy_backward",
 ]
 
 
@@ -240,3 +242,44 @@ def lmhead_dW_rows(h, W, t, mask, T: float, lse, grad_out, vrows):
             dz = g * ((t == v).astype(np.float64) - np.exp(z - lse)) / T
             out[k] = dz @ hr
     return out
+
+
+def entropy_forward(x, t, mask, T: float):
+    """Selected-token log-probability, lse and the per-token entropy of the
+    same softmax, H[n] = -sum_v p[n, v] log p[n, v] with p = softmax(x[n] / T)
+    (slime issue #2253: get_log_probs_and_entropy computes both over the same
+    rows).  Returns (logprob, lse, entropy) in float64; inactive rows are 0."""
+    x = _as_f64(x)
+    N = x.shape[0]
+    lp, lse = selected_logprob_forward(x, t, mask, T)
+    active = _active_rows(N, mask)
+    H = np.zeros(N, dtype=np.float64)
+    with np.errstate(invalid="ignore", over="ignore", divide="ignore"):
+        for n in range(N):
+            if not active[n]:
+                continue
+            logp = x[n] / T - lse[n]
+            p = np.exp(logp)
+            H[n] = -np.sum(np.where(p > 0, p * logp, 0.0))
+    return lp, lse, H
+
+
+def entropy_backward(x, t, mask, T: float, lse, H, grad_out, grad_entropy):
+    """Gradient of sum_n (g[n] logprob[n] + gH[n] H[n]) with respect to x:
+    g (1[v = t] - p_v) / T - gH p_v (log p_v + H) / T, using
+    dH/dz_v = -p_v (log p_v + H) for z = x / T."""
+    x = _as_f64(x)
+    N, V = x.shape
+    grad = selected_logprob_backward(x, t, mask, T, lse, grad_out)
+    active = _active_rows(N, mask)
+    lse = _as_f64(lse).reshape(N)
+    H = _as_f64(H).reshape(N)
+    gH = _as_f64(grad_entropy).reshape(N)
+    with np.errstate(invalid="ignore", over="ignore"):
+        for n in range(N):
+            if not active[n]:
+                continue
+            logp = x[n] / T - lse[n]
+            p = np.exp(logp)
+            grad[n] -= gH[n] * np.where(p > 0, p * (logp + H[n]), 0.0) / T
+    return grad

@@ -281,3 +281,55 @@ ALL_PINS = [
 def run_all(impl: Impl):
     for p in ALL_PINS:
         p(impl)
+
+
+# --- entropy (per-token entropy of the same softmax) ---------------------------
+
+def pin_entropy_closed_forms(ent_fwd):
+    """Uniform logits give log V; two classes give the binary entropy; a huge
+    spike gives ~0; all match torch's Categorical entropy."""
+    for V in (1, 3, 1000):
+        x = np.full((2, V), -1.5)
+        _, _, H = ent_fwd(x, np.zeros(2, int), None, 0.9)
+        _close(H, np.full(2, math.log(V)), 1e-13, 1e-13, f"uniform entropy V={V}")
+    r = _rng(13)
+    x = r.normal(0, 2, (16, 2))
+    T = 0.8
+    _, _, H = ent_fwd(x, np.zeros(16, int), None, T)
+    p = 1.0 / (1.0 + np.exp(-(x[:, 0] - x[:, 1]) / T))
+    ref = -(p * np.log(p) + (1 - p) * np.log(1 - p))
+    _close(H, ref, 1e-12, 1e-13, "binary entropy")
+    x = np.zeros((1, 50)); x[0, 7] = 500.0
+    _, _, H = ent_fwd(x, np.array([7]), None, 1.0)
+    assert 0 <= H[0] < 1e-100 or H[0] == 0.0
+    x = r.normal(0, 3, (10, 333))
+    _, _, H = ent_fwd(x, r.integers(0, 333, 10), None, 1.3)
+    ref = torch.distributions.Categorical(logits=torch.from_numpy(x / 1.3)).entropy().numpy()
+    _close(H, ref, 1e-12, 1e-12, "Categorical entropy")
+
+
+def pin_entropy_finite_differences(ent_fwd, ent_bwd):
+    """Analytic gradient of sum_n (g_n lp_n + gH_n H_n) matches central
+    differences; masked rows are exactly 0."""
+    r = _rng(14)
+    N, V, T, hs = 4, 9, 0.7, 1e-6
+    x = r.normal(0, 1.5, (N, V))
+    t = r.integers(0, V, N)
+    g = r.uniform(-1, 1, N)
+    gH = r.uniform(-1, 1, N)
+    mask = np.array([1, 1, 0, 1], np.uint8)
+    _, lse, H = ent_fwd(x, t, mask, T)
+    gx = ent_bwd(x, t, mask, T, lse, H, g, gH)
+
+    def L(xx):
+        lp, _, HH = ent_fwd(xx, t, mask, T)
+        return float(np.dot(g, lp) + np.dot(gH, HH))
+
+    fd = np.zeros_like(x)
+    for n in range(N):
+        for v in range(V):
+            xp = x.copy(); xp[n, v] += hs
+            xm = x.copy(); xm[n, v] -= hs
+            fd[n, v] = (L(xp) - L(xm)) / (2 * hs)
+    _close(gx, fd, 1e-7, 1e-9, "entropy finite differences")
+    assert (gx[2] == 0).all()

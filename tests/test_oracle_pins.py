@@ -135,3 +135,28 @@ def test_sampled_lmhead_gradients_match_full_backward():
     assert np.allclose(O.lmhead_dh_rows(h, W, t, mask, T, lse, g, rows), dh[rows], rtol=1e-12, atol=1e-14)
     vr = [0, 7, 29, 13]
     assert np.allclose(O.lmhead_dW_rows(h, W, t, mask, T, lse, g, vr), dW[vr], rtol=1e-12, atol=1e-14)
+
+
+def test_entropy_pins():
+    from tests.oracle_pins import pin_entropy_closed_forms, pin_entropy_finite_differences
+    pin_entropy_closed_forms(O.entropy_forward)
+    pin_entropy_finite_differences(O.entropy_forward, O.entropy_backward)
+
+
+def test_entropy_pins_catch_planted_mistakes():
+    from tests.oracle_pins import pin_entropy_closed_forms, pin_entropy_finite_differences
+
+    def fwd_no_T(x, t, mask, T):
+        return O.entropy_forward(np.asarray(x, np.float64) * T, t, mask, T)
+
+    def bwd_wrong_sign(x, t, mask, T, lse, H, g, gH):
+        return O.entropy_backward(x, t, mask, T, lse, H, g, -np.asarray(gH))
+
+    def bwd_no_H(x, t, mask, T, lse, H, g, gH):
+        return O.entropy_backward(x, t, mask, T, lse, np.zeros_like(np.asarray(H)), g, gH)
+
+    with pytest.raises(AssertionError):
+        pin_entropy_closed_forms(fwd_no_T)
+    for bad in (bwd_wrong_sign, bwd_no_H):
+        with pytest.raises(AssertionError):
+            pin_entropy_finite_differences(O.entropy_forward, bad)
