@@ -125,6 +125,40 @@ int slp_backward(const void* x, int dtype, int64_t N, int64_t V, int64_t ld,
                  void* grad_x, int64_t ld_grad, int32_t* err, void* stream);
 
 /*
+ * slp_forward_entropy - slp_forward plus the per-token entropy of the same
+ * softmax, H[n] = -sum_v p[n,v] log p[n,v] with p = softmax(x[n] / T), from
+ * the same single read of the logits (one more running accumulator).
+ *
+ * Defined by: slime issue #2253 (get_log_probs_and_entropy computes the
+ * selected log-probability and the entropy over the same rows); the entropy
+ * itself is the textbook definition.
+ *
+ *   as slp_forward, plus entropy [N] float32 out (0 on inactive rows, NaN
+ *   where logprob is NaN).
+ */
+int slp_forward_entropy(const void* x, int dtype, int64_t N, int64_t V, int64_t ld,
+                        const int32_t* t, const uint8_t* mask, float T,
+                        float* logprob, float* lse, float* entropy, int32_t* err, void* stream);
+
+/*
+ * slp_backward_entropy - gradient of sum_n (g[n] logprob[n] + gH[n] H[n])
+ * with respect to x:
+ *
+ *   grad_x[n,v] = ( g[n] (1[v == t_n] - p_v) - gH[n] p_v (log p_v + H[n]) ) / T
+ *
+ * (dH/dz_v = -p_v (log p_v + H) for z = x / T), recomputing p from x and lse.
+ *
+ *   as slp_backward, plus entropy [N] from slp_forward_entropy and
+ *   grad_entropy [N] float32.  grad_out or grad_entropy may be NULL, meaning
+ *   zero.
+ */
+int slp_backward_entropy(const void* x, int dtype, int64_t N, int64_t V, int64_t ld,
+                         const int32_t* t, const uint8_t* mask, float T,
+                         const float* lse, const float* entropy,
+                         const float* grad_out, const float* grad_entropy,
+                         void* grad_x, int64_t ld_grad, int32_t* err, void* stream);
+
+/*
  * slp_forward_backward - slp_forward and slp_backward in one pass, for the
  * training case where grad_out is known when the forward runs (for example
  * g = -advantage for a plain policy-gradient loss).

@@ -25,6 +25,7 @@ from ._lib import SlpError
 
 __all__ = [
     "SlpError", "slp_forward", "slp_backward", "slp_forward_backward",
+    "slp_forward_entropy", "slp_backward_entropy", "selected_logprob_and_entropy",
     "slp_lmhead_workspace_size",
     "slp_lmhead_forward_workspace_size", "slp_lmhead_forward_noalloc",
     "slp_lmhead_forward", "slp_lmhead_backward", "selected_logprob",
@@ -99,6 +100,69 @@ def slp_backward(x, t, mask, T: float, lse, grad_out, grad_x=None, err=None, str
     _lib.call("slp_backward", _ptr(x), _DTYPES[x.dtype], N, V, ld, _ptr(t), _ptr(mask), float(T),
               _ptr(lse), _ptr(grad_out), _ptr(grad_x), ldg, _ptr(err), _stream_handle(stream))
     return grad_x
+
+
+def slp_forward_entropy(x, t, mask=None, T: float = 1.0, logprob=None, lse=None, entropy=None,
+                        err=None, stream=None):
+    """Forward plus per-token entropy.  Returns (logprob, lse, entropy)."""
+    N, V, ld = _logits_layout(x)
+    _check_vec("t", t, N, torch.int32)
+    if mask is not None:
+        _check_vec("mask", mask, N, torch.uint8)
+    out = []
+    for v in (logprob, lse, entropy):
+        v = torch.empty(N, dtype=torch.float32, device=x.device) if v is None else v
+        _check_vec("output", v, N, torch.float32)
+        out.append(v)
+    _lib.call("slp_forward_entropy", _ptr(x), _DTYPES[x.dtype], N, V, ld, _ptr(t), _ptr(mask),
+              float(T), _ptr(out[0]), _ptr(out[1]), _ptr(out[2]), _ptr(err), _stream_handle(stream))
+    return tuple(out)
+
+
+def slp_backward_entropy(x, t, mask, T: float, lse, entropy, grad_out=None, grad_entropy=None,
+                         grad_x=None, err=None, stream=None):
+    """Gradient of sum(g * logprob + gH * entropy) with respect to x."""
+    N, V, ld = _logits_layout(x)
+    _check_vec("t", t, N, torch.int32)
+    if mask is not None:
+        _check_vec("mask", mask, N, torch.uint8)
+    _check_vec("lse", lse, N, torch.float32)
+    _check_vec("entropy", entropy, N, torch.float32)
+    for name, v in (("grad_out", grad_out), ("grad_entropy", grad_entropy)):
+        if v is not None:
+            _check_vec(name, v, N, torch.float32)
+    if grad_x is None:
+        grad_x = torch.empty((N, V), dtype=x.dtype, device=x.device)
+    ldg = grad_x.stride(0) if N > 1 else max(V, 1)
+    _lib.call("slp_backward_entropy", _ptr(x), _DTYPES[x.dtype], N, V, ld, _ptr(t), _ptr(mask),
+              float(T), _ptr(lse), _ptr(entropy), _ptr(grad_out), _ptr(grad_entropy),
+              _ptr(grad_x), ldg, _ptr(err), _stream_handle(stream))
+    return grad_x
+
+
+class _SelectedLogprobEntropy(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, x, t, mask, T):
+        lp, lse, H = slp_forward_entropy(x, t, mask, T)
+        ctx.save_for_backward(x, t, mask, lse, H)
+        ctx.T = T
+        ctx.mark_non_differentiable(lse)
+        return lp, H, lse
+
+    @staticmethod
+    def backward(ctx, g, gH, _g_lse):
+        x, t, mask, lse, H = ctx.saved_tensors
+        gx = slp_backward_entropy(x, t, mask, ctx.T, lse, H,
+                                  None if g is None else g.float().contiguous(),
+                                  None if gH is None else gH.float().contiguous())
+        return gx, None, None, None
+
+
+def selected_logprob_and_entropy(x, t, mask=None, temperature: float = 1.0):
+    """(logprob[N], entropy[N]) of softmax(x / T) from one read of x, with an
+    autograd backward covering both outputs."""
+    lp, H, _ = _SelectedLogprobEntropy.apply(x, t, mask, float(temperature))
+    return lp, H
 
 
 def slp_forward_backward(x, t, mask, T: float, grad_out, logprob=None, lse=None, grad_x=None,

@@ -31,6 +31,10 @@ SIGNATURES = {
     "slp_forward": (_int, [_vp, _int, _i64, _i64, _i64, _vp, _vp, _f32, _vp, _vp, _vp, _vp]),
     "slp_backward": (_int, [_vp, _int, _i64, _i64, _i64, _vp, _vp, _f32, _vp, _vp, _vp, _i64,
                             _vp, _vp]),
+    "slp_forward_entropy": (_int, [_vp, _int, _i64, _i64, _i64, _vp, _vp, _f32, _vp, _vp, _vp,
+                                   _vp, _vp]),
+    "slp_backward_entropy": (_int, [_vp, _int, _i64, _i64, _i64, _vp, _vp, _f32, _vp, _vp, _vp,
+                                    _vp, _vp, _i64, _vp, _vp]),
     "slp_forward_backward": (_int, [_vp, _int, _i64, _i64, _i64, _vp, _vp, _f32, _vp, _vp, _vp,
                                     _vp, _i64, _vp, _vp]),
     "slp_lmhead_workspace_size": (_sz, [_i64, _i64, _i64]),

@@ -82,6 +82,31 @@ int slp_backward(const void* x, int dtype, int64_t N, int64_t V, int64_t ld, con
                                           ld_grad, err, static_cast<cudaStream_t>(stream)));
 }
 
+int slp_forward_entropy(const void* x, int dtype, int64_t N, int64_t V, int64_t ld,
+                        const int32_t* t, const uint8_t* mask, float T, float* logprob,
+                        float* lse, float* entropy, int32_t* err, void* stream) {
+  int st = check_logits_args(x, dtype, N, V, ld, t, T);
+  if (st != SLP_OK) return st;
+  if (N == 0) return SLP_OK;
+  if (logprob == nullptr || lse == nullptr || entropy == nullptr) return SLP_ERR_INVALID_ARG;
+  return cuda_status(slp::launch_forward_entropy(x, dtype, N, V, ld, t, mask, T, logprob, lse,
+                                                 entropy, err, static_cast<cudaStream_t>(stream)));
+}
+
+int slp_backward_entropy(const void* x, int dtype, int64_t N, int64_t V, int64_t ld,
+                         const int32_t* t, const uint8_t* mask, float T, const float* lse,
+                         const float* entropy, const float* grad_out, const float* grad_entropy,
+                         void* grad_x, int64_t ld_grad, int32_t* err, void* stream) {
+  int st = check_logits_args(x, dtype, N, V, ld, t, T);
+  if (st != SLP_OK) return st;
+  if (ld_grad < V) return SLP_ERR_INVALID_ARG;
+  if (N == 0) return SLP_OK;
+  if (lse == nullptr || entropy == nullptr || grad_x == nullptr) return SLP_ERR_INVALID_ARG;
+  return cuda_status(slp::launch_backward_entropy(x, dtype, N, V, ld, t, mask, T, lse, entropy,
+                                                  grad_out, grad_entropy, grad_x, ld_grad, err,
+                                                  static_cast<cudaStream_t>(stream)));
+}
+
 int slp_forward_backward(const void* x, int dtype, int64_t N, int64_t V, int64_t ld,
                          const int32_t* t, const uint8_t* mask, float T, const float* grad_out,
                          float* logprob, float* lse, void* grad_x, int64_t ld_grad, int32_t* err,

@@ -171,6 +171,106 @@ __device__ __forceinline__ void write_row_result(const Lse2& a, float xt, bool t
   lse[row] = l;
 }
 
+// Log-sum-exp state with the entropy accumulator: w = sum 2^(x*c - mc) (x - m),
+// the softmax-weighted spread of the logits below the running max, kept
+// centred on m so nothing large cancels.  Then sum_v p_v x_v = m + w / s and
+// the entropy is ln(sum exp((x - m)/T)) - (w / s) / T.
+struct Lse3 {
+  float m, mc, s, w;
+};
+
+__device__ __forceinline__ Lse3 lse3_empty() { return Lse3{-INFINITY, -INFINITY, 0.f, 0.f}; }
+
+__device__ __forceinline__ Lse3 lse3_merge(Lse3 a, Lse3 b) {
+  if (b.m == -INFINITY) return a;
+  if (a.m == -INFINITY) return b;
+  if (b.m > a.m) {
+    const float sc = ex2(a.mc - b.mc);
+    a.w = fmaf(a.s, a.m - b.m, a.w) * sc + b.w;
+    a.s = a.s * sc + b.s;
+    a.m = b.m;
+    a.mc = b.mc;
+  } else {
+    const float sc = ex2(b.mc - a.mc);
+    a.w = fmaf(fmaf(b.s, b.m - a.m, b.w), sc, a.w);
+    a.s = fmaf(b.s, sc, a.s);
+  }
+  return a;
+}
+
+__device__ __forceinline__ Lse3 lse3_warp_reduce(Lse3 v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    Lse3 u;
+    u.m = __shfl_xor_sync(0xFFFFFFFFu, v.m, o);
+    u.mc = __shfl_xor_sync(0xFFFFFFFFu, v.mc, o);
+    u.s = __shfl_xor_sync(0xFFFFFFFFu, v.s, o);
+    u.w = __shfl_xor_sync(0xFFFFFFFFu, v.w, o);
+    v = lse3_merge(v, u);
+  }
+  return v;
+}
+
+template <int K>
+__device__ __forceinline__ void lse3_fold(Lse3& st, const float* f, float c) {
+  float bm = f[0];
+#pragma unroll
+  for (int k = 1; k < K; ++k) bm = fmaxf(bm, f[k]);
+  if (bm > st.m) {
+    const float nmc = __fmul_rn(bm, c);
+    if (st.m == -INFINITY) {
+      st.s = 0.f;
+      st.w = 0.f;
+    } else {
+      const float sc = ex2(st.mc - nmc);
+      st.w = fmaf(st.s, st.m - bm, st.w) * sc;
+      st.s *= sc;
+    }
+    st.m = bm;
+    st.mc = nmc;
+  }
+  if (st.m != -INFINITY) {
+    float a[4] = {0.f, 0.f, 0.f, 0.f}, b[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      const float e = ex2(fmaf(f[k], c, -st.mc));
+      a[k & 3] += e;
+      // -inf logits contribute e = 0; keep 0 * -inf out of the sum
+      b[k & 3] = fmaf(e, f[k] == -INFINITY ? 0.f : f[k] - st.m, b[k & 3]);
+    }
+    st.s += (a[0] + a[1]) + (a[2] + a[3]);
+    st.w += (b[0] + b[1]) + (b[2] + b[3]);
+  }
+}
+
+// Row results of the entropy state: logprob and lse as write_row_result,
+// plus the entropy.
+__device__ __forceinline__ void write_row_result(const Lse3& a, float xt, bool tvalid, float T,
+                                                 float c, float* logprob, float* lse,
+                                                 float* entropy, int32_t* err, int64_t row) {
+  write_row_result(Lse2{a.m, a.mc, a.s}, xt, tvalid, T, c, logprob, lse, err, row);
+  float H;
+  if (!tvalid || !(a.s > 0.f) || a.m == -INFINITY) {
+    H = __int_as_float(0x7FC00000);
+  } else {
+    const float r = fmaf(a.m, c, -a.mc);
+    H = (log2f(a.s) - r) * kLn2 - (a.w / a.s) / T;
+  }
+  entropy[row] = H;
+}
+
+// Overloads so kernels can be written once for either state.
+__device__ __forceinline__ void st_empty(Lse2& v) { v = lse2_empty(); }
+__device__ __forceinline__ void st_empty(Lse3& v) { v = lse3_empty(); }
+__device__ __forceinline__ Lse2 st_merge(Lse2 a, Lse2 b) { return lse2_merge(a, b); }
+__device__ __forceinline__ Lse3 st_merge(Lse3 a, Lse3 b) { return lse3_merge(a, b); }
+__device__ __forceinline__ Lse2 st_warp_reduce(Lse2 v) { return lse2_warp_reduce(v); }
+__device__ __forceinline__ Lse3 st_warp_reduce(Lse3 v) { return lse3_warp_reduce(v); }
+template <int K>
+__device__ __forceinline__ void st_fold(Lse2& st, const float* f, float c) { lse2_fold<K>(st, f, c); }
+template <int K>
+__device__ __forceinline__ void st_fold(Lse3& st, const float* f, float c) { lse3_fold<K>(st, f, c); }
+
 // ---- thread-block cluster helpers (distributed shared memory) --------------
 
 __device__ __forceinline__ void cluster_sync_all() {

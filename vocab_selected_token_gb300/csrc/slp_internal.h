@@ -21,6 +21,18 @@ cudaError_t launch_backward(const void* x, int dtype, int64_t N, int64_t V, int6
                             const float* grad_out, void* grad_x, int64_t ld_grad,
                             int32_t* err, cudaStream_t stream);
 
+cudaError_t launch_forward_entropy(const void* x, int dtype, int64_t N, int64_t V, int64_t ld,
+                                   const int32_t* t, const uint8_t* mask, float T,
+                                   float* logprob, float* lse, float* entropy, int32_t* err,
+                                   cudaStream_t stream);
+
+cudaError_t launch_backward_entropy(const void* x, int dtype, int64_t N, int64_t V, int64_t ld,
+                                    const int32_t* t, const uint8_t* mask, float T,
+                                    const float* lse, const float* entropy,
+                                    const float* grad_out, const float* grad_entropy,
+                                    void* grad_x, int64_t ld_grad, int32_t* err,
+                                    cudaStream_t stream);
+
 cudaError_t launch_forward_backward(const void* x, int dtype, int64_t N, int64_t V, int64_t ld,
                                     const int32_t* t, const uint8_t* mask, float T,
                                     const float* grad_out, float* logprob, float* lse,

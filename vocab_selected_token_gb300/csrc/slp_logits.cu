@@ -38,17 +38,20 @@ constexpr int kBwdThreads = 256;
 constexpr int kBwdUnroll = 4;
 constexpr int kMaxSplits = 8;  // portable cluster size
 
-template <typename Elt, bool kVecPath>
+// St is Lse2 (log-prob and lse) or Lse3 (also the entropy, written to
+// `entropy`, which is otherwise unused).
+template <typename Elt, bool kVecPath, typename St>
 __global__ void __launch_bounds__(kFwdThreads)
     slp_fwd_kernel(const Elt* __restrict__ x, int64_t V, int64_t ld,
                    const int32_t* __restrict__ t, const uint8_t* __restrict__ mask, float T,
                    float c, float* __restrict__ logprob, float* __restrict__ lse,
-                   int32_t* __restrict__ err, int splits) {
+                   float* __restrict__ entropy, int32_t* __restrict__ err, int splits) {
   using E = Elem<Elt>;
   constexpr int kVec = E::kVec;
   constexpr int kWarps = kFwdThreads / 32;
-  __shared__ Lse2 warp_part[kWarps];
-  __shared__ float cta_part[3];
+  constexpr bool kEnt = sizeof(St) == sizeof(Lse3);
+  __shared__ St warp_part[kWarps];
+  __shared__ float cta_part[4];
 
   const int64_t row = blockIdx.x / splits;
   const int rank = static_cast<int>(blockIdx.x - row * splits);
@@ -58,6 +61,7 @@ __global__ void __launch_bounds__(kFwdThreads)
     if (rank == 0 && threadIdx.x == 0) {
       logprob[row] = 0.f;
       lse[row] = 0.f;
+      if (kEnt) entropy[row] = 0.f;
     }
     return;
   }
@@ -67,7 +71,8 @@ __global__ void __launch_bounds__(kFwdThreads)
   float xt = 0.f;
   if (rank == 0 && threadIdx.x == 0 && tvalid) xt = E::load1(xr + tt);
 
-  Lse2 st = lse2_empty();
+  St st;
+  st_empty(st);
   if constexpr (kVecPath) {
     extern __shared__ __align__(128) uint8_t ring[];
     __shared__ __align__(8) uint64_t full[kFwdStages];
@@ -117,7 +122,7 @@ __global__ void __launch_bounds__(kFwdThreads)
       }
       __syncthreads();  // stage s fully read: thread 0 may refill it
       if (threadIdx.x == 0 && ch + kFwdStages < nch) issue(ch + kFwdStages);
-      lse2_fold<kPer * kVec>(st, &f[0][0], c);
+      st_fold<kPer * kVec>(st, &f[0][0], c);
     }
     if (ch < nch) {
       // a copy never landed: report it and wait (bounded) for the copies in
@@ -135,7 +140,7 @@ __global__ void __launch_bounds__(kFwdThreads)
       const int64_t e = nvec * kVec + threadIdx.x;
       if (e < V) {
         float f1[1] = {E::load1(xr + e)};
-        lse2_fold<1>(st, f1, c);
+        st_fold<1>(st, f1, c);
       }
     }
   } else {
@@ -148,23 +153,31 @@ __global__ void __launch_bounds__(kFwdThreads)
         const int64_t i = i0 + static_cast<int64_t>(u) * kFwdThreads;
         f[u] = (i < e1) ? E::load1(xr + i) : -INFINITY;
       }
-      lse2_fold<4>(st, f, c);
+      st_fold<4>(st, f, c);
     }
   }
 
   // CTA merge: warps, then the warp results in warp order.
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  st = lse2_warp_reduce(st);
+  st = st_warp_reduce(st);
   if (lane == 0) warp_part[warp] = st;
   __syncthreads();
+  auto finish = [&](const St& v) {
+    if constexpr (kEnt)
+      write_row_result(v, xt, tvalid, T, c, logprob, lse, entropy, err, row);
+    else
+      write_row_result(v, xt, tvalid, T, c, logprob, lse, err, row);
+  };
   if (warp == 0) {
-    Lse2 v = lane < kWarps ? warp_part[lane] : lse2_empty();
-    v = lse2_warp_reduce(v);
+    St v;
+    if (lane < kWarps) v = warp_part[lane];
+    else st_empty(v);
+    v = st_warp_reduce(v);
     if (lane == 0) {
-      cta_part[0] = v.m;
-      cta_part[1] = v.mc;
-      cta_part[2] = v.s;
-      if (splits == 1) write_row_result(v, xt, tvalid, T, c, logprob, lse, err, row);
+      const float* vf = reinterpret_cast<const float*>(&v);
+#pragma unroll
+      for (int k = 0; k < static_cast<int>(sizeof(St) / 4); ++k) cta_part[k] = vf[k];
+      if (splits == 1) finish(v);
     }
   }
   if (splits == 1) return;
@@ -174,24 +187,31 @@ __global__ void __launch_bounds__(kFwdThreads)
   // until those reads are done.
   cluster_sync_all();
   if (rank == 0 && threadIdx.x == 0) {
-    Lse2 acc{cta_part[0], cta_part[1], cta_part[2]};
+    St acc;
+    float* af = reinterpret_cast<float*>(&acc);
+#pragma unroll
+    for (int k = 0; k < static_cast<int>(sizeof(St) / 4); ++k) af[k] = cta_part[k];
     for (int r = 1; r < splits; ++r) {
-      Lse2 o;
-      o.m = ld_shared_cluster_f32(map_shared_rank(&cta_part[0], r));
-      o.mc = ld_shared_cluster_f32(map_shared_rank(&cta_part[1], r));
-      o.s = ld_shared_cluster_f32(map_shared_rank(&cta_part[2], r));
-      acc = lse2_merge(acc, o);
+      St o;
+      float* of = reinterpret_cast<float*>(&o);
+#pragma unroll
+      for (int k = 0; k < static_cast<int>(sizeof(St) / 4); ++k)
+        of[k] = ld_shared_cluster_f32(map_shared_rank(&cta_part[k], r));
+      acc = st_merge(acc, o);
     }
-    write_row_result(acc, xt, tvalid, T, c, logprob, lse, err, row);
+    finish(acc);
   }
   cluster_sync_all();
 }
 
-template <typename Elt, bool kVecPath>
+// kEnt adds the entropy term -gH p_v (log p_v + H) / T (H, gH per row; g and
+// gH may then be NULL, meaning zero).
+template <typename Elt, bool kVecPath, bool kEnt>
 __global__ void __launch_bounds__(kBwdThreads)
     slp_bwd_kernel(const Elt* __restrict__ x, int64_t V, int64_t ld,
                    const int32_t* __restrict__ t, const uint8_t* __restrict__ mask, float invT,
                    float c, const float* __restrict__ lse, const float* __restrict__ g,
+                   const float* __restrict__ H, const float* __restrict__ gH,
                    Elt* __restrict__ gx, int64_t ldg, int32_t* __restrict__ err,
                    int64_t tiles_per_row) {
   using E = Elem<Elt>;
@@ -205,18 +225,30 @@ __global__ void __launch_bounds__(kBwdThreads)
   Elt* gr = gx + row * ldg;
   const int64_t e_tile = tile * kTileElems;
 
-  float gT = 0.f, L2 = 0.f;
+  float gT = 0.f, L2 = 0.f, gHT = 0.f, offH = 0.f;
   int64_t tt = -1;
   if (active) {
     tt = t[row];
-    gT = g[row] * invT;
+    gT = (kEnt && g == nullptr) ? 0.f : g[row] * invT;
     L2 = lse[row] * kLog2e;
+    if (kEnt) {
+      gHT = gH == nullptr ? 0.f : gH[row] * invT;
+      offH = H[row] - lse[row];  // log p_v + H = x_v / T + offH
+    }
     if (tt < 0 || tt >= V) {
       if (err != nullptr && tile == 0 && threadIdx.x == 0) atomicOr(err, SLP_DATA_ERR_TARGET);
       gT = __int_as_float(0x7FC00000);
     }
   }
   const float a = -gT;
+  // gradient element from the logit xv, its probability p and whether it is
+  // the target
+  auto grad = [&](float xv, float p, bool is_t) {
+    float o = is_t ? fmaf(a, p, gT) : a * p;
+    // p log p -> 0 as p -> 0: a -inf logit adds nothing (and no 0 * -inf)
+    if (kEnt && p > 0.f) o = fmaf(-gHT * p, fmaf(xv, invT, offH), o);
+    return o;
+  };
 
   if constexpr (kVecPath) {
     uint4* gv = reinterpret_cast<uint4*>(gr);
@@ -250,13 +282,14 @@ __global__ void __launch_bounds__(kBwdThreads)
 #pragma unroll
         for (int k = 0; k < kVec; ++k) {
           const float p = ex2(fmaf(f[k], c, -L2));
-          f[k] = (rel == k) ? fmaf(a, p, gT) : a * p;
+          f[k] = grad(f[k], p, rel == k);
         }
         st_stream(gv + e / kVec, E::pack(f));
       } else {
         for (int64_t k = e; k < V; ++k) {
-          const float p = ex2(fmaf(E::load1(xr + k), c, -L2));
-          E::store1(gr + k, (k == tt) ? fmaf(a, p, gT) : a * p);
+          const float xv = E::load1(xr + k);
+          const float p = ex2(fmaf(xv, c, -L2));
+          E::store1(gr + k, grad(xv, p, k == tt));
         }
       }
     }
@@ -265,8 +298,9 @@ __global__ void __launch_bounds__(kBwdThreads)
     for (int64_t e = e_tile + threadIdx.x; e < e_end; e += kBwdThreads) {
       float out = 0.f;
       if (active) {
-        const float p = ex2(fmaf(E::load1(xr + e), c, -L2));
-        out = (e == tt) ? fmaf(a, p, gT) : a * p;
+        const float xv = E::load1(xr + e);
+        const float p = ex2(fmaf(xv, c, -L2));
+        out = grad(xv, p, e == tt);
       }
       E::store1(gr + e, out);
     }
@@ -473,10 +507,10 @@ int choose_splits(int64_t N, int64_t V) {
   return static_cast<int>(s);
 }
 
-template <typename Elt>
+template <typename Elt, typename St>
 cudaError_t fwd_typed(const Elt* x, int64_t N, int64_t V, int64_t ld, const int32_t* t,
-                      const uint8_t* mask, float T, float* logprob, float* lse, int32_t* err,
-                      cudaStream_t stream) {
+                      const uint8_t* mask, float T, float* logprob, float* lse, float* entropy,
+                      int32_t* err, cudaStream_t stream) {
   const int splits = choose_splits(N, V);
   if (N * splits > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
   const float c = static_cast<float>(1.4426950408889634 / static_cast<double>(T));
@@ -487,7 +521,7 @@ cudaError_t fwd_typed(const Elt* x, int64_t N, int64_t V, int64_t ld, const int3
   cfg.dynamicSmemBytes = vec ? kFwdSmem : 0;
   cfg.stream = stream;
   if (vec) {
-    cudaError_t e = cudaFuncSetAttribute(slp_fwd_kernel<Elt, true>,
+    cudaError_t e = cudaFuncSetAttribute(slp_fwd_kernel<Elt, true, St>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kFwdSmem);
     if (e != cudaSuccess) return e;
   }
@@ -501,16 +535,17 @@ cudaError_t fwd_typed(const Elt* x, int64_t N, int64_t V, int64_t ld, const int3
     cfg.numAttrs = 1;
   }
   if (vec)
-    return cudaLaunchKernelEx(&cfg, slp_fwd_kernel<Elt, true>, x, V, ld, t, mask, T, c, logprob,
-                              lse, err, splits);
-  return cudaLaunchKernelEx(&cfg, slp_fwd_kernel<Elt, false>, x, V, ld, t, mask, T, c, logprob,
-                            lse, err, splits);
+    return cudaLaunchKernelEx(&cfg, slp_fwd_kernel<Elt, true, St>, x, V, ld, t, mask, T, c,
+                              logprob, lse, entropy, err, splits);
+  return cudaLaunchKernelEx(&cfg, slp_fwd_kernel<Elt, false, St>, x, V, ld, t, mask, T, c, logprob,
+                            lse, entropy, err, splits);
 }
 
-template <typename Elt>
+template <typename Elt, bool kEnt>
 cudaError_t bwd_typed(const Elt* x, int64_t N, int64_t V, int64_t ld, const int32_t* t,
-                      const uint8_t* mask, float T, const float* lse, const float* g, Elt* gx,
-                      int64_t ldg, int32_t* err, cudaStream_t stream) {
+                      const uint8_t* mask, float T, const float* lse, const float* g,
+                      const float* H, const float* gH, Elt* gx, int64_t ldg, int32_t* err,
+                      cudaStream_t stream) {
   constexpr int64_t kTileElems =
       static_cast<int64_t>(kBwdThreads) * kBwdUnroll * Elem<Elt>::kVec;
   const int64_t tiles = (V + kTileElems - 1) / kTileElems;
@@ -520,11 +555,11 @@ cudaError_t bwd_typed(const Elt* x, int64_t N, int64_t V, int64_t ld, const int3
   const float c = static_cast<float>(1.4426950408889634 / static_cast<double>(T));
   const bool vec = aligned16(x, ld, sizeof(Elt)) && aligned16(gx, ldg, sizeof(Elt));
   if (vec)
-    slp_bwd_kernel<Elt, true><<<static_cast<unsigned>(blocks), kBwdThreads, 0, stream>>>(
-        x, V, ld, t, mask, invT, c, lse, g, gx, ldg, err, tiles);
+    slp_bwd_kernel<Elt, true, kEnt><<<static_cast<unsigned>(blocks), kBwdThreads, 0, stream>>>(
+        x, V, ld, t, mask, invT, c, lse, g, H, gH, gx, ldg, err, tiles);
   else
-    slp_bwd_kernel<Elt, false><<<static_cast<unsigned>(blocks), kBwdThreads, 0, stream>>>(
-        x, V, ld, t, mask, invT, c, lse, g, gx, ldg, err, tiles);
+    slp_bwd_kernel<Elt, false, kEnt><<<static_cast<unsigned>(blocks), kBwdThreads, 0, stream>>>(
+        x, V, ld, t, mask, invT, c, lse, g, H, gH, gx, ldg, err, tiles);
   return cudaGetLastError();
 }
 
@@ -571,10 +606,21 @@ cudaError_t launch_forward(const void* x, int dtype, int64_t N, int64_t V, int64
                            const int32_t* t, const uint8_t* mask, float T, float* logprob,
                            float* lse, int32_t* err, cudaStream_t stream) {
   if (dtype == SLP_BF16)
-    return fwd_typed(static_cast<const __nv_bfloat16*>(x), N, V, ld, t, mask, T, logprob, lse,
-                     err, stream);
-  return fwd_typed(static_cast<const float*>(x), N, V, ld, t, mask, T, logprob, lse, err,
-                   stream);
+    return fwd_typed<__nv_bfloat16, Lse2>(static_cast<const __nv_bfloat16*>(x), N, V, ld, t, mask,
+                                          T, logprob, lse, nullptr, err, stream);
+  return fwd_typed<float, Lse2>(static_cast<const float*>(x), N, V, ld, t, mask, T, logprob, lse,
+                                nullptr, err, stream);
+}
+
+cudaError_t launch_forward_entropy(const void* x, int dtype, int64_t N, int64_t V, int64_t ld,
+                                   const int32_t* t, const uint8_t* mask, float T,
+                                   float* logprob, float* lse, float* entropy, int32_t* err,
+                                   cudaStream_t stream) {
+  if (dtype == SLP_BF16)
+    return fwd_typed<__nv_bfloat16, Lse3>(static_cast<const __nv_bfloat16*>(x), N, V, ld, t, mask,
+                                          T, logprob, lse, entropy, err, stream);
+  return fwd_typed<float, Lse3>(static_cast<const float*>(x), N, V, ld, t, mask, T, logprob, lse,
+                                entropy, err, stream);
 }
 
 cudaError_t launch_backward(const void* x, int dtype, int64_t N, int64_t V, int64_t ld,
@@ -582,10 +628,29 @@ cudaError_t launch_backward(const void* x, int dtype, int64_t N, int64_t V, int6
                             const float* grad_out, void* grad_x, int64_t ld_grad,
                             int32_t* err, cudaStream_t stream) {
   if (dtype == SLP_BF16)
-    return bwd_typed(static_cast<const __nv_bfloat16*>(x), N, V, ld, t, mask, T, lse, grad_out,
-                     static_cast<__nv_bfloat16*>(grad_x), ld_grad, err, stream);
-  return bwd_typed(static_cast<const float*>(x), N, V, ld, t, mask, T, lse, grad_out,
-                   static_cast<float*>(grad_x), ld_grad, err, stream);
+    return bwd_typed<__nv_bfloat16, false>(static_cast<const __nv_bfloat16*>(x), N, V, ld, t,
+                                           mask, T, lse, grad_out, nullptr, nullptr,
+                                           static_cast<__nv_bfloat16*>(grad_x), ld_grad, err,
+                                           stream);
+  return bwd_typed<float, false>(static_cast<const float*>(x), N, V, ld, t, mask, T, lse,
+                                 grad_out, nullptr, nullptr, static_cast<float*>(grad_x),
+                                 ld_grad, err, stream);
+}
+
+cudaError_t launch_backward_entropy(const void* x, int dtype, int64_t N, int64_t V, int64_t ld,
+                                    const int32_t* t, const uint8_t* mask, float T,
+                                    const float* lse, const float* entropy,
+                                    const float* grad_out, const float* grad_entropy,
+                                    void* grad_x, int64_t ld_grad, int32_t* err,
+                                    cudaStream_t stream) {
+  if (dtype == SLP_BF16)
+    return bwd_typed<__nv_bfloat16, true>(static_cast<const __nv_bfloat16*>(x), N, V, ld, t,
+                                          mask, T, lse, grad_out, entropy, grad_entropy,
+                                          static_cast<__nv_bfloat16*>(grad_x), ld_grad, err,
+                                          stream);
+  return bwd_typed<float, true>(static_cast<const float*>(x), N, V, ld, t, mask, T, lse,
+                                grad_out, entropy, grad_entropy, static_cast<float*>(grad_x),
+                                ld_grad, err, stream);
 }
 
 cudaError_t launch_forward_backward(const void* x, int dtype, int64_t N, int64_t V, int64_t ld,
