@@ -439,8 +439,45 @@ def other_workloads(device, hbm):
         del inp, r
         torch.cuda.empty_cache()
     out["fused_fwd_bwd"] = time_fused(device, hbm)
+    out["entropy"] = time_entropy(device, hbm)
     out["lmhead"] = time_lmhead(device)
     return out
+
+
+def time_entropy(device, hbm, steps=30, warmup=3):
+    """slp_forward_entropy + slp_backward_entropy on c151k (same bytes as the
+    plain step: the entropy is one more accumulator in the same pass)."""
+    import vocab_selected_token_gb300 as slp
+    from vocab_selected_token_gb300 import workloads as W
+    inp = W.make_logits_inputs("c151k", device=device)
+    N, V = inp.x.shape
+    fwd_b, bwd_b, _ = logits_bytes(inp.x, inp.mask)
+    gH = torch.rand(N, device=device)
+    lp = torch.empty(N, device=device)
+    lse = torch.empty(N, device=device)
+    H = torch.empty(N, device=device)
+    gx = torch.empty_like(inp.x)
+    s = torch.cuda.current_stream(device)
+
+    def step():
+        slp.slp_forward_entropy(inp.x, inp.t, None, inp.T, logprob=lp, lse=lse, entropy=H)
+        slp.slp_backward_entropy(inp.x, inp.t, None, inp.T, lse, H, inp.g, gH, grad_x=gx)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(steps):
+        step()
+    e1.record(s)
+    torch.cuda.synchronize(device)
+    ms = e0.elapsed_time(e1) / steps
+    del inp, gx
+    torch.cuda.empty_cache()
+    return {"workload": "c151k", "ms_per_step": ms, "tokens_per_s": N * 1000.0 / ms,
+            "gbs": (fwd_b + bwd_b) / (ms * 1e-3) / 1e9,
+            "frac_of_measured": (fwd_b + bwd_b) / (ms * 1e-3) / 1e9 / hbm}
 
 
 def time_fused(device, hbm, steps=30, warmup=3):
