@@ -60,6 +60,8 @@ __all__ = [
     "lmhead_dW_rows",
     "entropy_forward",
     "entropy_backward",
+    "topk_kl_forward",
+    "topk_kl_backward",
 ]
 
 
@@ -282,4 +284,68 @@ def entropy_backward(x, t, mask, T: float, lse, H, grad_out, grad_entropy):
             logp = x[n] / T - lse[n]
             p = np.exp(logp)
             grad[n] -= gH[n] * np.where(p > 0, p * (logp + H[n]), 0.0) / T
+    return grad
+
+
+def topk_kl_forward(x, ids, teacher_logp, mask, T: float, clamp_min=None):
+    """Forward KL of the student softmax(x / T) against a teacher given only by
+    its top-K token ids and log-probabilities, over that support (verl PR
+    #7733 "memory-efficient chunked top-k KL", "Design & Code Changes":
+    gather the teacher top-k plus the student statistics at those ids, with
+    the student's global logZ):
+
+        ls[k] = x[n, ids[n, k]] / T - lse[n]         (student log-prob)
+        lc[k] = max(ls[k], clamp_min)                 (when a clamp is given)
+        kl[n] = sum_k exp(lt[k]) (lt[k] - lc[k])
+        student_mass[n] = sum_k exp(ls[k]),  teacher_mass[n] = sum_k exp(lt[k])
+
+    Returns (kl, student_mass, teacher_mass, lse) in float64; inactive rows 0.
+    """
+    x = _as_f64(x)
+    N = x.shape[0]
+    ids = np.asarray(ids).reshape(N, -1).astype(np.int64)
+    lt = _as_f64(teacher_logp).reshape(N, -1)
+    active = _active_rows(N, mask)
+    _, lse = selected_logprob_forward(x, np.zeros(N, np.int64), mask, T)
+    kl = np.zeros(N)
+    sm = np.zeros(N)
+    tm = np.zeros(N)
+    for n in range(N):
+        if not active[n]:
+            continue
+        ls = x[n, ids[n]] / T - lse[n]
+        lc = ls if clamp_min is None else np.maximum(ls, clamp_min)
+        p = np.exp(lt[n])
+        kl[n] = np.sum(p * (lt[n] - lc))
+        sm[n] = np.sum(np.exp(ls))
+        tm[n] = np.sum(p)
+    return kl, sm, tm, lse
+
+
+def topk_kl_backward(x, ids, teacher_logp, mask, T: float, clamp_min, lse, grad_kl):
+    """Gradient of sum_n g[n] kl[n] with respect to x.  d kl / d ls[k] is
+    -p[k] where ls[k] >= clamp_min (the clamp's flat side gives 0), and
+    d ls[k] / d x[v] = (1[v = ids[k]] - q[v]) / T with q = softmax(x / T):
+
+        grad_x[n, v] = g[n] / T * ( P q[v] - sum_{k: ids[k] = v, kept} p[k] ),
+        P = sum of p[k] over the kept k.
+    """
+    x = _as_f64(x)
+    N, V = x.shape
+    ids = np.asarray(ids).reshape(N, -1).astype(np.int64)
+    lt = _as_f64(teacher_logp).reshape(N, -1)
+    lse = _as_f64(lse).reshape(N)
+    g = _as_f64(grad_kl).reshape(N)
+    active = _active_rows(N, mask)
+    grad = np.zeros((N, V))
+    for n in range(N):
+        if not active[n]:
+            continue
+        ls = x[n, ids[n]] / T - lse[n]
+        keep = np.ones_like(ls, bool) if clamp_min is None else ls >= clamp_min
+        p = np.exp(lt[n]) * keep
+        q = np.exp(x[n] / T - lse[n])
+        row = p.sum() * q
+        np.add.at(row, ids[n], -p)
+        grad[n] = g[n] * row / T
     return grad

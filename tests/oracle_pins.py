@@ -333,3 +333,64 @@ def pin_entropy_finite_differences(ent_fwd, ent_bwd):
             fd[n, v] = (L(xp) - L(xm)) / (2 * hs)
     _close(gx, fd, 1e-7, 1e-9, "entropy finite differences")
     assert (gx[2] == 0).all()
+
+
+# --- top-k forward KL ------------------------------------------------------------
+
+def pin_topk_kl_library(kl_fwd):
+    """kl equals torch's kl_div with log targets over the support; a teacher
+    equal to the student on the whole vocabulary gives kl = 0 and both masses 1."""
+    r = _rng(15)
+    N, V, K, T = 6, 200, 16, 0.8
+    x = r.normal(0, 2, (N, V))
+    ids = np.stack([r.choice(V, K, replace=False) for _ in range(N)])
+    lt = np.log(r.dirichlet(np.ones(K), N) * 0.9)
+    kl, sm, tm, lse = kl_fwd(x, ids, lt, None, T, None)
+    ls = x[np.arange(N)[:, None], ids] / T - lse[:, None]
+    ref = [float(F.kl_div(torch.from_numpy(ls[n]), torch.from_numpy(lt[n]), log_target=True,
+                          reduction="sum")) for n in range(N)]
+    _close(kl, ref, 1e-12, 1e-13, "top-k kl vs kl_div")
+    _close(tm, np.full(N, 0.9), 1e-12, 0, "teacher mass")
+    _close(sm, np.exp(ls).sum(axis=1), 1e-12, 0, "student mass")
+    full = np.tile(np.arange(V), (N, 1))
+    lt_s = x / T - torch.logsumexp(torch.from_numpy(x / T), dim=1).numpy()[:, None]
+    kl0, sm0, tm0, _ = kl_fwd(x, full, lt_s, None, T, None)
+    _close(kl0, np.zeros(N), 0, 1e-12, "self kl")
+    _close(sm0, np.ones(N), 1e-12, 0, "full student mass")
+
+
+def pin_topk_kl_clamp(kl_fwd):
+    """With a clamp, terms below it use the clamp value."""
+    x = np.array([[0.0, -30.0, 1.0, 2.0]])
+    ids = np.array([[1, 2]])
+    lt = np.log(np.array([[0.5, 0.25]]))
+    kl, _, _, lse = kl_fwd(x, ids, lt, None, 1.0, -10.0)
+    ls2 = 1.0 - lse[0]
+    ref = 0.5 * (np.log(0.5) + 10.0) + 0.25 * (np.log(0.25) - ls2)
+    _close(kl, [ref], 1e-13, 1e-13, "clamped kl")
+
+
+def pin_topk_kl_finite_differences(kl_fwd, kl_bwd):
+    r = _rng(16)
+    N, V, K, T, hs = 3, 11, 4, 0.9, 1e-6
+    x = r.normal(0, 1.5, (N, V))
+    x[1, 3] = -25.0          # far below the clamp: flat side
+    ids = np.array([[0, 5, 5, 9], [3, 1, 2, 10], [4, 6, 7, 8]])   # a repeated id too
+    lt = np.log(r.dirichlet(np.ones(K), N) * 0.8)
+    g = r.uniform(-1, 1, N)
+    mask = np.array([1, 1, 0], np.uint8)
+    for clamp in (None, -10.0):
+        kl, _, _, lse = kl_fwd(x, ids, lt, mask, T, clamp)
+        gx = kl_bwd(x, ids, lt, mask, T, clamp, lse, g)
+
+        def L(xx):
+            return float(np.dot(g, kl_fwd(xx, ids, lt, mask, T, clamp)[0]))
+
+        fd = np.zeros_like(x)
+        for n in range(N):
+            for v in range(V):
+                xp = x.copy(); xp[n, v] += hs
+                xm = x.copy(); xm[n, v] -= hs
+                fd[n, v] = (L(xp) - L(xm)) / (2 * hs)
+        _close(gx, fd, 1e-6, 1e-9, f"top-k kl finite differences clamp={clamp}")
+        assert (gx[2] == 0).all()

@@ -160,3 +160,33 @@ def test_entropy_pins_catch_planted_mistakes():
     for bad in (bwd_wrong_sign, bwd_no_H):
         with pytest.raises(AssertionError):
             pin_entropy_finite_differences(O.entropy_forward, bad)
+
+
+def test_topk_kl_pins():
+    from tests.oracle_pins import (pin_topk_kl_clamp, pin_topk_kl_finite_differences,
+                                   pin_topk_kl_library)
+    pin_topk_kl_library(O.topk_kl_forward)
+    pin_topk_kl_clamp(O.topk_kl_forward)
+    pin_topk_kl_finite_differences(O.topk_kl_forward, O.topk_kl_backward)
+
+
+def test_topk_kl_pins_catch_planted_mistakes():
+    from tests.oracle_pins import pin_topk_kl_finite_differences, pin_topk_kl_library
+
+    def fwd_unnormalised(x, ids, lt, mask, T, clamp):   # forgets the student's lse
+        kl, sm, tm, lse = O.topk_kl_forward(x, ids, lt, mask, T, clamp)
+        return kl + np.asarray(np.exp(lt)).sum(axis=1) * lse, sm, tm, lse
+
+    def bwd_no_dense(x, ids, lt, mask, T, clamp, lse, g):  # drops the P q term
+        gx = O.topk_kl_backward(x, ids, lt, mask, T, clamp, lse, g)
+        q = np.exp(np.asarray(x) / T - np.asarray(lse)[:, None])
+        return gx - 0.5 * np.asarray(g)[:, None] * q / T
+
+    def bwd_ignores_clamp(x, ids, lt, mask, T, clamp, lse, g):
+        return O.topk_kl_backward(x, ids, lt, mask, T, None, lse, g)
+
+    with pytest.raises(AssertionError):
+        pin_topk_kl_library(fwd_unnormalised)
+    for bad in (bwd_no_dense, bwd_ignores_clamp):
+        with pytest.raises(AssertionError):
+            pin_topk_kl_finite_differences(O.topk_kl_forward, bad)
