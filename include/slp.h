@@ -159,6 +159,53 @@ int slp_backward_entropy(const void* x, int dtype, int64_t N, int64_t V, int64_t
                          void* grad_x, int64_t ld_grad, int32_t* err, void* stream);
 
 /*
+ * slp_topk_kl_forward - per-token forward KL of the student softmax(x / T)
+ * against a teacher given only by its top-K token ids and log-probabilities,
+ * over that support, with the student's full-vocabulary logZ.
+ *
+ * Defined by: verl PR #7733 "memory-efficient chunked top-k KL", "What does
+ * this PR do?" and "Design & Code Changes" (teacher top-k plus student
+ * statistics, global logZ from MAX/SUM reductions, recompute in backward):
+ *
+ *   ls[k] = x[n, ids[n,k]] / T - lse[n],   lc[k] = max(ls[k], clamp_min)
+ *   kl[n] = sum_k exp(lt[n,k]) (lt[n,k] - lc[k])
+ *   student_mass[n] = sum_k exp(ls[k]),   teacher_mass[n] = sum_k exp(lt[n,k])
+ *
+ *   x, dtype, N, V, ld, mask, T, err, stream   as for slp_forward.
+ *   ids           [N, K] int32 teacher token ids, row-major (repeats allowed).
+ *   teacher_logp  [N, K] float32 teacher log-probabilities of those ids.
+ *   K             entries per row, >= 1.
+ *   clamp_min     lower clamp of the student log-probabilities in kl
+ *                 (-INFINITY for none; the pages' runs use -10).
+ *   kl, student_mass, teacher_mass, lse   [N] float32 out (0 on inactive rows).
+ * An id outside [0, V) on an active row sets SLP_DATA_ERR_TARGET and makes
+ * that row's outputs NaN.
+ */
+int slp_topk_kl_forward(const void* x, int dtype, int64_t N, int64_t V, int64_t ld,
+                        const int32_t* ids, const float* teacher_logp, int64_t K,
+                        const uint8_t* mask, float T, float clamp_min,
+                        float* kl, float* student_mass, float* teacher_mass, float* lse,
+                        int32_t* err, void* stream);
+
+/*
+ * slp_topk_kl_backward - gradient of sum_n grad_kl[n] kl[n] with respect to x:
+ *
+ *   grad_x[n,v] = grad_kl[n] / T * ( P q[v] - sum_{k: ids[k] = v, ls[k] >= clamp_min}
+ *                 exp(lt[k]) ),   P = sum of exp(lt[k]) over the kept k,
+ *
+ * with q = softmax(x / T) recomputed from x and the saved lse (the clamp's
+ * flat side contributes no gradient).  Arguments as slp_topk_kl_forward plus
+ * lse (from it), grad_kl [N] float32, grad_x [N, ld_grad] in x's dtype.
+ * Returns SLP_ERR_UNSUPPORTED when ceil(V/32)*4 + 8K bytes exceed 160 KB
+ * (the per-row id bitmap in shared memory), i.e. V above ~1.3 million.
+ */
+int slp_topk_kl_backward(const void* x, int dtype, int64_t N, int64_t V, int64_t ld,
+                         const int32_t* ids, const float* teacher_logp, int64_t K,
+                         const uint8_t* mask, float T, float clamp_min, const float* lse,
+                         const float* grad_kl, void* grad_x, int64_t ld_grad,
+                         int32_t* err, void* stream);
+
+/*
  * slp_forward_backward - slp_forward and slp_backward in one pass, for the
  * training case where grad_out is known when the forward runs (for example
  * g = -advantage for a plain policy-gradient loss).

@@ -26,6 +26,7 @@ from ._lib import SlpError
 __all__ = [
     "SlpError", "slp_forward", "slp_backward", "slp_forward_backward",
     "slp_forward_entropy", "slp_backward_entropy", "selected_logprob_and_entropy",
+    "slp_topk_kl_forward", "slp_topk_kl_backward",
     "slp_lmhead_workspace_size",
     "slp_lmhead_forward_workspace_size", "slp_lmhead_forward_noalloc",
     "slp_lmhead_forward", "slp_lmhead_backward", "selected_logprob",
@@ -163,6 +164,46 @@ def selected_logprob_and_entropy(x, t, mask=None, temperature: float = 1.0):
     autograd backward covering both outputs."""
     lp, H, _ = _SelectedLogprobEntropy.apply(x, t, mask, float(temperature))
     return lp, H
+
+
+def _check_topk(ids, lt, N):
+    if ids.dim() != 2 or ids.shape[0] != N or ids.dtype != torch.int32 or not ids.is_contiguous():
+        raise ValueError("ids must be a contiguous [N, K] int32 tensor")
+    if lt.shape != ids.shape or lt.dtype != torch.float32 or not lt.is_contiguous():
+        raise ValueError("teacher_logp must be a contiguous [N, K] float32 tensor")
+    return ids.shape[1]
+
+
+def slp_topk_kl_forward(x, ids, teacher_logp, mask=None, T: float = 1.0,
+                        clamp_min: float = float("-inf"), err=None, stream=None):
+    """Top-k forward KL.  Returns (kl, student_mass, teacher_mass, lse)."""
+    N, V, ld = _logits_layout(x)
+    K = _check_topk(ids, teacher_logp, N)
+    if mask is not None:
+        _check_vec("mask", mask, N, torch.uint8)
+    out = [torch.empty(N, dtype=torch.float32, device=x.device) for _ in range(4)]
+    _lib.call("slp_topk_kl_forward", _ptr(x), _DTYPES[x.dtype], N, V, ld, _ptr(ids),
+              _ptr(teacher_logp), K, _ptr(mask), float(T), float(clamp_min), _ptr(out[0]),
+              _ptr(out[1]), _ptr(out[2]), _ptr(out[3]), _ptr(err), _stream_handle(stream))
+    return tuple(out)
+
+
+def slp_topk_kl_backward(x, ids, teacher_logp, mask, T: float, clamp_min: float, lse, grad_kl,
+                         grad_x=None, err=None, stream=None):
+    """Gradient of sum(grad_kl * kl) with respect to x."""
+    N, V, ld = _logits_layout(x)
+    K = _check_topk(ids, teacher_logp, N)
+    if mask is not None:
+        _check_vec("mask", mask, N, torch.uint8)
+    _check_vec("lse", lse, N, torch.float32)
+    _check_vec("grad_kl", grad_kl, N, torch.float32)
+    if grad_x is None:
+        grad_x = torch.empty((N, V), dtype=x.dtype, device=x.device)
+    ldg = grad_x.stride(0) if N > 1 else max(V, 1)
+    _lib.call("slp_topk_kl_backward", _ptr(x), _DTYPES[x.dtype], N, V, ld, _ptr(ids),
+              _ptr(teacher_logp), K, _ptr(mask), float(T), float(clamp_min), _ptr(lse),
+              _ptr(grad_kl), _ptr(grad_x), ldg, _ptr(err), _stream_handle(stream))
+    return grad_x
 
 
 def slp_forward_backward(x, t, mask, T: float, grad_out, logprob=None, lse=None, grad_x=None,

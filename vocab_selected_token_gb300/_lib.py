@@ -35,6 +35,10 @@ SIGNATURES = {
                                    _vp, _vp]),
     "slp_backward_entropy": (_int, [_vp, _int, _i64, _i64, _i64, _vp, _vp, _f32, _vp, _vp, _vp,
                                     _vp, _vp, _i64, _vp, _vp]),
+    "slp_topk_kl_forward": (_int, [_vp, _int, _i64, _i64, _i64, _vp, _vp, _i64, _vp, _f32, _f32,
+                                   _vp, _vp, _vp, _vp, _vp, _vp]),
+    "slp_topk_kl_backward": (_int, [_vp, _int, _i64, _i64, _i64, _vp, _vp, _i64, _vp, _f32, _f32,
+                                    _vp, _vp, _vp, _i64, _vp, _vp]),
     "slp_forward_backward": (_int, [_vp, _int, _i64, _i64, _i64, _vp, _vp, _f32, _vp, _vp, _vp,
                                     _vp, _i64, _vp, _vp]),
     "slp_lmhead_workspace_size": (_sz, [_i64, _i64, _i64]),

@@ -107,6 +107,40 @@ int slp_backward_entropy(const void* x, int dtype, int64_t N, int64_t V, int64_t
                                                   static_cast<cudaStream_t>(stream)));
 }
 
+int slp_topk_kl_forward(const void* x, int dtype, int64_t N, int64_t V, int64_t ld,
+                        const int32_t* ids, const float* teacher_logp, int64_t K,
+                        const uint8_t* mask, float T, float clamp_min, float* kl,
+                        float* student_mass, float* teacher_mass, float* lse, int32_t* err,
+                        void* stream) {
+  int st = check_logits_args(x, dtype, N, V, ld, ids, T);
+  if (st != SLP_OK) return st;
+  if (K < 1 || K > INT32_MAX / 2 || isnan(clamp_min)) return SLP_ERR_INVALID_ARG;
+  if (N == 0) return SLP_OK;
+  if (teacher_logp == nullptr || kl == nullptr || student_mass == nullptr ||
+      teacher_mass == nullptr || lse == nullptr)
+    return SLP_ERR_INVALID_ARG;
+  return cuda_status(slp::launch_topk_kl_forward(x, dtype, N, V, ld, ids, teacher_logp, K, mask,
+                                                 T, clamp_min, kl, student_mass, teacher_mass,
+                                                 lse, err, static_cast<cudaStream_t>(stream)));
+}
+
+int slp_topk_kl_backward(const void* x, int dtype, int64_t N, int64_t V, int64_t ld,
+                         const int32_t* ids, const float* teacher_logp, int64_t K,
+                         const uint8_t* mask, float T, float clamp_min, const float* lse,
+                         const float* grad_kl, void* grad_x, int64_t ld_grad, int32_t* err,
+                         void* stream) {
+  int st = check_logits_args(x, dtype, N, V, ld, ids, T);
+  if (st != SLP_OK) return st;
+  if (K < 1 || K > INT32_MAX / 2 || isnan(clamp_min) || ld_grad < V) return SLP_ERR_INVALID_ARG;
+  if (static_cast<size_t>(V) > slp::topk_kl_max_vocab(K)) return SLP_ERR_UNSUPPORTED;
+  if (N == 0) return SLP_OK;
+  if (teacher_logp == nullptr || lse == nullptr || grad_kl == nullptr || grad_x == nullptr)
+    return SLP_ERR_INVALID_ARG;
+  return cuda_status(slp::launch_topk_kl_backward(x, dtype, N, V, ld, ids, teacher_logp, K, mask,
+                                                  T, clamp_min, lse, grad_kl, grad_x, ld_grad,
+                                                  err, static_cast<cudaStream_t>(stream)));
+}
+
 int slp_forward_backward(const void* x, int dtype, int64_t N, int64_t V, int64_t ld,
                          const int32_t* t, const uint8_t* mask, float T, const float* grad_out,
                          float* logprob, float* lse, void* grad_x, int64_t ld_grad, int32_t* err,

@@ -167,7 +167,7 @@ __device__ __forceinline__ void write_row_result(const Lse2& a, float xt, bool t
     l = a.m / T + ln_s;
     lp = (xt - a.m) / T - ln_s;
   }
-  logprob[row] = lp;
+  if (logprob != nullptr) logprob[row] = lp;  // NULL: log-sum-exp only
   lse[row] = l;
 }
 

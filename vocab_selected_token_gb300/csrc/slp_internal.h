@@ -39,6 +39,19 @@ cudaError_t launch_forward_backward(const void* x, int dtype, int64_t N, int64_t
                                     void* grad_x, int64_t ld_grad, int32_t* err,
                                     cudaStream_t stream);
 
+// Top-k forward KL (slp_topk.cu).
+size_t topk_kl_max_vocab(int64_t K);
+cudaError_t launch_topk_kl_forward(const void* x, int dtype, int64_t N, int64_t V, int64_t ld,
+                                   const int32_t* ids, const float* teacher_logp, int64_t K,
+                                   const uint8_t* mask, float T, float clamp_min, float* kl,
+                                   float* student_mass, float* teacher_mass, float* lse,
+                                   int32_t* err, cudaStream_t stream);
+cudaError_t launch_topk_kl_backward(const void* x, int dtype, int64_t N, int64_t V, int64_t ld,
+                                    const int32_t* ids, const float* teacher_logp, int64_t K,
+                                    const uint8_t* mask, float T, float clamp_min,
+                                    const float* lse, const float* grad_kl, void* grad_x,
+                                    int64_t ld_grad, int32_t* err, cudaStream_t stream);
+
 // Fused LM-head path (slp_lmhead.cu).
 size_t lmhead_workspace_size(int64_t N, int64_t V, int64_t d);
 size_t lmhead_forward_workspace_size(int64_t N, int64_t V, int64_t d);

@@ -59,14 +59,15 @@ __global__ void __launch_bounds__(kFwdThreads)
   // together (no cluster barrier is left waiting).
   if (mask != nullptr && mask[row] == 0) {
     if (rank == 0 && threadIdx.x == 0) {
-      logprob[row] = 0.f;
+      if (logprob != nullptr) logprob[row] = 0.f;
       lse[row] = 0.f;
       if (kEnt) entropy[row] = 0.f;
     }
     return;
   }
   const Elt* xr = x + row * ld;
-  const int32_t tt = t[row];
+  // t == NULL: log-sum-exp only (no target, logprob not written)
+  const int32_t tt = t != nullptr ? t[row] : 0;
   const bool tvalid = tt >= 0 && static_cast<int64_t>(tt) < V;
   float xt = 0.f;
   if (rank == 0 && threadIdx.x == 0 && tvalid) xt = E::load1(xr + tt);

@@ -37,6 +37,10 @@ WORKLOADS = {
                       recipe="f32 x~N(0,4^2); each entry +-80 with p=0.01; "
                              "round(0.05N) rows get 1024 distinct -inf columns; "
                              "t~U over finite columns; g~U(-1,1)"),
+    "topk": dict(seed=5, N=4096, V=248320, K=128, dtype="bf16", T=1.0, clamp=-10.0,
+                 recipe="student bf16 x~N(0,3^2); teacher ids = top-K of x + N(0,1) noise; "
+                        "teacher p_k = mass (1-r) r^k / (1-r^K), r=0.95, mass~U(0.85,0.99); "
+                        "clamp -10; g~U(-1,1)"),
     "lmhead": dict(seed=4, N=8192, V=151936, d=2560, dtype="bf16", T=1.0,
                    recipe="h bf16~N(0,1) [N,d]; W bf16~N(0,0.02^2) [V,d]; "
                           "t~U[0,V); mask~Bernoulli(0.5); g~U(-1,1)"),
@@ -50,6 +54,18 @@ class LogitsInputs:
     mask: torch.Tensor | None  # [N] uint8 or None
     T: float
     g: torch.Tensor          # [N] f32 (upstream gradient of logprob)
+    name: str
+
+
+@dataclass
+class TopKInputs:
+    x: torch.Tensor          # [N, V] student logits
+    ids: torch.Tensor        # [N, K] int32 teacher top-K token ids (distinct per row)
+    lt: torch.Tensor         # [N, K] f32 teacher log-probabilities of those ids
+    mask: torch.Tensor | None
+    T: float
+    clamp: float
+    g: torch.Tensor          # [N] f32 upstream gradient of the per-token KL
     name: str
 
 
@@ -186,3 +202,34 @@ def make_lmhead_inputs(name: str = "lmhead", device="cpu", N: int | None = None,
     mask = (torch.rand(N, generator=gen, device=device) < p_mask).to(torch.uint8)
     g = _grad_out(N, gen, device)
     return LMHeadInputs(h=h, W=W, t=t, mask=mask, T=float(w["T"]), g=g, name=name)
+
+
+def make_topk_inputs(name: str = "topk", device="cpu", N: int | None = None,
+                     V: int | None = None, K: int | None = None,
+                     seed: int | None = None) -> TopKInputs:
+    """Student logits and a synthetic teacher given by its top-K ids and
+    log-probabilities (the distillation payload of a top-k forward KL): the
+    ids are the top K of the student's logits plus unit Gaussian noise, and the
+    probabilities decay geometrically with rank, summing to the teacher's mass
+    on its top K."""
+    w = WORKLOADS[name]
+    N = w["N"] if N is None else int(N)
+    V = w["V"] if V is None else int(V)
+    K = w["K"] if K is None else int(K)
+    gen = _gen(w["seed"] if seed is None else seed, device)
+    xf = _randn((N, V), 3.0, gen, device)
+    ids = torch.empty((N, K), dtype=torch.int32, device=device)
+    for r in range(0, N, 1024):
+        blk = xf[r:r + 1024]
+        noisy = blk + torch.randn(blk.shape, generator=gen, device=device)
+        ids[r:r + 1024] = torch.topk(noisy, K, dim=1).indices.to(torch.int32)
+    x = _to_bf16_chunked(xf)
+    del xf
+    rr = 0.95
+    k = torch.arange(K, dtype=torch.float64, device=device)
+    shape = (1 - rr) * rr ** k / (1 - rr ** K)
+    mass = 0.85 + 0.14 * torch.rand(N, generator=gen, device=device, dtype=torch.float64)
+    lt = torch.log(mass[:, None] * shape[None, :]).to(torch.float32)
+    g = _grad_out(N, gen, device)
+    return TopKInputs(x=x, ids=ids, lt=lt, mask=None, T=float(w["T"]), clamp=float(w["clamp"]),
+                      g=g, name=name)
