@@ -440,6 +440,7 @@ def other_workloads(device, hbm):
         torch.cuda.empty_cache()
     out["fused_fwd_bwd"] = time_fused(device, hbm)
     out["entropy"] = time_entropy(device, hbm)
+    out["topk_kl"] = time_topk(device, hbm)
     out["lmhead"] = time_lmhead(device)
     return out
 
@@ -478,6 +479,47 @@ def time_entropy(device, hbm, steps=30, warmup=3):
     return {"workload": "c151k", "ms_per_step": ms, "tokens_per_s": N * 1000.0 / ms,
             "gbs": (fwd_b + bwd_b) / (ms * 1e-3) / 1e9,
             "frac_of_measured": (fwd_b + bwd_b) / (ms * 1e-3) / 1e9 / hbm}
+
+
+def time_topk(device, hbm, steps=20, warmup=3):
+    """Top-k forward KL on the distillation workload (N=4096, V=248320, K=128,
+    clamp -10): the forward reads the logits once (+ K gathers per row), the
+    backward reads them once and writes the gradient."""
+    import vocab_selected_token_gb300 as slp
+    from vocab_selected_token_gb300 import workloads as W
+    a = W.make_topk_inputs(device=device)
+    N, V = a.x.shape
+    K = a.ids.shape[1]
+    s = torch.cuda.current_stream(device)
+    gx = torch.empty_like(a.x)
+    res = {}
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    for i in range(warmup + steps):
+        if i == warmup:
+            ev[0].record(s)
+        kl, sm, tm, lse = slp.slp_topk_kl_forward(a.x, a.ids, a.lt, None, a.T, a.clamp)
+        if i == warmup + steps - 1:
+            ev[1].record(s)
+        slp.slp_topk_kl_backward(a.x, a.ids, a.lt, None, a.T, a.clamp, lse, a.g, grad_x=gx)
+    ev[2].record(s)
+    torch.cuda.synchronize(device)
+    # forward-only timing: a second loop
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(steps):
+        slp.slp_topk_kl_forward(a.x, a.ids, a.lt, None, a.T, a.clamp)
+    e1.record(s)
+    torch.cuda.synchronize(device)
+    step_ms = ev[0].elapsed_time(ev[2]) / steps
+    fwd_ms = e0.elapsed_time(e1) / steps
+    nb = N * V * a.x.element_size()
+    res = {"N": N, "V": V, "K": K, "ms_per_step": step_ms, "fwd_ms": fwd_ms,
+           "bwd_ms": step_ms - fwd_ms, "tokens_per_s": N * 1000.0 / step_ms,
+           "step_gbs": 3 * nb / (step_ms * 1e-3) / 1e9,
+           "frac_of_measured": 3 * nb / (step_ms * 1e-3) / 1e9 / hbm}
+    del a, gx
+    torch.cuda.empty_cache()
+    return res
 
 
 def time_fused(device, hbm, steps=30, warmup=3):
