@@ -196,8 +196,8 @@ int slp_topk_kl_forward(const void* x, int dtype, int64_t N, int64_t V, int64_t 
  * with q = softmax(x / T) recomputed from x and the saved lse (the clamp's
  * flat side contributes no gradient).  Arguments as slp_topk_kl_forward plus
  * lse (from it), grad_kl [N] float32, grad_x [N, ld_grad] in x's dtype.
- * Returns SLP_ERR_UNSUPPORTED when ceil(V/32)*4 + 8K bytes exceed 160 KB
- * (the per-row id bitmap in shared memory), i.e. V above ~1.3 million.
+ * Returns SLP_ERR_UNSUPPORTED for K above 16384 (the teacher entries are
+ * staged in shared memory).
  */
 int slp_topk_kl_backward(const void* x, int dtype, int64_t N, int64_t V, int64_t ld,
                          const int32_t* ids, const float* teacher_logp, int64_t K,

@@ -132,7 +132,7 @@ int slp_topk_kl_backward(const void* x, int dtype, int64_t N, int64_t V, int64_t
   int st = check_logits_args(x, dtype, N, V, ld, ids, T);
   if (st != SLP_OK) return st;
   if (K < 1 || K > INT32_MAX / 2 || isnan(clamp_min) || ld_grad < V) return SLP_ERR_INVALID_ARG;
-  if (static_cast<size_t>(V) > slp::topk_kl_max_vocab(K)) return SLP_ERR_UNSUPPORTED;
+  if (K > slp::topk_kl_max_k()) return SLP_ERR_UNSUPPORTED;
   if (N == 0) return SLP_OK;
   if (teacher_logp == nullptr || lse == nullptr || grad_kl == nullptr || grad_x == nullptr)
     return SLP_ERR_INVALID_ARG;

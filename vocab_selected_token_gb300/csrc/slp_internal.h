@@ -40,7 +40,7 @@ cudaError_t launch_forward_backward(const void* x, int dtype, int64_t N, int64_t
                                     cudaStream_t stream);
 
 // Top-k forward KL (slp_topk.cu).
-size_t topk_kl_max_vocab(int64_t K);
+int64_t topk_kl_max_k();
 cudaError_t launch_topk_kl_forward(const void* x, int dtype, int64_t N, int64_t V, int64_t ld,
                                    const int32_t* ids, const float* teacher_logp, int64_t K,
                                    const uint8_t* mask, float T, float clamp_min, float* kl,

@@ -12,14 +12,15 @@
 //
 // Forward: the streaming log-sum-exp kernel of the logits path (no target),
 // then one warp per row over the K teacher entries.  Backward: one CTA per
-// row streams the row once, writing the dense part g/T P q[v]; a bitmap of the
-// row's teacher ids in shared memory flags the few elements that also take a
-// -g/T p[k] term, so the sparse part costs one shared-memory word test per
-// eight elements.
+// row streams the row once through a bulk-copy ring, writing the dense part
+// g/T P q[v] everywhere; then the K elements that carry teacher entries are
+// rewritten in full (recomputed in fp32 and rounded once), so the streaming
+// pass stays a plain elementwise pass.
 
 #include "slp.h"
 #include "slp_device.cuh"
 #include "slp_internal.h"
+#include "slp_sm100.cuh"
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -29,8 +30,11 @@ namespace slp {
 namespace {
 
 constexpr int kTkThreads = 256;
-constexpr int kTkUnroll = 4;
-constexpr int kTkMaxSmem = 160 * 1024;
+constexpr int kTkStages = 4;     // bulk-copy ring of the vector path
+constexpr int kTkChunk = 16384;  // bytes per copy: 4 vectors per thread
+constexpr int kTkRing = kTkStages * kTkChunk;
+constexpr int kTkMaxSmem = 128 * 1024;  // teacher entries (8 bytes each)
+constexpr uint64_t kTkWaitNs = 2000000000ull;
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -96,7 +100,7 @@ __global__ void __launch_bounds__(kTkThreads)
                            int32_t* __restrict__ err) {
   using E = Elem<Elt>;
   constexpr int kVec = E::kVec;
-  extern __shared__ uint32_t tk_smem[];
+  extern __shared__ __align__(128) uint8_t tk_smem[];
   __shared__ float warp_p[kTkThreads / 32];
   const int64_t row = blockIdx.x;
   const Elt* xr = x + row * ld;
@@ -112,14 +116,12 @@ __global__ void __launch_bounds__(kTkThreads)
     return;
   }
 
-  const int nwords = static_cast<int>((V + 31) / 32);
-  uint32_t* bitmap = tk_smem;
-  int* sid = reinterpret_cast<int*>(bitmap + nwords);
+  // teacher entries: id, kept probability p (0 where the clamp is active)
+  uint8_t* ring = tk_smem;                                        // kTkRing bytes (vector path)
+  int* sid = reinterpret_cast<int*>(tk_smem + (kVecPath ? kTkRing : 0));
   float* sp = reinterpret_cast<float*>(sid + K);
-  for (int w = threadIdx.x; w < nwords; w += kTkThreads) bitmap[w] = 0u;
-  __syncthreads();
-
   const float L = lse[row];
+  const float L2 = L * kLog2e;
   float gT = g[row] * invT;
   float pl = 0.f;
   bool bad = false;
@@ -133,7 +135,6 @@ __global__ void __launch_bounds__(kTkThreads)
       const float ls = fmaf(E::load1(xr + id), invT, -L);
       p = ls >= clamp_min ? expf(lt[row * K + k]) : 0.f;
       sid[k] = id;
-      atomicOr(&bitmap[id >> 5], 1u << (id & 31));
     }
     sp[k] = p;
     pl += p;
@@ -149,52 +150,97 @@ __global__ void __launch_bounds__(kTkThreads)
 #pragma unroll
   for (int w = 0; w < kTkThreads / 32; ++w) P += warp_p[w];
   const float dense = gT * P;
-  const float L2 = L * kLog2e;
 
-  // teacher mass sitting on element v (kept entries; ids may repeat)
-  auto sparse = [&](int64_t v) {
-    float s = 0.f;
-    for (int k = 0; k < K; ++k)
-      if (sid[k] == v) s += sp[k];
-    return s;
-  };
-  auto marked = [&](int64_t v) { return (bitmap[v >> 5] >> (v & 31)) & 1u; };
-
+  // pass 1: the dense part g/T P q[v] for every element
   if constexpr (kVecPath) {
-    const uint4* xv = reinterpret_cast<const uint4*>(xr);
+    __shared__ __align__(8) uint64_t full[kTkStages];
+    __shared__ int abort_flag;
+    const char* src = reinterpret_cast<const char*>(xr);
+    const int64_t nbytes = nvec * 16;
+    const int64_t nch = (nbytes + kTkChunk - 1) / kTkChunk;
+    const uint32_t sbase = sm100::smem_u32(ring);
+    const uint32_t bbase = sm100::smem_u32(full);
+    if (threadIdx.x == 0) {
+      for (int st = 0; st < kTkStages; ++st) sm100::mbar_init(bbase + 8 * st, 1);
+      abort_flag = 0;
+      sm100::fence_mbar_init();
+    }
+    __syncthreads();
+    auto issue = [&](int64_t ch) {
+      const int st = static_cast<int>(ch % kTkStages);
+      const int64_t off = ch * kTkChunk;
+      const uint32_t bytes = static_cast<uint32_t>(
+          nbytes - off < kTkChunk ? nbytes - off : static_cast<int64_t>(kTkChunk));
+      sm100::mbar_arrive_expect_tx(bbase + 8 * st, bytes);
+      sm100::bulk_load(sbase + st * kTkChunk, src + off, bytes, bbase + 8 * st);
+    };
+    if (threadIdx.x == 0)
+      for (int64_t ch = 0; ch < kTkStages && ch < nch; ++ch) issue(ch);
     uint4* gv = reinterpret_cast<uint4*>(gr);
-    for (int64_t i0 = threadIdx.x; i0 < nvec; i0 += kTkThreads * kTkUnroll) {
-      uint4 buf[kTkUnroll];
+    constexpr int kPer = kTkChunk / 16 / kTkThreads;
+    int64_t ch = 0;
+    for (; ch < nch; ++ch) {
+      const int st = static_cast<int>(ch % kTkStages);
+      const bool got = sm100::mbar_wait_bounded(bbase + 8 * st, (ch / kTkStages) & 1,
+                                                &abort_flag, kTkWaitNs);
+      if (__syncthreads_or(!got)) break;
+      const int64_t off = ch * kTkChunk;
+      const int nv = static_cast<int>(
+          (nbytes - off < kTkChunk ? nbytes - off : static_cast<int64_t>(kTkChunk)) / 16);
+      const uint4* q = reinterpret_cast<const uint4*>(ring + st * kTkChunk);
+      uint4 vv[kPer];
 #pragma unroll
-      for (int u = 0; u < kTkUnroll; ++u) {
-        const int64_t i = i0 + static_cast<int64_t>(u) * kTkThreads;
-        if (i < nvec) buf[u] = ld_stream(xv + i);
+      for (int u = 0; u < kPer; ++u) {
+        const int i = u * kTkThreads + threadIdx.x;
+        if (i < nv) vv[u] = q[i];
       }
+      __syncthreads();  // stage read: refill it while this chunk is written
+      if (threadIdx.x == 0 && ch + kTkStages < nch) issue(ch + kTkStages);
 #pragma unroll
-      for (int u = 0; u < kTkUnroll; ++u) {
-        const int64_t i = i0 + static_cast<int64_t>(u) * kTkThreads;
-        if (i < nvec) {
+      for (int u = 0; u < kPer; ++u) {
+        const int i = u * kTkThreads + threadIdx.x;
+        if (i < nv) {
           float f[kVec];
-          E::unpack(buf[u], f);
+          E::unpack(vv[u], f);
 #pragma unroll
           for (int j = 0; j < kVec; ++j) f[j] = dense * ex2(fmaf(f[j], c, -L2));
-          // the kVec elements of vector i share one bitmap word
-          const int64_t e0 = i * kVec;
-          const uint32_t bits = (bitmap[e0 >> 5] >> (e0 & 31)) & ((1u << kVec) - 1u);
-          if (bits != 0u) {
-#pragma unroll
-            for (int j = 0; j < kVec; ++j)
-              if ((bits >> j) & 1u) f[j] = fmaf(-gT, sparse(e0 + j), f[j]);
-          }
-          st_stream(gv + i, E::pack(f));
+          st_stream(gv + off / 16 + i, E::pack(f));
         }
       }
     }
+    if (ch < nch) {
+      if (threadIdx.x == 0) {
+        if (err != nullptr) atomicOr(err, SLP_DEVICE_ERR_TIMEOUT);
+        const int64_t last = ch + kTkStages < nch ? ch + kTkStages : nch;
+        for (int64_t j = ch; j < last; ++j)
+          sm100::mbar_wait_bounded(bbase + 8 * (j % kTkStages), (j / kTkStages) & 1, nullptr,
+                                   kTkWaitNs);
+      }
+      __syncthreads();
+    }
   }
-  for (int64_t e = nvec * kVec + threadIdx.x; e < V; e += kTkThreads) {
-    float o = dense * ex2(fmaf(E::load1(xr + e), c, -L2));
-    if (marked(e)) o = fmaf(-gT, sparse(e), o);
-    E::store1(gr + e, o);
+  for (int64_t e = nvec * kVec + threadIdx.x; e < V; e += kTkThreads)
+    E::store1(gr + e, dense * ex2(fmaf(E::load1(xr + e), c, -L2)));
+
+  // pass 2: the elements carrying teacher entries, rewritten in full:
+  // g/T (P q[v] - sum of the kept p over every entry with that id).  The first
+  // entry of each id writes; the barrier orders it after pass 1's store.
+  __syncthreads();
+  for (int k = threadIdx.x; k < K; k += kTkThreads) {
+    const int id = sid[k];
+    if (id < 0) continue;
+    bool first = true;
+    float tot = 0.f;
+    for (int j = 0; j < K; ++j) {
+      if (sid[j] == id) {
+        if (j < k) first = false;
+        tot += sp[j];
+      }
+    }
+    if (first) {
+      const float q = ex2(fmaf(E::load1(xr + id), c, -L2));
+      E::store1(gr + id, gT * fmaf(P, q, -tot));
+    }
   }
 }
 
@@ -207,13 +253,15 @@ cudaError_t topk_bwd_typed(const Elt* x, int64_t N, int64_t V, int64_t ld, const
                            const float* lt, int K, const uint8_t* mask, float T, float clamp_min,
                            const float* lse, const float* g, Elt* gx, int64_t ldg, int32_t* err,
                            cudaStream_t stream) {
-  const int64_t smem = (V + 31) / 32 * 4 + static_cast<int64_t>(K) * 8;
-  if (smem > kTkMaxSmem || N > 0x7FFFFFFFLL) return cudaErrorNotSupported;
+  const int64_t tables = static_cast<int64_t>(K) * 8;
+  if (tables > kTkMaxSmem || N > 0x7FFFFFFFLL) return cudaErrorNotSupported;
   const float invT = 1.0f / T;
   const float c = static_cast<float>(1.4426950408889634 / static_cast<double>(T));
   const bool vec = aligned16(x, ld, sizeof(Elt)) && aligned16(gx, ldg, sizeof(Elt));
   auto k = vec ? slp_topk_kl_bwd_kernel<Elt, true> : slp_topk_kl_bwd_kernel<Elt, false>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kTkMaxSmem);
+  const int64_t smem = vec ? tables + kTkRing : tables;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kTkMaxSmem + kTkRing);
   if (e != cudaSuccess) return e;
   k<<<static_cast<unsigned>(N), kTkThreads, static_cast<size_t>(smem), stream>>>(
       x, V, ld, ids, lt, K, mask, invT, c, clamp_min, lse, g, gx, ldg, err);
@@ -222,10 +270,7 @@ cudaError_t topk_bwd_typed(const Elt* x, int64_t N, int64_t V, int64_t ld, const
 
 }  // namespace
 
-size_t topk_kl_max_vocab(int64_t K) {
-  const int64_t words = (kTkMaxSmem - K * 8) / 4;
-  return words > 0 ? static_cast<size_t>(words * 32) : 0;
-}
+int64_t topk_kl_max_k() { return kTkMaxSmem / 8; }
 
 cudaError_t launch_topk_kl_forward(const void* x, int dtype, int64_t N, int64_t V, int64_t ld,
                                    const int32_t* ids, const float* teacher_logp, int64_t K,
