@@ -171,28 +171,33 @@ __device__ __forceinline__ void write_row_result(const Lse2& a, float xt, bool t
   lse[row] = l;
 }
 
-// Log-sum-exp state with the entropy accumulator: w = sum 2^(x*c - mc) (x - m),
-// the softmax-weighted spread of the logits below the running max, kept
-// centred on m so nothing large cancels.  Then sum_v p_v x_v = m + w / s and
-// the entropy is ln(sum exp((x - m)/T)) - (w / s) / T.
+// Log-sum-exp state with the entropy accumulator, in the base-2 frame of the
+// offset mc: with u_v = x_v c - mc (the exponent already formed for ex2) and
+// s = sum 2^u, w = sum 2^u u.  Then p_v = 2^u_v / s and
+//   H = -sum p ln p = ln 2 (log2 s - w / s).
+// u is clamped at -256 (2^-256 flushes to 0), so a -inf logit adds nothing to
+// either sum without a separate test.
 struct Lse3 {
   float m, mc, s, w;
 };
 
 __device__ __forceinline__ Lse3 lse3_empty() { return Lse3{-INFINITY, -INFINITY, 0.f, 0.f}; }
 
+// Moving a state to a larger offset (by d >= 0): s' = s 2^-d, w' = (w - d s) 2^-d.
 __device__ __forceinline__ Lse3 lse3_merge(Lse3 a, Lse3 b) {
   if (b.m == -INFINITY) return a;
   if (a.m == -INFINITY) return b;
   if (b.m > a.m) {
-    const float sc = ex2(a.mc - b.mc);
-    a.w = fmaf(a.s, a.m - b.m, a.w) * sc + b.w;
-    a.s = a.s * sc + b.s;
+    const float d = b.mc - a.mc;
+    const float sc = ex2(-d);
+    a.w = fmaf(fmaf(-d, a.s, a.w), sc, b.w);
+    a.s = fmaf(a.s, sc, b.s);
     a.m = b.m;
     a.mc = b.mc;
   } else {
-    const float sc = ex2(b.mc - a.mc);
-    a.w = fmaf(fmaf(b.s, b.m - a.m, b.w), sc, a.w);
+    const float d = a.mc - b.mc;
+    const float sc = ex2(-d);
+    a.w = fmaf(fmaf(-d, b.s, b.w), sc, a.w);
     a.s = fmaf(b.s, sc, a.s);
   }
   return a;
@@ -222,8 +227,9 @@ __device__ __forceinline__ void lse3_fold(Lse3& st, const float* f, float c) {
       st.s = 0.f;
       st.w = 0.f;
     } else {
-      const float sc = ex2(st.mc - nmc);
-      st.w = fmaf(st.s, st.m - bm, st.w) * sc;
+      const float d = nmc - st.mc;
+      const float sc = ex2(-d);
+      st.w = fmaf(-d, st.s, st.w) * sc;
       st.s *= sc;
     }
     st.m = bm;
@@ -233,10 +239,10 @@ __device__ __forceinline__ void lse3_fold(Lse3& st, const float* f, float c) {
     float a[4] = {0.f, 0.f, 0.f, 0.f}, b[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int k = 0; k < K; ++k) {
-      const float e = ex2(fmaf(f[k], c, -st.mc));
+      const float u = fmaxf(fmaf(f[k], c, -st.mc), -256.f);
+      const float e = ex2(u);
       a[k & 3] += e;
-      // -inf logits contribute e = 0; keep 0 * -inf out of the sum
-      b[k & 3] = fmaf(e, f[k] == -INFINITY ? 0.f : f[k] - st.m, b[k & 3]);
+      b[k & 3] = fmaf(e, u, b[k & 3]);
     }
     st.s += (a[0] + a[1]) + (a[2] + a[3]);
     st.w += (b[0] + b[1]) + (b[2] + b[3]);
@@ -253,8 +259,7 @@ __device__ __forceinline__ void write_row_result(const Lse3& a, float xt, bool t
   if (!tvalid || !(a.s > 0.f) || a.m == -INFINITY) {
     H = __int_as_float(0x7FC00000);
   } else {
-    const float r = fmaf(a.m, c, -a.mc);
-    H = (log2f(a.s) - r) * kLn2 - (a.w / a.s) / T;
+    H = (log2f(a.s) - a.w / a.s) * kLn2;
   }
   entropy[row] = H;
 }

@@ -226,7 +226,7 @@ __global__ void __launch_bounds__(kBwdThreads)
   Elt* gr = gx + row * ldg;
   const int64_t e_tile = tile * kTileElems;
 
-  float gT = 0.f, L2 = 0.f, gHT = 0.f, offH = 0.f;
+  float gT = 0.f, L2 = 0.f, gHT = 0.f, Hl2 = 0.f;
   int64_t tt = -1;
   if (active) {
     tt = t[row];
@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(kBwdThreads)
     L2 = lse[row] * kLog2e;
     if (kEnt) {
       gHT = gH == nullptr ? 0.f : gH[row] * invT;
-      offH = H[row] - lse[row];  // log p_v + H = x_v / T + offH
+      Hl2 = H[row] * kLog2e;  // log p_v + H = ln 2 (log2 p_v + H log2 e)
     }
     if (tt < 0 || tt >= V) {
       if (err != nullptr && tile == 0 && threadIdx.x == 0) atomicOr(err, SLP_DATA_ERR_TARGET);
@@ -242,13 +242,14 @@ __global__ void __launch_bounds__(kBwdThreads)
     }
   }
   const float a = -gT;
-  // gradient element from the logit xv, its probability p and whether it is
-  // the target
-  auto grad = [&](float xv, float p, bool is_t) {
-    float o = is_t ? fmaf(a, p, gT) : a * p;
-    // p log p -> 0 as p -> 0: a -inf logit adds nothing (and no 0 * -inf)
-    if (kEnt && p > 0.f) o = fmaf(-gHT * p, fmaf(xv, invT, offH), o);
-    return o;
+  // gradient element from log2 p (the exponent l2p, clamped at -256 so a -inf
+  // logit gives p = 0 and a finite entropy factor), p and the target flag
+  auto clamp_ent = [](float u) { return kEnt ? fmaxf(u, -256.f) : u; };
+  const float gHl = -gHT * kLn2;
+  auto grad = [&](float l2p, float p, bool is_t) {
+    // p (a - gH/T ln2 (log2 p + H log2 e)), plus g/T on the target
+    const float w = kEnt ? fmaf(gHl, l2p + Hl2, a) : a;
+    return is_t ? fmaf(w, p, gT) : w * p;
   };
 
   if constexpr (kVecPath) {
@@ -282,15 +283,14 @@ __global__ void __launch_bounds__(kBwdThreads)
         const int64_t rel = tt - e;
 #pragma unroll
         for (int k = 0; k < kVec; ++k) {
-          const float p = ex2(fmaf(f[k], c, -L2));
-          f[k] = grad(f[k], p, rel == k);
+          const float l2p = clamp_ent(fmaf(f[k], c, -L2));
+          f[k] = grad(l2p, ex2(l2p), rel == k);
         }
         st_stream(gv + e / kVec, E::pack(f));
       } else {
         for (int64_t k = e; k < V; ++k) {
-          const float xv = E::load1(xr + k);
-          const float p = ex2(fmaf(xv, c, -L2));
-          E::store1(gr + k, grad(xv, p, k == tt));
+          const float l2p = clamp_ent(fmaf(E::load1(xr + k), c, -L2));
+          E::store1(gr + k, grad(l2p, ex2(l2p), k == tt));
         }
       }
     }
@@ -299,9 +299,8 @@ __global__ void __launch_bounds__(kBwdThreads)
     for (int64_t e = e_tile + threadIdx.x; e < e_end; e += kBwdThreads) {
       float out = 0.f;
       if (active) {
-        const float xv = E::load1(xr + e);
-        const float p = ex2(fmaf(xv, c, -L2));
-        out = grad(xv, p, e == tt);
+        const float l2p = clamp_ent(fmaf(E::load1(xr + e), c, -L2));
+        out = grad(l2p, ex2(l2p), e == tt);
       }
       E::store1(gr + e, out);
     }
