@@ -12,13 +12,15 @@
 //                catch the target logit; one partial per (slab, row)
 //   4. combine : merge the slab partials of each row in slab order, scatter
 //                logprob/lse to the original rows (inactive rows -> 0)
-// Backward
-//   1-2. scan + gather as above
-//   3. GEMM (recompute): same tiles; the epilogue writes
+// Backward, per vocabulary chunk of at most kVChunk columns (the survey's
+// per-V-chunk form: bounded workspace instead of a [rows, V] buffer)
+//   1-2. scan + gather as above (once)
+//   3. GEMM (recompute): the chunk's tiles; the epilogue writes
 //        dz = g/T (1[v == t] - 2^(x*c - lse*log2 e)) as bf16 (rows >= Na: 0)
 //   4. GEMM dh_part[ks] = dz[:, K-slice] W[K-slice, :]  (split-K, fp32)
-//   5. reduce  : dh[r] = bf16(sum_ks dh_part[ks][pos[r]]) (inactive rows 0)
-//   6. GEMM dW = dz^T h_c (K = compact rows), bf16 stores
+//   5. accumulate: dh_acc (+)= sum_ks dh_part[ks]   (fixed order, fp32)
+//   6. GEMM dW[chunk] = dz^T h_c (K = compact rows), bf16 stores
+//   then once: dh[r] = bf16(dh_acc[pos[r]]) (inactive rows 0)
 //
 // GEMM kernel layout (one CTA per SM, 256 threads): warp 0 issues TMA loads
 // into a 4-stage shared-memory ring (128-byte swizzle), warp 1 issues
@@ -54,6 +56,7 @@ constexpr int kSmemBytes = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barrier
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr int kSlabCap = 256;  // most vocabulary slabs per row (forward partials)
 constexpr int kKSplitCap = 24;  // most K splits of the dh GEMM
+constexpr int kVChunk = 32768;  // vocabulary columns per backward chunk
 
 enum Epi { EPI_LSE = 0, EPI_DZ = 1, EPI_F32 = 2, EPI_BF16 = 3 };
 
@@ -81,24 +84,25 @@ __host__ __device__ inline int choose_slabs(int m_tiles, int n_tiles, int G) {
   return best;
 }
 
-// K splits of the dh GEMM: balance the busiest CTA, with at least s_min
-// splits so that one K-slice of W (V/S rows x d) stays in L2 while every row
-// block reads it.
+// K splits of the dh GEMM: the fewest splits (at least s_min, so that one
+// K-slice of W stays in L2 while every row block reads it) whose busiest CTA
+// is within 3 % of the best balance.  Fewer splits mean less partial storage
+// and less partial traffic for the accumulation.
 __host__ __device__ inline int choose_ksplits(int tiles, int k_blocks, int G, int s_min) {
-  int best = 1;
-  long long best_cost = -1;
   int lo = s_min < 1 ? 1 : s_min;
   if (lo > kKSplitCap) lo = kKSplitCap;
   if (lo > k_blocks) lo = k_blocks > 0 ? k_blocks : 1;
   const int hi = k_blocks < kKSplitCap ? (k_blocks > 0 ? k_blocks : 1) : kKSplitCap;
+  long long best_cost = -1;
   for (int S = lo; S <= hi; ++S) {
     const long long cost = static_cast<long long>(cdiv(tiles * S, G)) * cdiv(k_blocks, S);
-    if (best_cost < 0 || cost < best_cost) {
-      best_cost = cost;
-      best = S;
-    }
+    if (best_cost < 0 || cost < best_cost) best_cost = cost;
   }
-  return best;
+  for (int S = lo; S <= hi; ++S) {
+    const long long cost = static_cast<long long>(cdiv(tiles * S, G)) * cdiv(k_blocks, S);
+    if (cost * 100 <= best_cost * 103) return S;
+  }
+  return lo;
 }
 
 __host__ __device__ inline int ksplit_min(int V, int d) {
@@ -107,7 +111,10 @@ __host__ __device__ inline int ksplit_min(int V, int d) {
   return static_cast<int>((bytes + (48ll << 20) - 1) / (48ll << 20));
 }
 
-__host__ __device__ inline Sched make_sched(int epi, int Na, int V, int d, int G) {
+// f32_cap: floats of split-K partial storage available to the dh GEMM; the
+// split count is clamped to it (fewer splits are still a correct schedule).
+__host__ __device__ inline Sched make_sched(int epi, int Na, int V, int d, int G,
+                                            long long f32_cap = -1) {
   Sched s{};
   if (epi == EPI_LSE || epi == EPI_DZ) {
     s.m_tiles = cdiv(Na, BM);
@@ -120,6 +127,11 @@ __host__ __device__ inline Sched make_sched(int epi, int Na, int V, int d, int G
     s.n_tiles = cdiv(d, BN);
     s.k_blocks = cdiv(V, BK);
     s.S = choose_ksplits(s.m_tiles * s.n_tiles, s.k_blocks, G, ksplit_min(V, d));
+    if (f32_cap >= 0 && s.m_tiles > 0) {
+      const long long per_split = static_cast<long long>(s.m_tiles) * BM * d;
+      const long long smax = f32_cap / per_split;
+      if (s.S > smax) s.S = smax < 1 ? 1 : static_cast<int>(smax);
+    }
     s.units = s.m_tiles * s.n_tiles * s.S;
   } else {
     s.m_tiles = cdiv(V, BM);
@@ -165,7 +177,10 @@ __device__ __forceinline__ Unit decode(const Sched& s, int epi, int u) {
 }
 
 struct Params {
-  int V, d, N, Mcap;
+  int V;                      // vocabulary columns of this launch (a backward chunk)
+  int d, N, Mcap;
+  int v0;                     // first vocabulary column of this launch
+  int Vtot;                   // whole vocabulary (valid targets are [0, Vtot))
   int G;                      // grid size the schedule was made for
   const int32_t* counters;    // [0] = Na
   const int32_t* idx;         // compact row -> original row
@@ -180,7 +195,9 @@ struct Params {
   float* part_xt;
   __nv_bfloat16* dz;          // [Mcap][ld_dz]
   long long ld_dz;
-  float* part_f32;            // [kKSplitCap][Mcap][d]
+  float* part_f32;            // [S][Mpad][d] split-K partials of dh (Mpad from Na)
+  float* dh_acc;              // [Mcap][d] fp32 dh accumulated over the chunks
+  long long pf32_cap;         // floats available at part_f32
   __nv_bfloat16* out;         // dW [V][d]
   int32_t* err;
 };
@@ -254,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *tmem_holder;
 
   const int Na = p.counters[0];
-  const Sched sc = make_sched(kEpi, Na, p.V, p.d, p.G);
+  const Sched sc = make_sched(kEpi, Na, p.V, p.d, p.G, p.pf32_cap);
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -362,11 +379,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (valid) {
           const int orig = p.idx[row];
           tr = p.t[orig];
-          if (tr < 0 || tr >= p.V) {
+          if (tr < 0 || tr >= p.Vtot) {
             tr = -1;  // invalid target: no gradient contribution, flagged elsewhere
-          } else if (kEpi == EPI_DZ) {
-            coef = p.g[orig] * p.invT;
-            L2 = p.lse[orig] * kLog2e;
+            valid = kEpi == EPI_LSE;
+          } else {
+            tr -= p.v0;  // column within this launch (may fall outside it)
+            if (kEpi == EPI_DZ) {
+              coef = p.g[orig] * p.invT;
+              L2 = p.lse[orig] * kLog2e;
+            }
           }
         }
       }
@@ -407,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int j = 0; j < 32; ++j) {
                 const float pr = ex2(fmaf(v[j], p.c, -L2));
                 o[j] = (col0 + j == tr) ? fmaf(-coef, pr, coef) : -coef * pr;
-                if (!valid || tr < 0) o[j] = 0.f;
+                if (!valid) o[j] = 0.f;
               }
               __nv_bfloat16* dst = p.dz + static_cast<long long>(row) * p.ld_dz + col0;
               if (col0 + 32 <= p.V) {
@@ -420,8 +441,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           } else if (kEpi == EPI_F32) {
             if (row < Na && col0 < p.d) {
-              float* dst = p.part_f32 +
-                           (static_cast<long long>(w.slab) * p.Mcap + row) * p.d + col0;
+              const long long mpad = static_cast<long long>(sc.m_tiles) * BM;
+              float* dst = p.part_f32 + (static_cast<long long>(w.slab) * mpad + row) * p.d + col0;
               float4* d4 = reinterpret_cast<float4*>(dst);
 #pragma unroll
               for (int j = 0; j < 8; ++j)
@@ -537,7 +558,7 @@ __global__ void __launch_bounds__(256)
   }
   const Sched sc = make_sched(EPI_LSE, p.counters[0], p.V, p.d, p.G);
   const int tt = p.t[r];
-  const bool tvalid = tt >= 0 && tt < p.V;
+  const bool tvalid = tt >= 0 && tt < p.Vtot;
   Lse2 acc = lse2_empty();
   float xt = 0.f;
   const int ttile = tvalid ? tt / BN : -1;
@@ -551,33 +572,48 @@ __global__ void __launch_bounds__(256)
   write_row_result(acc, xt, tvalid, T, p.c, logprob, lse, p.err, r);
 }
 
-// ---- dh reduction -------------------------------------------------------------
+// ---- dh accumulation over the chunks, then the final scatter ------------------
 
+// dh_acc[i] (first chunk: =, later: +=) sum over the K splits of this chunk, in
+// split order, for every compact row i < Na.
 __global__ void __launch_bounds__(256)
-    lmh_dh_reduce_kernel(const Params p, const int32_t* __restrict__ pos,
+    lmh_dh_accum_kernel(const Params p, int first) {
+  const int i = blockIdx.x;
+  const int Na = p.counters[0];
+  if (i >= Na) return;
+  const Sched sc = make_sched(EPI_F32, Na, p.V, p.d, p.G, p.pf32_cap);
+  const long long mpad = static_cast<long long>(sc.m_tiles) * BM;
+  float* acc = p.dh_acc + static_cast<long long>(i) * p.d;
+  for (int j = threadIdx.x * 4; j < p.d; j += blockDim.x * 4) {
+    float4 a = first ? make_float4(0.f, 0.f, 0.f, 0.f) : *reinterpret_cast<const float4*>(acc + j);
+    for (int s = 0; s < sc.S; ++s) {
+      const float4 v =
+          *reinterpret_cast<const float4*>(p.part_f32 + (s * mpad + i) * p.d + j);
+      a.x += v.x;
+      a.y += v.y;
+      a.z += v.z;
+      a.w += v.w;
+    }
+    *reinterpret_cast<float4*>(acc + j) = a;
+  }
+}
+
+// dh[r] = bf16(dh_acc[pos[r]]); inactive rows 0; rows with a bad target NaN.
+__global__ void __launch_bounds__(256)
+    lmh_dh_finish_kernel(const Params p, const int32_t* __restrict__ pos,
                          __nv_bfloat16* __restrict__ dh) {
   const int r = blockIdx.x;
   const int i = pos[r];
   __nv_bfloat16* out = dh + static_cast<long long>(r) * p.d;
   const int tt = p.t[r];
-  const bool bad = i >= 0 && (tt < 0 || tt >= p.V);
+  const bool bad = i >= 0 && (tt < 0 || tt >= p.Vtot);
   if (bad && threadIdx.x == 0 && p.err != nullptr) atomicOr(p.err, SLP_DATA_ERR_TARGET);
-  const Sched sc = make_sched(EPI_F32, p.counters[0], p.V, p.d, p.G);
   for (int j = threadIdx.x * 4; j < p.d; j += blockDim.x * 4) {
-    float a[4] = {0.f, 0.f, 0.f, 0.f};
-    if (i >= 0) {
-      for (int s = 0; s < sc.S; ++s) {
-        const float4 v = *reinterpret_cast<const float4*>(
-            p.part_f32 + (static_cast<long long>(s) * p.Mcap + i) * p.d + j);
-        a[0] += v.x;
-        a[1] += v.y;
-        a[2] += v.z;
-        a[3] += v.w;
-      }
-      if (bad) a[0] = a[1] = a[2] = a[3] = __int_as_float(0x7FC00000);
-    }
-    __nv_bfloat162 lo = __floats2bfloat162_rn(a[0], a[1]);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(a[2], a[3]);
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (i >= 0) a = *reinterpret_cast<const float4*>(p.dh_acc + static_cast<long long>(i) * p.d + j);
+    if (bad) a.x = a.y = a.z = a.w = __int_as_float(0x7FC00000);
+    __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(a.z, a.w);
     uint2 w;
     w.x = *reinterpret_cast<uint32_t*>(&lo);
     w.y = *reinterpret_cast<uint32_t*>(&hi);
@@ -624,15 +660,32 @@ inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255);
 
 struct Layout {
   int Mcap;
-  long long ld_dz;
+  int vchunk;          // vocabulary columns per backward chunk
+  long long ld_dz;     // row stride of the dz chunk buffer
   size_t off_counters, off_pos, off_idx, off_hc, off_pm, off_pmc, off_ps, off_pxt, fwd_end;
-  size_t off_dz, off_pf32, bwd_end;
+  size_t off_dz, off_pf32, off_acc, bwd_end;
 };
+
+// Largest split-K partial footprint S * roundup(Na,128) * d over every Na <= N
+// and both chunk widths, for the grid the kernels will use.
+size_t max_partial_floats(int Mcap, int V, int vchunk, int d, int G) {
+  size_t best = 0;
+  const int widths[2] = {vchunk < V ? vchunk : V, V % vchunk == 0 ? (vchunk < V ? vchunk : V)
+                                                                 : V % vchunk};
+  for (int w = 0; w < 2; ++w)
+    for (int mt = 1; mt * BM <= Mcap; ++mt) {
+      const Sched sc = make_sched(EPI_F32, mt * BM, widths[w], d, G);
+      const size_t f = static_cast<size_t>(sc.S) * mt * BM * d;
+      if (f > best) best = f;
+    }
+  return best;
+}
 
 Layout layout(int64_t N, int64_t V, int64_t d) {
   Layout L{};
   L.Mcap = static_cast<int>(cdiv(static_cast<int>(N), BM) * BM);
-  L.ld_dz = (V + 63) / 64 * 64;
+  L.vchunk = V < kVChunk ? static_cast<int>(V) : kVChunk;
+  L.ld_dz = (L.vchunk + 63) / 64 * 64;
   size_t o = 0;
   L.off_counters = o; o += 256;
   L.off_pos = o; o = align256(o + 4 * static_cast<size_t>(N));
@@ -644,9 +697,13 @@ Layout layout(int64_t N, int64_t V, int64_t d) {
   L.off_ps = o; o = align256(o + part);
   L.off_pxt = o; o = align256(o + part);
   L.fwd_end = o;
-  L.off_dz = o; o = align256(o + 2 * static_cast<size_t>(L.Mcap) * L.ld_dz);
-  L.off_pf32 = o; o = align256(o + 4 * static_cast<size_t>(kKSplitCap) * L.Mcap * d);
-  L.bwd_end = o;
+  L.off_dz = L.off_pm;  // the backward does not use the forward partials
+  o = align256(L.off_dz + 2 * static_cast<size_t>(L.Mcap) * L.ld_dz);
+  L.off_pf32 = o;
+  o = align256(o + 4 * max_partial_floats(L.Mcap, static_cast<int>(V), L.vchunk,
+                                         static_cast<int>(d), sm_count()));
+  L.off_acc = o; o = align256(o + 4 * static_cast<size_t>(L.Mcap) * d);
+  L.bwd_end = o > L.fwd_end ? o : L.fwd_end;
   return L;
 }
 
@@ -680,6 +737,8 @@ cudaError_t prepare(const void* h, int64_t N, int64_t V, int64_t d, const int32_
   Params& p = P.p;
   p = Params{};
   p.V = static_cast<int>(V);
+  p.Vtot = static_cast<int>(V);
+  p.v0 = 0;
   p.d = static_cast<int>(d);
   p.N = static_cast<int>(N);
   p.Mcap = P.L.Mcap;
@@ -696,6 +755,8 @@ cudaError_t prepare(const void* h, int64_t N, int64_t V, int64_t d, const int32_
   p.dz = reinterpret_cast<__nv_bfloat16*>(w + P.L.off_dz);
   p.ld_dz = P.L.ld_dz;
   p.part_f32 = reinterpret_cast<float*>(w + P.L.off_pf32);
+  p.dh_acc = reinterpret_cast<float*>(w + P.L.off_acc);
+  p.pf32_cap = static_cast<long long>((P.L.off_acc - P.L.off_pf32) / 4);
   p.err = err;
   lmh_scan_kernel<<<1, 1024, 0, stream>>>(mask, p.N, counters, P.pos, idx);
   lmh_gather_kernel<<<p.N + BM, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(h), p.N,
@@ -741,25 +802,38 @@ cudaError_t launch_lmhead_backward(const void* h, const void* W, int64_t N, int6
   if (e != cudaSuccess) return e;
   P.p.g = grad_out;
   P.p.lse = lse;
-  P.p.out = static_cast<__nv_bfloat16*>(dW);
-  CUtensorMap m_hc_k, m_w_k, m_dz_k, m_w_mn, m_dz_mn, m_hc_mn;
-  const uint64_t dz_row = static_cast<uint64_t>(P.L.ld_dz) * 2;
-  if (!make_map(&m_hc_k, P.hc, d, P.L.Mcap, d * 2, BK, BM) ||     // A of recompute
-      !make_map(&m_w_k, W, d, V, d * 2, BK, BN) ||                // B of recompute
-      !make_map(&m_dz_k, P.p.dz, V, P.L.Mcap, dz_row, BK, BM) ||  // A of dh (K = V)
-      !make_map(&m_w_mn, W, d, V, d * 2, 64, BK) ||               // B of dh (N = d)
-      !make_map(&m_dz_mn, P.p.dz, V, P.L.Mcap, dz_row, 64, BK) || // A of dW (M = V)
-      !make_map(&m_hc_mn, P.hc, d, P.L.Mcap, d * 2, 64, BK))      // B of dW (N = d)
+  CUtensorMap m_hc_k, m_hc_mn;
+  if (!make_map(&m_hc_k, P.hc, d, P.L.Mcap, d * 2, BK, BM) ||    // A of recompute
+      !make_map(&m_hc_mn, P.hc, d, P.L.Mcap, d * 2, 64, BK))     // B of dW (N = d)
     return cudaErrorInvalidValue;
-  e = launch_gemm<EPI_DZ, false, false>(m_hc_k, m_w_k, P.p, stream);
-  if (e != cudaSuccess) return e;
-  e = launch_gemm<EPI_F32, false, true>(m_dz_k, m_w_mn, P.p, stream);
-  if (e != cudaSuccess) return e;
-  lmh_dh_reduce_kernel<<<static_cast<int>(N), 256, 0, stream>>>(P.p, P.pos,
-                                                               static_cast<__nv_bfloat16*>(dh));
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  return launch_gemm<EPI_BF16, true, true>(m_dz_mn, m_hc_mn, P.p, stream);
+  const uint64_t dz_row = static_cast<uint64_t>(P.L.ld_dz) * 2;
+  const __nv_bfloat16* Wb = static_cast<const __nv_bfloat16*>(W);
+  for (int64_t v0 = 0; v0 < V; v0 += P.L.vchunk) {
+    const int64_t vc = V - v0 < P.L.vchunk ? V - v0 : P.L.vchunk;
+    Params pc = P.p;
+    pc.v0 = static_cast<int>(v0);
+    pc.V = static_cast<int>(vc);
+    pc.out = static_cast<__nv_bfloat16*>(dW) + v0 * d;
+    const __nv_bfloat16* Wc = Wb + v0 * d;
+    CUtensorMap m_w_k, m_dz_k, m_w_mn, m_dz_mn;
+    if (!make_map(&m_w_k, Wc, d, vc, d * 2, BK, BN) ||                // B of recompute
+        !make_map(&m_dz_k, pc.dz, vc, P.L.Mcap, dz_row, BK, BM) ||    // A of dh (K = chunk)
+        !make_map(&m_w_mn, Wc, d, vc, d * 2, 64, BK) ||               // B of dh (N = d)
+        !make_map(&m_dz_mn, pc.dz, vc, P.L.Mcap, dz_row, 64, BK))     // A of dW (M = chunk)
+      return cudaErrorInvalidValue;
+    e = launch_gemm<EPI_DZ, false, false>(m_hc_k, m_w_k, pc, stream);
+    if (e != cudaSuccess) return e;
+    e = launch_gemm<EPI_F32, false, true>(m_dz_k, m_w_mn, pc, stream);
+    if (e != cudaSuccess) return e;
+    lmh_dh_accum_kernel<<<P.L.Mcap, 256, 0, stream>>>(pc, v0 == 0 ? 1 : 0);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    e = launch_gemm<EPI_BF16, true, true>(m_dz_mn, m_hc_mn, pc, stream);
+    if (e != cudaSuccess) return e;
+  }
+  lmh_dh_finish_kernel<<<static_cast<int>(N), 256, 0, stream>>>(P.p, P.pos,
+                                                                static_cast<__nv_bfloat16*>(dh));
+  return cudaGetLastError();
 }
 
 }  // namespace slp
