@@ -49,8 +49,8 @@ def forward_backward_from_host(x, t, grad_out, mask=None, T: float = 1.0, *,
     if N == 0:
         return logprob, lse, grad_x
     if rows_per_chunk is None:
-        # about 128 MB of logits per chunk
-        rows_per_chunk = max(1, (128 << 20) // max(1, V * x.element_size()))
+        # about 64 MB of logits per chunk: short pipeline fill and drain
+        rows_per_chunk = max(1, (64 << 20) // max(1, V * x.element_size()))
     R = min(rows_per_chunk, N)
     nchunks = (N + R - 1) // R
     slots = max(1, min(slots, nchunks))
