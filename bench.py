@@ -108,12 +108,20 @@ def barrier(world):
 
 
 def max_over_ranks(v, world, device):
+    """The slowest rank's time (measurement only: no data-path collective)."""
     if world == 1:
         return v
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device=device)
+    on = device if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([v], dtype=torch.float64, device=on)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_tokens_per_s(tokens_per_rank, world, ms_per_step_max):
+    """Weak scaling: every rank processes its own replica of the workload, so
+    the job's throughput is all ranks' tokens over the slowest rank's time."""
+    return world * tokens_per_rank * 1000.0 / ms_per_step_max
 
 
 # ---------------------------------------------------------------- clocks
@@ -359,7 +367,7 @@ def main():
     base_mem = torch.cuda.memory_allocated(device)
     res = time_logits(inp, args.steps, args.warmup, world, device, ClockSampler(device))
     extra_mem = torch.cuda.max_memory_allocated(device) - base_mem
-    value = world * N * 1000.0 / res["ms_per_step"]
+    value = whole_job_tokens_per_s(N, world, res["ms_per_step"])
 
     kern = "slp_bwd_kernel" if res["bwd_ms"] >= res["fwd_ms"] else "slp_fwd_kernel"
     k_bytes, k_ms = (bwd_b, res["bwd_ms"]) if kern == "slp_bwd_kernel" else (fwd_b, res["fwd_ms"])

@@ -1,0 +1,64 @@
+"""CPU-only: the multi-rank path of bench.py (one replica per rank, barrier,
+max of the ranks' times, whole-job throughput) on two gloo ranks."""
+
+import os
+import socket
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import bench
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        bench.barrier(world)
+        mine = 1.5 + rank          # rank 1 is the slower one
+        slowest = bench.max_over_ranks(mine, world, torch.device("cpu"))
+        value = bench.whole_job_tokens_per_s(4096, world, slowest)
+        bench.barrier(world)
+        q.put((rank, slowest, value))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_rank_timing_uses_the_slowest_rank():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=5) for _ in range(2))
+    for rank, slowest, value in got:
+        assert slowest == 2.5
+        assert value == pytest.approx(2 * 4096 * 1000.0 / 2.5)
+
+
+def test_reference_arm_other_ranks_print_nothing(capsys):
+    sys.path.insert(0, ROOT)
+    import bench
+
+    class A:
+        config, rows, steps, warmup, gpus = "tiny", 8, 1, 0, 2
+    bench.run_reference(A, 2, 1)      # rank 1 of 2: exits without work
+    assert capsys.readouterr().out == ""
