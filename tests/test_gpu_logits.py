@@ -275,14 +275,15 @@ def test_fused_forward_backward_full_size(name):
         assert bool((gx[off].view(torch.int16) == 0).all())
 
 
-def test_fused_forward_backward_long_rows_fall_back():
-    """Rows longer than one cluster can hold (8 x 96 KB) take the separate
+@pytest.mark.parametrize("V", [400008, 420000])
+def test_fused_forward_backward_long_rows(V):
+    """Rows longer than one cluster holds (8 x 96 KB) take the separate
     kernels and still match the oracle."""
     dev = device()
-    a = W.make_logits_inputs("tiny", device=dev, N=3, V=400008)
+    a = W.make_logits_inputs("tiny", device=dev, N=5, V=V)
     lp, lse, gx = slp.slp_forward_backward(a.x, a.t, a.mask, a.T, a.g)
     torch.cuda.synchronize()
-    check_rows(a.x, a.t, a.mask, a.T, a.g, lp, lse, gx, range(3))
+    check_rows(a.x, a.t, a.mask, a.T, a.g, lp, lse, gx, range(5))
 
 
 def test_fused_forward_backward_bad_target():
