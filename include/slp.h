@@ -320,6 +320,29 @@ int slp_lmhead_forward_noalloc(const void* h, const void* W, int64_t N, int64_t 
                                const int32_t* t, const uint8_t* mask, float T,
                                float* logprob, float* lse, int32_t* err, void* stream);
 
+/*
+ * slp_lmhead_backward_accumulate - slp_lmhead_backward for gradient
+ * accumulation across micro-batches: dh is written as in slp_lmhead_backward,
+ * and this micro-batch's dW is ADDED into a float32 accumulator,
+ *
+ *   dW_accum[V, d] += dz^T h      (float32, no rounding to bf16)
+ *
+ * so a trainer can sum W's gradient over several micro-batches without a
+ * separate [V, d] buffer and add.  Same arguments and errors as
+ * slp_lmhead_backward with dW replaced by dW_accum (float32, 16-byte
+ * aligned).  Each element gets one add per call, in a fixed order, so the
+ * result is deterministic.
+ *
+ * Defined by: slp_lmhead_backward's gradient, summed over the micro-batches
+ * of one update (Megatron-LM issue #6700, "Prototype performance": several
+ * micro-batches per update).
+ */
+int slp_lmhead_backward_accumulate(const void* h, const void* W, int64_t N, int64_t V, int64_t d,
+                                   const int32_t* t, const uint8_t* mask, float T,
+                                   const float* lse, const float* grad_out, void* dh,
+                                   float* dW_accum, void* ws, size_t ws_bytes, int32_t* err,
+                                   void* stream);
+
 /* Static, human-readable text for a slp_status value. */
 const char* slp_status_string(int status);
 

@@ -150,3 +150,25 @@ def test_autograd():
     lp2, lse2, dh, dW = run_fwd_bwd(a)
     assert torch.equal(lp.detach(), lp2)
     assert torch.equal(h.grad, dh) and torch.equal(Wt.grad, dW)
+
+
+def test_backward_accumulate_into_fp32_dW():
+    """Two micro-batches accumulated into one fp32 dW equal the sum of their
+    oracle gradients; dh is the plain backward's, bit for bit."""
+    dev = device()
+    a = W.make_lmhead_inputs(device=dev, N=300, V=5000, d=256, seed=41)
+    b = W.make_lmhead_inputs(device=dev, N=200, V=5000, d=256, seed=42)
+    b.W = a.W  # same weights, two micro-batches
+    acc = torch.randn((5000, 256), device=dev) * 1e-3
+    acc0 = acc.clone()
+    refs = []
+    for m in (a, b):
+        lp, lse = slp.slp_lmhead_forward(m.h, m.W, m.t, m.mask, m.T)
+        dh = slp.slp_lmhead_backward_accumulate(m.h, m.W, m.t, m.mask, m.T, lse, m.g, acc)
+        dh_plain, _ = slp.slp_lmhead_backward(m.h, m.W, m.t, m.mask, m.T, lse, m.g)
+        torch.cuda.synchronize()
+        assert torch.equal(dh, dh_plain)
+        t, mk = m.t.cpu().numpy(), m.mask.cpu().numpy()
+        _, rlse = O.lmhead_forward(to64(m.h), to64(m.W), t, mk, m.T)
+        refs.append(O.lmhead_backward(to64(m.h), to64(m.W), t, mk, m.T, rlse, to64(m.g))[1])
+    grad_ok(to64(acc - acc0), refs[0] + refs[1], "accumulated dW")

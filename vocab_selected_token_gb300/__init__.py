@@ -29,6 +29,7 @@ __all__ = [
     "slp_topk_kl_forward", "slp_topk_kl_backward",
     "slp_lmhead_workspace_size",
     "slp_lmhead_forward_workspace_size", "slp_lmhead_forward_noalloc",
+    "slp_lmhead_backward_accumulate",
     "slp_lmhead_forward", "slp_lmhead_backward", "selected_logprob",
     "lmhead_selected_logprob", "library_path",
 ]
@@ -307,6 +308,27 @@ def slp_lmhead_backward(h, W, t, mask, T: float, lse, grad_out, dh=None, dW=None
               _ptr(lse), _ptr(grad_out), _ptr(dh), _ptr(dW), _ptr(ws), nbytes, _ptr(err),
               _stream_handle(stream))
     return dh, dW
+
+
+def slp_lmhead_backward_accumulate(h, W, t, mask, T: float, lse, grad_out, dW_accum, dh=None,
+                                   ws=None, err=None, stream=None):
+    """Fused LM-head backward that writes dh and ADDS this micro-batch's dW into
+    the float32 accumulator dW_accum [V, d].  Returns dh."""
+    N, V, d = _lmhead_check(h, W)
+    _check_vec("t", t, N, torch.int32)
+    if mask is not None:
+        _check_vec("mask", mask, N, torch.uint8)
+    _check_vec("lse", lse, N, torch.float32)
+    _check_vec("grad_out", grad_out, N, torch.float32)
+    if dW_accum.shape != (V, d) or dW_accum.dtype != torch.float32 or not dW_accum.is_contiguous():
+        raise ValueError("dW_accum must be a contiguous [V, d] float32 tensor")
+    if dh is None:
+        dh = torch.empty((N, d), dtype=torch.bfloat16, device=h.device)
+    ws, nbytes = _workspace(N, V, d, ws, h.device)
+    _lib.call("slp_lmhead_backward_accumulate", _ptr(h), _ptr(W), N, V, d, _ptr(t), _ptr(mask),
+              float(T), _ptr(lse), _ptr(grad_out), _ptr(dh), _ptr(dW_accum), _ptr(ws), nbytes,
+              _ptr(err), _stream_handle(stream))
+    return dh
 
 
 class _SelectedLogprob(torch.autograd.Function):

@@ -49,6 +49,8 @@ SIGNATURES = {
                                    _vp, _vp, _sz, _vp, _vp]),
     "slp_lmhead_forward_noalloc": (_int, [_vp, _vp, _i64, _i64, _i64, _vp, _vp, _f32, _vp, _vp,
                                           _vp, _vp]),
+    "slp_lmhead_backward_accumulate": (_int, [_vp, _vp, _i64, _i64, _i64, _vp, _vp, _f32, _vp, _vp,
+                                              _vp, _vp, _vp, _sz, _vp, _vp]),
     "slp_status_string": (ctypes.c_char_p, [_int]),
 }
 

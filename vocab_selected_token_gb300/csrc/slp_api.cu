@@ -194,6 +194,24 @@ int slp_lmhead_backward(const void* h, const void* W, int64_t N, int64_t V, int6
                                                  dW, ws, err, static_cast<cudaStream_t>(stream)));
 }
 
+int slp_lmhead_backward_accumulate(const void* h, const void* W, int64_t N, int64_t V, int64_t d,
+                                   const int32_t* t, const uint8_t* mask, float T,
+                                   const float* lse, const float* grad_out, void* dh,
+                                   float* dW_accum, void* ws, size_t ws_bytes, int32_t* err,
+                                   void* stream) {
+  int st = check_lmhead_args(h, W, N, V, d, t, T, ws, ws_bytes,
+                             slp::lmhead_workspace_size(N, V, d));
+  if (st != SLP_OK) return st;
+  if (N == 0) return SLP_OK;
+  if (lse == nullptr || grad_out == nullptr || dh == nullptr || dW_accum == nullptr)
+    return SLP_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(dh) & 15u) || (reinterpret_cast<uintptr_t>(dW_accum) & 15u))
+    return SLP_ERR_MISALIGNED;
+  return cuda_status(slp::launch_lmhead_backward(h, W, N, V, d, t, mask, T, lse, grad_out, dh,
+                                                 dW_accum, ws, err,
+                                                 static_cast<cudaStream_t>(stream), true));
+}
+
 const char* slp_status_string(int status) {
   switch (status) {
     case SLP_OK: return "ok";

@@ -64,6 +64,7 @@ cudaError_t launch_lmhead_forward(const void* h, const void* W, int64_t N, int64
 cudaError_t launch_lmhead_backward(const void* h, const void* W, int64_t N, int64_t V, int64_t d,
                                    const int32_t* t, const uint8_t* mask, float T,
                                    const float* lse, const float* grad_out, void* dh, void* dW,
-                                   void* ws, int32_t* err, cudaStream_t stream);
+                                   void* ws, int32_t* err, cudaStream_t stream,
+                                   bool accumulate_f32 = false);
 
 }  // namespace slp

@@ -58,7 +58,7 @@ constexpr int kSlabCap = 256;  // most vocabulary slabs per row (forward partial
 constexpr int kKSplitCap = 24;  // most K splits of the dh GEMM
 constexpr int kVChunk = 32768;  // vocabulary columns per backward chunk
 
-enum Epi { EPI_LSE = 0, EPI_DZ = 1, EPI_F32 = 2, EPI_BF16 = 3 };
+enum Epi { EPI_LSE = 0, EPI_DZ = 1, EPI_F32 = 2, EPI_BF16 = 3, EPI_ACC32 = 4 };
 
 __host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
 
@@ -198,7 +198,8 @@ struct Params {
   float* part_f32;            // [S][Mpad][d] split-K partials of dh (Mpad from Na)
   float* dh_acc;              // [Mcap][d] fp32 dh accumulated over the chunks
   long long pf32_cap;         // floats available at part_f32
-  __nv_bfloat16* out;         // dW [V][d]
+  __nv_bfloat16* out;         // dW [V][d] (this launch's rows)
+  float* out_acc;             // fp32 dW accumulated into (EPI_ACC32)
   int32_t* err;
 };
 
@@ -448,9 +449,22 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int j = 0; j < 8; ++j)
                 d4[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
             }
-          } else {  // EPI_BF16
+          } else if (kEpi == EPI_BF16) {
             if (row < p.V && col0 < p.d)
               store_bf16x32(p.out + static_cast<long long>(row) * p.d + col0, v);
+          } else {  // EPI_ACC32: dW += this micro-batch's gradient, in fp32
+            if (row < p.V && col0 < p.d) {
+              float4* d4 = reinterpret_cast<float4*>(p.out_acc + static_cast<long long>(row) * p.d + col0);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                float4 o = d4[j];
+                o.x += v[4 * j];
+                o.y += v[4 * j + 1];
+                o.z += v[4 * j + 2];
+                o.w += v[4 * j + 3];
+                d4[j] = o;
+              }
+            }
           }
         }
         tc_fence_before();
@@ -795,7 +809,8 @@ cudaError_t launch_lmhead_forward(const void* h, const void* W, int64_t N, int64
 cudaError_t launch_lmhead_backward(const void* h, const void* W, int64_t N, int64_t V, int64_t d,
                                    const int32_t* t, const uint8_t* mask, float T,
                                    const float* lse, const float* grad_out, void* dh, void* dW,
-                                   void* ws, int32_t* err, cudaStream_t stream) {
+                                   void* ws, int32_t* err, cudaStream_t stream,
+                                   bool accumulate_f32) {
   using namespace lmh;
   Prepared P;
   cudaError_t e = prepare(h, N, V, d, t, mask, T, ws, err, stream, &P);
@@ -813,7 +828,10 @@ cudaError_t launch_lmhead_backward(const void* h, const void* W, int64_t N, int6
     Params pc = P.p;
     pc.v0 = static_cast<int>(v0);
     pc.V = static_cast<int>(vc);
-    pc.out = static_cast<__nv_bfloat16*>(dW) + v0 * d;
+    if (accumulate_f32)
+      pc.out_acc = static_cast<float*>(dW) + v0 * d;
+    else
+      pc.out = static_cast<__nv_bfloat16*>(dW) + v0 * d;
     const __nv_bfloat16* Wc = Wb + v0 * d;
     CUtensorMap m_w_k, m_dz_k, m_w_mn, m_dz_mn;
     if (!make_map(&m_w_k, Wc, d, vc, d * 2, BK, BN) ||                // B of recompute
@@ -828,7 +846,8 @@ cudaError_t launch_lmhead_backward(const void* h, const void* W, int64_t N, int6
     lmh_dh_accum_kernel<<<P.L.Mcap, 256, 0, stream>>>(pc, v0 == 0 ? 1 : 0);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    e = launch_gemm<EPI_BF16, true, true>(m_dz_mn, m_hc_mn, pc, stream);
+    e = accumulate_f32 ? launch_gemm<EPI_ACC32, true, true>(m_dz_mn, m_hc_mn, pc, stream)
+                       : launch_gemm<EPI_BF16, true, true>(m_dz_mn, m_hc_mn, pc, stream);
     if (e != cudaSuccess) return e;
   }
   lmh_dh_finish_kernel<<<static_cast<int>(N), 256, 0, stream>>>(P.p, P.pos,
