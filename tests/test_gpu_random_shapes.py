@@ -1,0 +1,43 @@
+"""GPU: a seeded sweep of random shapes, strides, dtypes, temperatures and mask
+densities through slp_forward / slp_backward / slp_forward_backward, every row
+against the oracle (tolerances of the logits path)."""
+
+import numpy as np
+import pytest
+import torch
+
+import vocab_selected_token_gb300 as slp
+from tests.gpu_util import check_rows, device
+
+pytestmark = pytest.mark.gpu
+
+
+def _case(seed):
+    r = np.random.default_rng(1000 + seed)
+    N = int(r.integers(1, 200))
+    V = int(r.choice([1, 3, 8, 31, 256, 1000, 4096, 33333, 70001, 160000]))
+    pad = int(r.choice([0, 0, 1, 8, 13]))
+    dtype = torch.bfloat16 if r.random() < 0.7 else torch.float32
+    T = float(r.choice([1.0, 0.7, 1.9, 0.25]))
+    pm = float(r.choice([1.0, 0.5, 0.1, 0.0]))
+    std = float(r.choice([1.0, 4.0, 12.0]))
+    return N, V, pad, dtype, T, pm, std
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_shape(seed):
+    dev = device()
+    N, V, pad, dtype, T, pm, std = _case(seed)
+    g = torch.Generator(device=dev).manual_seed(seed)
+    base = (torch.randn((N, V + pad), generator=g, device=dev) * std).to(dtype)
+    x = base[:, :V]
+    t = torch.randint(0, V, (N,), generator=g, device=dev, dtype=torch.int32)
+    mask = None if pm == 1.0 else (torch.rand(N, generator=g, device=dev) < pm).to(torch.uint8)
+    grad = torch.rand(N, generator=g, device=dev) * 2 - 1
+    lp, lse = slp.slp_forward(x, t, mask, T)
+    gx = slp.slp_backward(x, t, mask, T, lse, grad)
+    lp2, lse2, gx2 = slp.slp_forward_backward(x, t, mask, T, grad)
+    torch.cuda.synchronize()
+    rows = range(N)
+    check_rows(x, t, mask, T, grad, lp, lse, gx, rows)
+    check_rows(x, t, mask, T, grad, lp2, lse2, gx2, rows)
