@@ -2,10 +2,12 @@
 densities through slp_forward / slp_backward / slp_forward_backward, every row
 against the oracle with the logits-path tolerances.
 
-The sweep goes past the workloads' range (|x/T| up to ~200).  There a
-gradient recomputed from an fp32 lse has an absolute floor of about
-|g/T| ulp(|x/T| + |lse|) (the target's 1 - p when p -> 1 above all), so cases
-with std/T > 8 add that floor (gpu_util.lse_floor) to the bound."""
+The sweep goes past the workloads' range: V down to 1, T down to 0.25 and
+|x/T| up to ~200.  A gradient recomputed from an fp32 lse has an absolute
+floor of about |g/T| ulp(|x/T| + |lse|), which shows on the target's 1 - p
+when p -> 1 (V = 1 makes it exactly 1 in exact arithmetic), so every case here
+adds that floor (gpu_util.lse_floor) to the bound.  The workload tests keep
+the plain bound."""
 
 import numpy as np
 import pytest
@@ -44,6 +46,5 @@ def test_random_shape(seed):
     lp2, lse2, gx2 = slp.slp_forward_backward(x, t, mask, T, grad)
     torch.cuda.synchronize()
     rows = range(N)
-    floor = std / T > 8
-    check_rows(x, t, mask, T, grad, lp, lse, gx, rows, fp32_floor=floor)
-    check_rows(x, t, mask, T, grad, lp2, lse2, gx2, rows, fp32_floor=floor)
+    check_rows(x, t, mask, T, grad, lp, lse, gx, rows, fp32_floor=True)
+    check_rows(x, t, mask, T, grad, lp2, lse2, gx2, rows, fp32_floor=True)
