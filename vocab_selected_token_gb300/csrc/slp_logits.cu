@@ -115,15 +115,22 @@ __global__ void __launch_bounds__(kFwdThreads)
       const int nv = static_cast<int>(
           (nbytes - off < kFwdChunk ? nbytes - off : static_cast<int64_t>(kFwdChunk)) / 16);
       const uint4* q = reinterpret_cast<const uint4*>(ring + s * kFwdChunk);
-      float f[kPer][kVec];
+      uint4 vv[kPer];
 #pragma unroll
       for (int u = 0; u < kPer; ++u) {
         const int i = u * kFwdThreads + threadIdx.x;
-        E::unpack(i < nv ? q[i] : pad, f[u]);
+        vv[u] = i < nv ? q[i] : pad;
       }
       __syncthreads();  // stage s fully read: thread 0 may refill it
       if (threadIdx.x == 0 && ch + kFwdStages < nch) issue(ch + kFwdStages);
-      st_fold<kPer * kVec>(st, &f[0][0], c);
+      if constexpr (kEnt) {
+        float f[kPer][kVec];
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) E::unpack(vv[u], f[u]);
+        st_fold<kPer * kVec>(st, &f[0][0], c);
+      } else {
+        lse2_fold_vec<kPer>(st, vv, c, static_cast<const Elt*>(nullptr));
+      }
     }
     if (ch < nch) {
       // a copy never landed: report it and wait (bounded) for the copies in
@@ -274,6 +281,27 @@ __global__ void __launch_bounds__(kBwdThreads)
       const int64_t e = e_tile + (static_cast<int64_t>(u) * kBwdThreads + threadIdx.x) * kVec;
       if (e + kVec <= V) buf[u] = ld_stream(xv + e / kVec);
     }
+    if constexpr (!kEnt) {
+      const float2 cc = make_float2(c, c);
+      const float no1 = log2f(fabsf(a)) - L2;  // -(L2 - log2 |a|)
+      const float2 no = make_float2(no1, no1);
+      const uint32_t sgn = sign_mask(a, static_cast<const Elt*>(nullptr));
+#pragma unroll
+      for (int u = 0; u < kBwdUnroll; ++u) {
+        const int64_t e = e_tile + (static_cast<int64_t>(u) * kBwdThreads + threadIdx.x) * kVec;
+        if (e + kVec <= V) {
+          st_stream(gv + e / kVec, scaled_exp2_vec(buf[u], cc, no, sgn, static_cast<const Elt*>(nullptr)));
+          if (tt >= e && tt < e + kVec)  // the target, over the value just stored (same thread)
+            E::store1(gr + tt, grad(0.f, ex2(fmaf(E::load1(xr + tt), c, -L2)), true));
+        } else {
+          for (int64_t k = e; k < V; ++k) {
+            const float l2p = fmaf(E::load1(xr + k), c, -L2);
+            E::store1(gr + k, grad(l2p, ex2(l2p), k == tt));
+          }
+        }
+      }
+      return;
+    }
 #pragma unroll
     for (int u = 0; u < kBwdUnroll; ++u) {
       const int64_t e = e_tile + (static_cast<int64_t>(u) * kBwdThreads + threadIdx.x) * kVec;
@@ -325,6 +353,9 @@ constexpr int kFbThreads = 256;
 constexpr int kFbChunk = 16384;
 constexpr int kFbMaxChunks = 6;
 constexpr int kFbMaxSeg = kFbChunk * kFbMaxChunks;  // 96 KB per CTA
+// Largest segment that keeps three CTAs resident per SM: 228 KB of shared
+// memory per SM, less 1 KB reserved and 256 B of static shared memory per CTA.
+constexpr int kFbSegTarget = 233472 / 3 - 1024 - 256;
 constexpr int kFbMaxCluster = 8;
 
 template <typename Elt>
@@ -407,13 +438,13 @@ __global__ void __launch_bounds__(kFbThreads)
       ok = false;
       break;
     }
-    float f[kPer][kVec];
+    uint4 vv[kPer];
 #pragma unroll
     for (int u = 0; u < kPer; ++u) {
       const int i = k * (kFbChunk / 16) + u * kFbThreads + threadIdx.x;
-      E::unpack(i < nv ? q[i] : pad, f[u]);
+      vv[u] = i < nv ? q[i] : pad;
     }
-    lse2_fold<kPer * kVec>(st, &f[0][0], c);
+    lse2_fold_vec<kPer>(st, vv, c, static_cast<const Elt*>(nullptr));
   }
   if (!ok && threadIdx.x == 0) {
     if (err != nullptr) atomicOr(err, SLP_DEVICE_ERR_TIMEOUT);
@@ -444,17 +475,28 @@ __global__ void __launch_bounds__(kFbThreads)
   }
   cluster_sync_all();
   __shared__ Lse2 row_state;
-  if (threadIdx.x == 0) {
+  if (warp == 0) {
+    // lane r fetches rank r's partial (the C remote reads overlap), then
+    // every lane merges them in rank order
+    Lse2 o = lse2_empty();
+    if (lane < C) {
+      const uint32_t b = map_shared_rank(&cta_part[0], lane);
+      o.m = ld_shared_cluster_f32(b);
+      o.mc = ld_shared_cluster_f32(b + 4);
+      o.s = ld_shared_cluster_f32(b + 8);
+    }
     Lse2 acc = lse2_empty();
     for (int r = 0; r < C; ++r) {
-      Lse2 o;
-      o.m = ld_shared_cluster_f32(map_shared_rank(&cta_part[0], r));
-      o.mc = ld_shared_cluster_f32(map_shared_rank(&cta_part[1], r));
-      o.s = ld_shared_cluster_f32(map_shared_rank(&cta_part[2], r));
-      acc = lse2_merge(acc, o);
+      Lse2 pr;
+      pr.m = __shfl_sync(0xFFFFFFFFu, o.m, r);
+      pr.mc = __shfl_sync(0xFFFFFFFFu, o.mc, r);
+      pr.s = __shfl_sync(0xFFFFFFFFu, o.s, r);
+      acc = lse2_merge(acc, pr);
     }
-    row_state = acc;
-    if (rank == 0) write_row_result(acc, xt, tvalid, T, c, logprob, lse, err, row);
+    if (lane == 0) {
+      row_state = acc;
+      if (rank == 0) write_row_result(acc, xt, tvalid, T, c, logprob, lse, err, row);
+    }
   }
   // no CTA may leave before the others have read its partial: arrive now,
   // wait at the end
@@ -462,21 +504,23 @@ __global__ void __launch_bounds__(kFbThreads)
   __syncthreads();
   const Lse2 rs = row_state;
 
-  // pass 2: gradient from shared memory.  p = 2^(x*c - mc) / s.
+  // pass 2: gradient from shared memory.  p = 2^(x*c - off), off = mc + log2 s;
+  // a p = sign(a) 2^(x*c - off + log2 |a|) (scaled_exp2_vec), the target's
+  // element then rewritten by the thread that stored it.
   const float off = (rs.m == -INFINITY || !(rs.s > 0.f)) ? __int_as_float(0x7FC00000)
                                                           : rs.mc + log2f(rs.s);
   const float a = -gT;
+  const float no1 = log2f(fabsf(a)) - off;
+  const float2 cc = make_float2(c, c), no = make_float2(no1, no1);
+  const uint32_t sgn = sign_mask(a, static_cast<const Elt*>(nullptr));
   const int64_t rel0 = static_cast<int64_t>(tt) - v0 * kVec;  // target offset in segment
+  const int64_t tvec = rel0 >= 0 ? rel0 / kVec : -1;
   for (int i = threadIdx.x; i < nv; i += kFbThreads) {
-    float f[kVec];
-    E::unpack(q[i], f);
-    const int64_t rel = rel0 - static_cast<int64_t>(i) * kVec;
-#pragma unroll
-    for (int k2 = 0; k2 < kVec; ++k2) {
-      const float p = ex2(fmaf(f[k2], c, -off));
-      f[k2] = (rel == k2) ? fmaf(a, p, gT) : a * p;
+    st_stream(gv + i, scaled_exp2_vec(q[i], cc, no, sgn, static_cast<const Elt*>(nullptr)));
+    if (i == tvec) {
+      const float p = ex2(fmaf(E::load1(xr + tt), c, -off));
+      E::store1(gx + row * ldg + tt, fmaf(a, p, gT));
     }
-    st_stream(gv + i, E::pack(f));
   }
   if (rank == C - 1) {
     for (int64_t e = nvec * kVec + threadIdx.x; e < V; e += kFbThreads) {
@@ -574,7 +618,10 @@ cudaError_t fwd_bwd_typed(const Elt* x, int64_t N, int64_t V, int64_t ld, const 
   if (!aligned16(x, ld, sizeof(Elt)) || !aligned16(gx, ldg, sizeof(Elt)))
     return cudaErrorNotSupported;
   const int64_t nvec = V / kVec;
-  int64_t C = (nvec * 16 + kFbMaxSeg - 1) / kFbMaxSeg;
+  // Segments of at most kFbSegTarget bytes keep three CTAs resident per SM;
+  // longer rows take up to kFbMaxSeg per CTA (two per SM).
+  int64_t C = (nvec * 16 + kFbSegTarget - 1) / kFbSegTarget;
+  if (C > kFbMaxCluster) C = (nvec * 16 + kFbMaxSeg - 1) / kFbMaxSeg;
   if (C < 1) C = 1;
   if (C > kFbMaxCluster) return cudaErrorNotSupported;
   if (N * C > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
@@ -589,13 +636,15 @@ cudaError_t fwd_bwd_typed(const Elt* x, int64_t N, int64_t V, int64_t ld, const 
   cfg.blockDim = dim3(kFbThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = static_cast<unsigned>(C);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeClusterSchedulingPolicyPreference;
+  attr[1].val.clusterSchedulingPolicyPreference = cudaClusterSchedulingPolicyLoadBalancing;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, slp_fwd_bwd_kernel<Elt>, x, V, ld, t, mask, T, c, invT, g,
                             logprob, lse, gx, ldg, err, static_cast<int>(C));
 }
@@ -643,6 +692,10 @@ cudaError_t launch_backward_entropy(const void* x, int dtype, int64_t N, int64_t
                                     const float* grad_out, const float* grad_entropy,
                                     void* grad_x, int64_t ld_grad, int32_t* err,
                                     cudaStream_t stream) {
+  // no entropy term: the plain backward, which then gives the same bits
+  if (grad_entropy == nullptr && grad_out != nullptr)
+    return launch_backward(x, dtype, N, V, ld, t, mask, T, lse, grad_out, grad_x, ld_grad, err,
+                           stream);
   if (dtype == SLP_BF16)
     return bwd_typed<__nv_bfloat16, true>(static_cast<const __nv_bfloat16*>(x), N, V, ld, t,
                                           mask, T, lse, grad_out, entropy, grad_entropy,
