@@ -150,119 +150,6 @@ __device__ __forceinline__ void lse2_fold(Lse2& st, const float* f, float c) {
   }
 }
 
-// lse2_fold over NV 16-byte vectors of raw elements, with paired arithmetic:
-// bf16x2 max on the packed words, then f32x2 fma / add (__ffma2_rn,
-// __fadd2_rn).  Every element goes through the same roundings, and the four
-// partial sums see the same terms in the same order, as lse2_fold<NV * kVec>
-// on the unpacked elements (element k feeds partial k & 3), so the two give
-// bit-identical states.
-template <int NV>
-__device__ __forceinline__ void lse2_fold_vec(Lse2& st, const uint4 (&v)[NV], float c,
-                                              const __nv_bfloat16*) {
-  __nv_bfloat162 m2 = *reinterpret_cast<const __nv_bfloat162*>(&v[0].x);
-#pragma unroll
-  for (int u = 0; u < NV; ++u) {
-    const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-    for (int j = (u == 0 ? 1 : 0); j < 4; ++j)
-      m2 = __hmax2(m2, *reinterpret_cast<const __nv_bfloat162*>(&w[j]));
-  }
-  const float bm = fmaxf(__low2float(m2), __high2float(m2));
-  if (bm > st.m) {
-    const float nmc = __fmul_rn(bm, c);
-    st.s *= ex2(st.mc - nmc);
-    st.m = bm;
-    st.mc = nmc;
-  }
-  if (st.m != -INFINITY) {
-    const float2 cc = make_float2(c, c), nm = make_float2(-st.mc, -st.mc);
-    float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int u = 0; u < NV; ++u) {
-      const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {  // word j holds elements 2j, 2j + 1
-        const float2 xf = make_float2(__uint_as_float(w[j] << 16),
-                                      __uint_as_float(w[j] & 0xFFFF0000u));
-        const float2 y = __ffma2_rn(xf, cc, nm);
-        const float2 e = make_float2(ex2(y.x), ex2(y.y));
-        if (j & 1) a23 = __fadd2_rn(a23, e);
-        else a01 = __fadd2_rn(a01, e);
-      }
-    }
-    st.s += (a01.x + a01.y) + (a23.x + a23.y);
-  }
-}
-
-template <int NV>
-__device__ __forceinline__ void lse2_fold_vec(Lse2& st, const uint4 (&v)[NV], float c, const float*) {
-  float bm = __uint_as_float(v[0].x);
-#pragma unroll
-  for (int u = 0; u < NV; ++u) {
-    bm = fmaxf(bm, __uint_as_float(v[u].x));
-    bm = fmaxf(bm, __uint_as_float(v[u].y));
-    bm = fmaxf(bm, __uint_as_float(v[u].z));
-    bm = fmaxf(bm, __uint_as_float(v[u].w));
-  }
-  if (bm > st.m) {
-    const float nmc = __fmul_rn(bm, c);
-    st.s *= ex2(st.mc - nmc);
-    st.m = bm;
-    st.mc = nmc;
-  }
-  if (st.m != -INFINITY) {
-    const float2 cc = make_float2(c, c), nm = make_float2(-st.mc, -st.mc);
-    float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int u = 0; u < NV; ++u) {
-      const float2 y0 = __ffma2_rn(make_float2(__uint_as_float(v[u].x), __uint_as_float(v[u].y)), cc, nm);
-      const float2 y1 = __ffma2_rn(make_float2(__uint_as_float(v[u].z), __uint_as_float(v[u].w)), cc, nm);
-      a01 = __fadd2_rn(a01, make_float2(ex2(y0.x), ex2(y0.y)));
-      a23 = __fadd2_rn(a23, make_float2(ex2(y1.x), ex2(y1.y)));
-    }
-    st.s += (a01.x + a01.y) + (a23.x + a23.y);
-  }
-}
-
-// The element-type argument of lse2_fold_vec, scaled_exp2_vec and sign_mask
-// is a null pointer used only to pick the overload.
-//
-// Gradient vector without the target term: every element becomes
-// a * 2^(x c - off) = sign(a) 2^(x c - off2) with off2 = off - log2 |a|, so the
-// scale costs nothing per element; the sign of a is applied to the packed
-// bits (sgn = the sign bit of a in every lane).  a = 0 gives off2 = +inf and
-// zeros; a NaN a gives NaN.
-__device__ __forceinline__ uint4 scaled_exp2_vec(const uint4& v, float2 cc, float2 no, uint32_t sgn,
-                                                 const __nv_bfloat16*) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t o[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const float2 y = __ffma2_rn(
-        make_float2(__uint_as_float(w[j] << 16), __uint_as_float(w[j] & 0xFFFF0000u)), cc, no);
-    uint32_t b;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(b) : "f"(ex2(y.y)), "f"(ex2(y.x)));
-    o[j] = b ^ sgn;
-  }
-  return make_uint4(o[0], o[1], o[2], o[3]);
-}
-
-__device__ __forceinline__ uint4 scaled_exp2_vec(const uint4& v, float2 cc, float2 no, uint32_t sgn,
-                                                 const float*) {
-  const float2 y0 = __ffma2_rn(make_float2(__uint_as_float(v.x), __uint_as_float(v.y)), cc, no);
-  const float2 y1 = __ffma2_rn(make_float2(__uint_as_float(v.z), __uint_as_float(v.w)), cc, no);
-  return make_uint4(__float_as_uint(ex2(y0.x)) ^ sgn, __float_as_uint(ex2(y0.y)) ^ sgn,
-                    __float_as_uint(ex2(y1.x)) ^ sgn, __float_as_uint(ex2(y1.y)) ^ sgn);
-}
-
-// Sign mask of a for scaled_exp2_vec, per element width.
-__device__ __forceinline__ uint32_t sign_mask(float a, const __nv_bfloat16*) {
-  return signbit(a) ? 0x80008000u : 0u;
-}
-__device__ __forceinline__ uint32_t sign_mask(float a, const float*) {
-  return signbit(a) ? 0x80000000u : 0u;
-}
-
 // Row result from the merged state.  ln sum_v exp((x_v - m)/T) is recovered
 // from the base-2 sum and the exact rounding residual of the offset.
 __device__ __forceinline__ void write_row_result(const Lse2& a, float xt, bool tvalid, float T,
@@ -375,6 +262,190 @@ __device__ __forceinline__ void write_row_result(const Lse3& a, float xt, bool t
     H = (log2f(a.s) - a.w / a.s) * kLn2;
   }
   entropy[row] = H;
+}
+
+// ---- paired (f32x2) arithmetic on raw 16-byte vectors ----------------------
+//
+// A vector holds kVec elements, read as kVec / 2 pairs (2j, 2j + 1).  The
+// folds and gradients below use the sm_100 f32x2 instructions (__ffma2_rn,
+// __fadd2_rn, __fmul2_rn) on those pairs, with exactly the roundings of the
+// scalar forms: element k of a batch still feeds partial k & 3, and the
+// pairs of even index hold partials 0 and 1, the odd ones 2 and 3.
+
+__device__ __forceinline__ float2 vec_pair(const uint4& v, int j, const __nv_bfloat16*) {
+  const uint32_t w = j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+__device__ __forceinline__ float2 vec_pair(const uint4& v, int j, const float*) {
+  return j == 0 ? make_float2(__uint_as_float(v.x), __uint_as_float(v.y))
+                : make_float2(__uint_as_float(v.z), __uint_as_float(v.w));
+}
+
+// Largest element of NV vectors (bf16: max.bf16x2 on the packed words, exact).
+template <int NV>
+__device__ __forceinline__ float vec_max(const uint4 (&v)[NV], const __nv_bfloat16*) {
+  __nv_bfloat162 m2 = *reinterpret_cast<const __nv_bfloat162*>(&v[0].x);
+#pragma unroll
+  for (int u = 0; u < NV; ++u) {
+    const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+    for (int j = (u == 0 ? 1 : 0); j < 4; ++j)
+      m2 = __hmax2(m2, *reinterpret_cast<const __nv_bfloat162*>(&w[j]));
+  }
+  return fmaxf(__low2float(m2), __high2float(m2));
+}
+template <int NV>
+__device__ __forceinline__ float vec_max(const uint4 (&v)[NV], const float*) {
+  float bm = __uint_as_float(v[0].x);
+#pragma unroll
+  for (int u = 0; u < NV; ++u) {
+    bm = fmaxf(bm, __uint_as_float(v[u].y));
+    bm = fmaxf(bm, __uint_as_float(v[u].z));
+    bm = fmaxf(bm, __uint_as_float(v[u].w));
+    if (u + 1 < NV) bm = fmaxf(bm, __uint_as_float(v[u + 1].x));
+  }
+  return bm;
+}
+
+// Pack kVec / 2 pairs back into a vector, round-to-nearest-even for bf16,
+// then XOR the sign mask.
+__device__ __forceinline__ uint4 vec_pack(const float2 (&p)[4], uint32_t sgn, const __nv_bfloat16*) {
+  uint32_t o[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o[j]) : "f"(p[j].y), "f"(p[j].x));
+    o[j] ^= sgn;
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+__device__ __forceinline__ uint4 vec_pack(const float2 (&p)[2], uint32_t sgn, const float*) {
+  return make_uint4(__float_as_uint(p[0].x) ^ sgn, __float_as_uint(p[0].y) ^ sgn,
+                    __float_as_uint(p[1].x) ^ sgn, __float_as_uint(p[1].y) ^ sgn);
+}
+
+// Sign bit of a in every lane of a vector word.
+__device__ __forceinline__ uint32_t sign_mask(float a, const __nv_bfloat16*) {
+  return signbit(a) ? 0x80008000u : 0u;
+}
+__device__ __forceinline__ uint32_t sign_mask(float a, const float*) {
+  return signbit(a) ? 0x80000000u : 0u;
+}
+
+// The pointer argument of these helpers is null; it only picks the element
+// type (Elt = __nv_bfloat16 or float).
+
+// lse2_fold over the NV vectors: bit-identical to lse2_fold<NV * kVec> on the
+// unpacked elements.
+template <int NV, typename Elt>
+__device__ __forceinline__ void lse2_fold_vec(Lse2& st, const uint4 (&v)[NV], float c,
+                                              const Elt* tag) {
+  constexpr int kPairs = Elem<Elt>::kVec / 2;
+  const float bm = vec_max<NV>(v, tag);
+  if (bm > st.m) {
+    const float nmc = __fmul_rn(bm, c);
+    st.s *= ex2(st.mc - nmc);
+    st.m = bm;
+    st.mc = nmc;
+  }
+  if (st.m != -INFINITY) {
+    const float2 cc = make_float2(c, c), nm = make_float2(-st.mc, -st.mc);
+    float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int u = 0; u < NV; ++u) {
+#pragma unroll
+      for (int j = 0; j < kPairs; ++j) {
+        const float2 y = __ffma2_rn(vec_pair(v[u], j, tag), cc, nm);
+        const float2 e = make_float2(ex2(y.x), ex2(y.y));
+        if (j & 1) a23 = __fadd2_rn(a23, e);
+        else a01 = __fadd2_rn(a01, e);
+      }
+    }
+    st.s += (a01.x + a01.y) + (a23.x + a23.y);
+  }
+}
+
+// lse3_fold over the NV vectors: bit-identical to lse3_fold<NV * kVec>.
+template <int NV, typename Elt>
+__device__ __forceinline__ void lse3_fold_vec(Lse3& st, const uint4 (&v)[NV], float c,
+                                              const Elt* tag) {
+  constexpr int kPairs = Elem<Elt>::kVec / 2;
+  const float bm = vec_max<NV>(v, tag);
+  if (bm > st.m) {
+    const float nmc = __fmul_rn(bm, c);
+    if (st.m == -INFINITY) {
+      st.s = 0.f;
+      st.w = 0.f;
+    } else {
+      const float d = nmc - st.mc;
+      const float sc = ex2(-d);
+      st.w = fmaf(-d, st.s, st.w) * sc;
+      st.s *= sc;
+    }
+    st.m = bm;
+    st.mc = nmc;
+  }
+  if (st.m != -INFINITY) {
+    const float2 cc = make_float2(c, c), nm = make_float2(-st.mc, -st.mc);
+    float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
+    float2 b01 = make_float2(0.f, 0.f), b23 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int u = 0; u < NV; ++u) {
+#pragma unroll
+      for (int j = 0; j < kPairs; ++j) {
+        float2 y = __ffma2_rn(vec_pair(v[u], j, tag), cc, nm);
+        y.x = fmaxf(y.x, -256.f);
+        y.y = fmaxf(y.y, -256.f);
+        const float2 e = make_float2(ex2(y.x), ex2(y.y));
+        if (j & 1) {
+          a23 = __fadd2_rn(a23, e);
+          b23 = __ffma2_rn(e, y, b23);
+        } else {
+          a01 = __fadd2_rn(a01, e);
+          b01 = __ffma2_rn(e, y, b01);
+        }
+      }
+    }
+    st.s += (a01.x + a01.y) + (a23.x + a23.y);
+    st.w += (b01.x + b01.y) + (b23.x + b23.y);
+  }
+}
+
+// Gradient vector without the target term: every element becomes
+// a * 2^(x c - off) = sign(a) 2^(x c - off2) with off2 = off - log2 |a|, so the
+// scale costs nothing per element; the sign of a goes onto the packed bits
+// (sgn = sign_mask(a)).  no = -off2 in both lanes.  a = 0 gives off2 = +inf
+// and zeros; a NaN a gives NaN.
+template <typename Elt>
+__device__ __forceinline__ uint4 scaled_exp2_vec(const uint4& v, float2 cc, float2 no, uint32_t sgn,
+                                                 const Elt* tag) {
+  constexpr int kPairs = Elem<Elt>::kVec / 2;
+  float2 p[kPairs];
+#pragma unroll
+  for (int j = 0; j < kPairs; ++j) {
+    const float2 y = __ffma2_rn(vec_pair(v, j, tag), cc, no);
+    p[j] = make_float2(ex2(y.x), ex2(y.y));
+  }
+  return vec_pack(p, sgn, tag);
+}
+
+// Entropy-backward vector without the target term:
+// p (a - gH/T ln 2 (log2 p + H log2 e)) = p (a2 + gHl log2 p), with
+// log2 p = x c - L2 clamped at -256, gHl = -gH/T ln 2 and a2 = a + gHl H log2 e
+// (both lanes of each float2 alike).  nL2 = -L2.
+template <typename Elt>
+__device__ __forceinline__ uint4 entropy_grad_vec(const uint4& v, float2 cc, float2 nL2, float2 gHl,
+                                                  float2 a2, const Elt* tag) {
+  constexpr int kPairs = Elem<Elt>::kVec / 2;
+  float2 p[kPairs];
+#pragma unroll
+  for (int j = 0; j < kPairs; ++j) {
+    float2 l = __ffma2_rn(vec_pair(v, j, tag), cc, nL2);
+    l.x = fmaxf(l.x, -256.f);
+    l.y = fmaxf(l.y, -256.f);
+    const float2 e = make_float2(ex2(l.x), ex2(l.y));
+    p[j] = __fmul2_rn(__ffma2_rn(gHl, l, a2), e);
+  }
+  return vec_pack(p, 0u, tag);
 }
 
 // Overloads so kernels can be written once for either state.

@@ -123,14 +123,10 @@ __global__ void __launch_bounds__(kFwdThreads)
       }
       __syncthreads();  // stage s fully read: thread 0 may refill it
       if (threadIdx.x == 0 && ch + kFwdStages < nch) issue(ch + kFwdStages);
-      if constexpr (kEnt) {
-        float f[kPer][kVec];
-#pragma unroll
-        for (int u = 0; u < kPer; ++u) E::unpack(vv[u], f[u]);
-        st_fold<kPer * kVec>(st, &f[0][0], c);
-      } else {
+      if constexpr (kEnt)
+        lse3_fold_vec<kPer>(st, vv, c, static_cast<const Elt*>(nullptr));
+      else
         lse2_fold_vec<kPer>(st, vv, c, static_cast<const Elt*>(nullptr));
-      }
     }
     if (ch < nch) {
       // a copy never landed: report it and wait (bounded) for the copies in
@@ -281,40 +277,28 @@ __global__ void __launch_bounds__(kBwdThreads)
       const int64_t e = e_tile + (static_cast<int64_t>(u) * kBwdThreads + threadIdx.x) * kVec;
       if (e + kVec <= V) buf[u] = ld_stream(xv + e / kVec);
     }
-    if constexpr (!kEnt) {
-      const float2 cc = make_float2(c, c);
-      const float no1 = log2f(fabsf(a)) - L2;  // -(L2 - log2 |a|)
-      const float2 no = make_float2(no1, no1);
-      const uint32_t sgn = sign_mask(a, static_cast<const Elt*>(nullptr));
-#pragma unroll
-      for (int u = 0; u < kBwdUnroll; ++u) {
-        const int64_t e = e_tile + (static_cast<int64_t>(u) * kBwdThreads + threadIdx.x) * kVec;
-        if (e + kVec <= V) {
-          st_stream(gv + e / kVec, scaled_exp2_vec(buf[u], cc, no, sgn, static_cast<const Elt*>(nullptr)));
-          if (tt >= e && tt < e + kVec)  // the target, over the value just stored (same thread)
-            E::store1(gr + tt, grad(0.f, ex2(fmaf(E::load1(xr + tt), c, -L2)), true));
-        } else {
-          for (int64_t k = e; k < V; ++k) {
-            const float l2p = fmaf(E::load1(xr + k), c, -L2);
-            E::store1(gr + k, grad(l2p, ex2(l2p), k == tt));
-          }
-        }
-      }
-      return;
-    }
+    // Off-target elements in paired arithmetic (scaled_exp2_vec /
+    // entropy_grad_vec); the thread whose vector holds the target stores that
+    // element again, in full, after the vector (same thread: it lands last).
+    const Elt* tag = nullptr;
+    const float2 cc = make_float2(c, c);
+    const float no1 = kEnt ? -L2 : log2f(fabsf(a)) - L2;  // -(L2 - log2 |a|) without entropy
+    const float2 no = make_float2(no1, no1);
+    const uint32_t sgn = sign_mask(a, tag);
+    const float2 gHl2 = make_float2(gHl, gHl);
+    const float a2s = fmaf(gHl, Hl2, a);
+    const float2 a2 = make_float2(a2s, a2s);
 #pragma unroll
     for (int u = 0; u < kBwdUnroll; ++u) {
       const int64_t e = e_tile + (static_cast<int64_t>(u) * kBwdThreads + threadIdx.x) * kVec;
       if (e + kVec <= V) {
-        float f[kVec];
-        E::unpack(buf[u], f);
-        const int64_t rel = tt - e;
-#pragma unroll
-        for (int k = 0; k < kVec; ++k) {
-          const float l2p = clamp_ent(fmaf(f[k], c, -L2));
-          f[k] = grad(l2p, ex2(l2p), rel == k);
+        const uint4 out = kEnt ? entropy_grad_vec(buf[u], cc, no, gHl2, a2, tag)
+                               : scaled_exp2_vec(buf[u], cc, no, sgn, tag);
+        st_stream(gv + e / kVec, out);
+        if (tt >= e && tt < e + kVec) {
+          const float l2p = clamp_ent(fmaf(E::load1(xr + tt), c, -L2));
+          E::store1(gr + tt, grad(l2p, ex2(l2p), true));
         }
-        st_stream(gv + e / kVec, E::pack(f));
       } else {
         for (int64_t k = e; k < V; ++k) {
           const float l2p = clamp_ent(fmaf(E::load1(xr + k), c, -L2));

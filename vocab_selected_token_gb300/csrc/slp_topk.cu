@@ -178,6 +178,11 @@ __global__ void __launch_bounds__(kTkThreads)
       for (int64_t ch = 0; ch < kTkStages && ch < nch; ++ch) issue(ch);
     uint4* gv = reinterpret_cast<uint4*>(gr);
     constexpr int kPer = kTkChunk / 16 / kTkThreads;
+    const Elt* tag = nullptr;
+    const float2 cc = make_float2(c, c);
+    const float no1 = log2f(fabsf(dense)) - L2;
+    const float2 no = make_float2(no1, no1);
+    const uint32_t sgn = sign_mask(dense, tag);
     int64_t ch = 0;
     for (; ch < nch; ++ch) {
       const int st = static_cast<int>(ch % kTkStages);
@@ -199,13 +204,8 @@ __global__ void __launch_bounds__(kTkThreads)
 #pragma unroll
       for (int u = 0; u < kPer; ++u) {
         const int i = u * kTkThreads + threadIdx.x;
-        if (i < nv) {
-          float f[kVec];
-          E::unpack(vv[u], f);
-#pragma unroll
-          for (int j = 0; j < kVec; ++j) f[j] = dense * ex2(fmaf(f[j], c, -L2));
-          st_stream(gv + off / 16 + i, E::pack(f));
-        }
+        if (i < nv)  // dense * 2^(x c - L2) = sign(dense) 2^(x c - L2 + log2 |dense|)
+          st_stream(gv + off / 16 + i, scaled_exp2_vec(vv[u], cc, no, sgn, tag));
       }
     }
     if (ch < nch) {
