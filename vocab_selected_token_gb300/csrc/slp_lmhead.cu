@@ -197,6 +197,7 @@ struct Params {
   long long ld_dz;
   float* part_f32;            // [S][Mpad][d] split-K partials of dh (Mpad from Na)
   float* dh_acc;              // [Mcap][d] fp32 dh accumulated over the chunks
+  int dh_fold;                // dW launches: warps 2-3 fold this chunk's dh partials into dh_acc
   long long pf32_cap;         // floats available at part_f32
   __nv_bfloat16* out;         // dW [V][d] (this launch's rows)
   float* out_acc;             // fp32 dW accumulated into (EPI_ACC32)
@@ -357,6 +358,44 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (!ok) break;
           mma_commit(bar_accf + 8 * buf);  // accumulator ready for the epilogue
+        }
+      }
+    }
+  } else if ((kEpi == EPI_BF16 || kEpi == EPI_ACC32) && warp < 4) {
+    // ------- warps 2-3 of a dW launch: dh split-K fold (tensor pipe idle) -------
+    // dh_acc[i] (first chunk: =, later: +=) sum over the K splits of the dh
+    // GEMM that ran just before, in split order, for every compact row i < Na.
+    // The dW GEMM does not touch dh_acc or the partials, so the two overlap.
+    if (p.dh_fold) {
+      const Sched sf = make_sched(EPI_F32, Na, p.V, p.d, p.G, p.pf32_cap);
+      const long long mpad = static_cast<long long>(sf.m_tiles) * BM;
+      const bool first = p.v0 == 0;
+      const int nw = static_cast<int>(gridDim.x) * 2;
+      for (int i = static_cast<int>(blockIdx.x) * 2 + (warp - 2); i < Na; i += nw) {
+        float* acc = p.dh_acc + static_cast<long long>(i) * p.d;
+        for (int j0 = lane * 4; j0 < p.d; j0 += 512) {
+          float4 a[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            a[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (j0 + 128 * k < p.d && !first)
+              a[k] = *reinterpret_cast<const float4*>(acc + j0 + 128 * k);
+          }
+          for (int sp = 0; sp < sf.S; ++sp) {
+            const float* src = p.part_f32 + (sp * mpad + i) * p.d + j0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              if (j0 + 128 * k >= p.d) continue;
+              const float4 v = *reinterpret_cast<const float4*>(src + 128 * k);
+              a[k].x += v.x;
+              a[k].y += v.y;
+              a[k].z += v.z;
+              a[k].w += v.w;
+            }
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            if (j0 + 128 * k < p.d) *reinterpret_cast<float4*>(acc + j0 + 128 * k) = a[k];
         }
       }
     }
@@ -586,31 +625,7 @@ __global__ void __launch_bounds__(256)
   write_row_result(acc, xt, tvalid, T, p.c, logprob, lse, p.err, r);
 }
 
-// ---- dh accumulation over the chunks, then the final scatter ------------------
-
-// dh_acc[i] (first chunk: =, later: +=) sum over the K splits of this chunk, in
-// split order, for every compact row i < Na.
-__global__ void __launch_bounds__(256)
-    lmh_dh_accum_kernel(const Params p, int first) {
-  const int i = blockIdx.x;
-  const int Na = p.counters[0];
-  if (i >= Na) return;
-  const Sched sc = make_sched(EPI_F32, Na, p.V, p.d, p.G, p.pf32_cap);
-  const long long mpad = static_cast<long long>(sc.m_tiles) * BM;
-  float* acc = p.dh_acc + static_cast<long long>(i) * p.d;
-  for (int j = threadIdx.x * 4; j < p.d; j += blockDim.x * 4) {
-    float4 a = first ? make_float4(0.f, 0.f, 0.f, 0.f) : *reinterpret_cast<const float4*>(acc + j);
-    for (int s = 0; s < sc.S; ++s) {
-      const float4 v =
-          *reinterpret_cast<const float4*>(p.part_f32 + (s * mpad + i) * p.d + j);
-      a.x += v.x;
-      a.y += v.y;
-      a.z += v.z;
-      a.w += v.w;
-    }
-    *reinterpret_cast<float4*>(acc + j) = a;
-  }
-}
+// ---- dh: the final scatter ---------------------------------------------------------
 
 // dh[r] = bf16(dh_acc[pos[r]]); inactive rows 0; rows with a bad target NaN.
 __global__ void __launch_bounds__(256)
@@ -843,9 +858,7 @@ cudaError_t launch_lmhead_backward(const void* h, const void* W, int64_t N, int6
     if (e != cudaSuccess) return e;
     e = launch_gemm<EPI_F32, false, true>(m_dz_k, m_w_mn, pc, stream);
     if (e != cudaSuccess) return e;
-    lmh_dh_accum_kernel<<<P.L.Mcap, 256, 0, stream>>>(pc, v0 == 0 ? 1 : 0);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    pc.dh_fold = 1;
     e = accumulate_f32 ? launch_gemm<EPI_ACC32, true, true>(m_dz_mn, m_hc_mn, pc, stream)
                        : launch_gemm<EPI_BF16, true, true>(m_dz_mn, m_hc_mn, pc, stream);
     if (e != cudaSuccess) return e;
