@@ -4,22 +4,24 @@
 // projection, compute compact rows, scatter scalars back).
 //
 // Forward
-//   1. scan    : mask -> pos[N] (compact index or -1), idx[Na], Na     (1 CTA)
+//   1. scan    : mask -> pos[N] (compact index or -1), idx[Na], Na     (1 CTA);
+//                inactive rows get logprob = lse = 0
 //   2. gather  : h_c[i] = h[idx[i]], rows Na..roundup(Na,128) zeroed
 //   3. GEMM    : persistent tcgen05 kernel, 128 x 256 tiles of h_c W^T with
 //                fp32 accumulators in TMEM; the epilogue warps keep an online
 //                (max, sum-exp) per row over a slab of vocabulary tiles and
-//                catch the target logit; one partial per (slab, row)
-//   4. combine : merge the slab partials of each row in slab order, scatter
-//                logprob/lse to the original rows (inactive rows -> 0)
+//                catch the target logit; one partial per (slab, row).  The
+//                epilogue warp that stores the last slab of its 32 rows merges
+//                their partials in slab order and writes logprob/lse to the
+//                original rows.
 // Backward, per vocabulary chunk of at most kVChunk columns (the survey's
 // per-V-chunk form: bounded workspace instead of a [rows, V] buffer)
 //   1-2. scan + gather as above (once)
 //   3. GEMM (recompute): the chunk's tiles; the epilogue writes
 //        dz = g/T (1[v == t] - 2^(x*c - lse*log2 e)) as bf16 (rows >= Na: 0)
 //   4. GEMM dh_part[ks] = dz[:, K-slice] W[K-slice, :]  (split-K, fp32)
-//   5. accumulate: dh_acc (+)= sum_ks dh_part[ks]   (fixed order, fp32)
-//   6. GEMM dW[chunk] = dz^T h_c (K = compact rows), bf16 stores
+//   5. GEMM dW[chunk] = dz^T h_c (K = compact rows), bf16 stores; its idle
+//        warps 2-3 meanwhile fold dh_acc (+)= sum_ks dh_part[ks] (fixed order)
 //   then once: dh[r] = bf16(dh_acc[pos[r]]) (inactive rows 0)
 //
 // GEMM kernel layout (one CTA per SM, 256 threads): warp 0 issues TMA loads
@@ -202,6 +204,10 @@ struct Params {
   __nv_bfloat16* out;         // dW [V][d] (this launch's rows)
   float* out_acc;             // fp32 dW accumulated into (EPI_ACC32)
   int32_t* err;
+  int32_t* row_cnt;           // [Mcap / BM][4] slab counters of the forward GEMM (zeroed by the scan)
+  float* out_lp;              // forward results [N] (original rows)
+  float* out_lse;
+  float T;
 };
 
 __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float (&v)[32]) {
@@ -510,12 +516,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_acce + 8 * buf);
       }
-      if (kEpi == EPI_LSE && ok && valid) {
-        const long long o = static_cast<long long>(w.slab) * p.Mcap + row;
-        p.part_m[o] = st.m;
-        p.part_mc[o] = st.mc;
-        p.part_s[o] = st.s;
-        p.part_xt[o] = xt;
+      if (kEpi == EPI_LSE && ok) {
+        if (valid) {
+          const long long o = static_cast<long long>(w.slab) * p.Mcap + row;
+          p.part_m[o] = st.m;
+          p.part_mc[o] = st.mc;
+          p.part_s[o] = st.s;
+          p.part_xt[o] = xt;
+        }
+        // Each epilogue warp counts its 32 rows' slabs; the warp completing
+        // the count (the last slab to store them) merges the S partials of
+        // each row in slab order and writes the row's results.
+        __threadfence();
+        __syncwarp();
+        int* cnt = p.row_cnt + w.m * 4 + q;
+        int old = 0;
+        if (lane == 0) old = atomicAdd(cnt, 1);
+        old = __shfl_sync(0xFFFFFFFFu, old, 0);
+        if (old == sc.S - 1 && row < Na) {
+          __threadfence();
+          const int orig = p.idx[row];
+          const int tt = p.t[orig];
+          const bool tvalid = tt >= 0 && tt < p.Vtot;
+          const int ttile = tvalid ? tt / BN : -1;
+          Lse2 acc = lse2_empty();
+          float xtr = 0.f;
+          for (int sl = 0; sl < sc.S; ++sl) {
+            const long long o = static_cast<long long>(sl) * p.Mcap + row;
+            acc = lse2_merge(acc, Lse2{__ldcg(p.part_m + o), __ldcg(p.part_mc + o),
+                                       __ldcg(p.part_s + o)});
+            const int n0 = static_cast<int>(static_cast<long long>(sl) * sc.n_tiles / sc.S);
+            const int n1 = static_cast<int>(static_cast<long long>(sl + 1) * sc.n_tiles / sc.S);
+            if (ttile >= n0 && ttile < n1) xtr = __ldcg(p.part_xt + o);
+          }
+          write_row_result(acc, xtr, tvalid, p.T, p.c, p.out_lp, p.out_lse, p.err, orig);
+        }
       }
     }
   }
@@ -533,7 +568,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 __global__ void __launch_bounds__(1024)
     lmh_scan_kernel(const uint8_t* __restrict__ mask, int N, int32_t* __restrict__ counters,
-                    int32_t* __restrict__ pos, int32_t* __restrict__ idx) {
+                    int32_t* __restrict__ pos, int32_t* __restrict__ idx,
+                    int32_t* __restrict__ row_cnt, int n_row_cnt, float* __restrict__ lp0,
+                    float* __restrict__ lse0) {
+  for (int j = threadIdx.x; j < n_row_cnt; j += blockDim.x) row_cnt[j] = 0;
   __shared__ int warp_sums[32];
   __shared__ int carry;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -564,6 +602,10 @@ __global__ void __launch_bounds__(1024)
     if (r < N) {
       pos[r] = f ? excl : -1;
       if (f) idx[excl] = r;
+      if (!f && lp0 != nullptr) {  // forward: inactive rows give zeros
+        lp0[r] = 0.f;
+        lse0[r] = 0.f;
+      }
     }
     __syncthreads();
     if (threadIdx.x == 0) carry += warp_sums[31];
@@ -594,35 +636,6 @@ __global__ void __launch_bounds__(256)
   uint4* dst = reinterpret_cast<uint4*>(hc + static_cast<long long>(dst_row) * d);
   for (int i = threadIdx.x; i < nv; i += blockDim.x)
     dst[i] = src ? src[i] : make_uint4(0u, 0u, 0u, 0u);
-}
-
-// ---- forward combine ------------------------------------------------------------
-
-__global__ void __launch_bounds__(256)
-    lmh_fwd_combine_kernel(const Params p, const int32_t* __restrict__ pos, float T,
-                           float* __restrict__ logprob, float* __restrict__ lse) {
-  const int r = blockIdx.x * blockDim.x + threadIdx.x;
-  if (r >= p.N) return;
-  const int i = pos[r];
-  if (i < 0) {
-    logprob[r] = 0.f;
-    lse[r] = 0.f;
-    return;
-  }
-  const Sched sc = make_sched(EPI_LSE, p.counters[0], p.V, p.d, p.G);
-  const int tt = p.t[r];
-  const bool tvalid = tt >= 0 && tt < p.Vtot;
-  Lse2 acc = lse2_empty();
-  float xt = 0.f;
-  const int ttile = tvalid ? tt / BN : -1;
-  for (int s = 0; s < sc.S; ++s) {
-    const long long o = static_cast<long long>(s) * p.Mcap + i;
-    acc = lse2_merge(acc, Lse2{p.part_m[o], p.part_mc[o], p.part_s[o]});
-    const int n0 = static_cast<int>(static_cast<long long>(s) * sc.n_tiles / sc.S);
-    const int n1 = static_cast<int>(static_cast<long long>(s + 1) * sc.n_tiles / sc.S);
-    if (ttile >= n0 && ttile < n1) xt = p.part_xt[o];
-  }
-  write_row_result(acc, xt, tvalid, T, p.c, logprob, lse, p.err, r);
 }
 
 // ---- dh: the final scatter ---------------------------------------------------------
@@ -691,7 +704,7 @@ struct Layout {
   int Mcap;
   int vchunk;          // vocabulary columns per backward chunk
   long long ld_dz;     // row stride of the dz chunk buffer
-  size_t off_counters, off_pos, off_idx, off_hc, off_pm, off_pmc, off_ps, off_pxt, fwd_end;
+  size_t off_counters, off_rcnt, off_pos, off_idx, off_hc, off_pm, off_pmc, off_ps, off_pxt, fwd_end;
   size_t off_dz, off_pf32, off_acc, bwd_end;
 };
 
@@ -717,6 +730,7 @@ Layout layout(int64_t N, int64_t V, int64_t d) {
   L.ld_dz = (L.vchunk + 63) / 64 * 64;
   size_t o = 0;
   L.off_counters = o; o += 256;
+  L.off_rcnt = o; o = align256(o + 4 * static_cast<size_t>(L.Mcap / BM) * 4);
   L.off_pos = o; o = align256(o + 4 * static_cast<size_t>(N));
   L.off_idx = o; o = align256(o + 4 * static_cast<size_t>(L.Mcap));
   L.off_hc = o; o = align256(o + 2 * static_cast<size_t>(L.Mcap) * d);
@@ -753,9 +767,11 @@ struct Prepared {
   __nv_bfloat16* hc;
 };
 
+// logprob / lse: the forward's outputs (their inactive rows are zeroed here),
+// NULL for the backward.
 cudaError_t prepare(const void* h, int64_t N, int64_t V, int64_t d, const int32_t* t,
                     const uint8_t* mask, float T, void* ws, int32_t* err, cudaStream_t stream,
-                    Prepared* out) {
+                    Prepared* out, float* logprob = nullptr, float* lse = nullptr) {
   Prepared& P = *out;
   P.L = layout(N, V, d);
   uint8_t* w = static_cast<uint8_t*>(ws);
@@ -787,7 +803,12 @@ cudaError_t prepare(const void* h, int64_t N, int64_t V, int64_t d, const int32_
   p.dh_acc = reinterpret_cast<float*>(w + P.L.off_acc);
   p.pf32_cap = static_cast<long long>((P.L.off_acc - P.L.off_pf32) / 4);
   p.err = err;
-  lmh_scan_kernel<<<1, 1024, 0, stream>>>(mask, p.N, counters, P.pos, idx);
+  p.row_cnt = reinterpret_cast<int32_t*>(w + P.L.off_rcnt);
+  p.out_lp = logprob;
+  p.out_lse = lse;
+  p.T = T;
+  lmh_scan_kernel<<<1, 1024, 0, stream>>>(mask, p.N, counters, P.pos, idx, p.row_cnt,
+                                          (P.L.Mcap / BM) * 4, logprob, lse);
   lmh_gather_kernel<<<p.N + BM, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(h), p.N,
                                                  p.d, counters, P.pos, P.hc);
   return cudaGetLastError();
@@ -808,17 +829,13 @@ cudaError_t launch_lmhead_forward(const void* h, const void* W, int64_t N, int64
                                   float* lse, void* ws, int32_t* err, cudaStream_t stream) {
   using namespace lmh;
   Prepared P;
-  cudaError_t e = prepare(h, N, V, d, t, mask, T, ws, err, stream, &P);
+  cudaError_t e = prepare(h, N, V, d, t, mask, T, ws, err, stream, &P, logprob, lse);
   if (e != cudaSuccess) return e;
   CUtensorMap ma, mb;
   if (!make_map(&ma, P.hc, d, P.L.Mcap, d * 2, BK, BM) ||
       !make_map(&mb, W, d, V, d * 2, BK, BN))
     return cudaErrorInvalidValue;
-  e = launch_gemm<EPI_LSE, false, false>(ma, mb, P.p, stream);
-  if (e != cudaSuccess) return e;
-  lmh_fwd_combine_kernel<<<cdiv(static_cast<int>(N), 256), 256, 0, stream>>>(P.p, P.pos, T,
-                                                                              logprob, lse);
-  return cudaGetLastError();
+  return launch_gemm<EPI_LSE, false, false>(ma, mb, P.p, stream);
 }
 
 cudaError_t launch_lmhead_backward(const void* h, const void* W, int64_t N, int64_t V, int64_t d,
