@@ -267,8 +267,8 @@ def e2e_logits(inp, steps, device):
     ms = (time.perf_counter() - t0) * 1000.0 / steps
     return {"value": N * 1000.0 / ms, "unit": UNIT, "ms_per_step": ms,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "api": "streaming.forward_backward_from_host (fused forward+backward, "
-                   "3 overlapping streams)"}
+            "api": "streaming.forward_backward_from_host -> slp_forward_backward_host "
+                   "(native 3-stream pipeline, ~64 MB chunks, fused forward+backward)"}
 
 
 # ---------------------------------------------------------------- oracle arm

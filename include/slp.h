@@ -25,7 +25,8 @@
  * Conventions shared by every call
  * --------------------------------
  *  - All array arguments are DEVICE pointers on the current CUDA device,
- *    allocated and owned by the caller.  The library allocates no device
+ *    allocated and owned by the caller (except the *_host buffers of
+ *    slp_forward_backward_host, which are page-locked host memory).  The library allocates no device
  *    memory, keeps no pointer after a call returns and never synchronises:
  *    every kernel is enqueued on `stream` (a cudaStream_t passed as void*;
  *    NULL = the legacy default stream), so results are ready when the stream
@@ -227,6 +228,41 @@ int slp_forward_backward(const void* x, int dtype, int64_t N, int64_t V, int64_t
                          const int32_t* t, const uint8_t* mask, float T,
                          const float* grad_out, float* logprob, float* lse,
                          void* grad_x, int64_t ld_grad, int32_t* err, void* stream);
+
+/*
+ * slp_forward_backward_host - slp_forward_backward for logits that live in
+ * pinned host memory (for example after an offload), streamed through the GPU
+ * in row chunks.  No counterpart in the pages: it only moves the rows of the
+ * call above to and from the host.
+ *
+ * Three streams overlap: chunk k+1 is copied in while chunk k is computed on
+ * `stream` and chunk k-1's results are copied out.  The copy streams are the
+ * library's own (created once per device).  They wait for `stream` at entry,
+ * and `stream` waits for the last copy before the call returns.  Work enqueued
+ * on `stream` after the call therefore sees the results in host memory,
+ * which are complete once `stream` has reached that point.  The call does
+ * not synchronise.
+ *
+ *   x_host   [N, ld] rows of dtype in page-locked host memory (cudaHostAlloc
+ *            or cudaHostRegister); t_host [N] int32, mask_host [N] uint8
+ *            (nullable), g_host [N] float32: page-locked too.
+ *   logprob_host, lse_host [N] float32 and grad_x_host [N, ld_grad] (dtype)
+ *            out, page-locked.
+ *   rows_per_chunk  rows per chunk; 0 picks about 64 MB of logits per chunk.
+ *   ws, ws_bytes  device workspace of at least
+ *            slp_forward_backward_host_workspace_size(N, V, dtype,
+ *            rows_per_chunk) bytes, 256-byte aligned.
+ *   err, stream  as for slp_backward (err is a device pointer).
+ * Returns SLP_ERR_INVALID_ARG if a host buffer is not page-locked, and
+ * SLP_ERR_WORKSPACE if ws is too small.
+ */
+size_t slp_forward_backward_host_workspace_size(int64_t N, int64_t V, int dtype,
+                                                int64_t rows_per_chunk);
+int slp_forward_backward_host(const void* x_host, int dtype, int64_t N, int64_t V, int64_t ld,
+                              const int32_t* t_host, const uint8_t* mask_host, float T,
+                              const float* g_host, float* logprob_host, float* lse_host,
+                              void* grad_x_host, int64_t ld_grad, int64_t rows_per_chunk,
+                              void* ws, size_t ws_bytes, int32_t* err, void* stream);
 
 /*
  * slp_lmhead_workspace_size - bytes of device workspace that

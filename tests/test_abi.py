@@ -122,3 +122,38 @@ def test_product_path_has_no_oracle_import():
         for f in files:
             if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
                 assert not pat.search(open(os.path.join(dirpath, f)).read()), f
+
+
+def test_host_streaming_argument_errors(lib):
+    """slp_forward_backward_host rejects bad arguments before any CUDA call."""
+    f = lib.slp_forward_backward_host
+    # (x, dtype, N, V, ld, t, mask, T, g, lp, lse, gx, ld_grad, rows_per_chunk, ws, ws_bytes, err, stream)
+    good = [FAKE, 0, 4, 16, 16, FAKE, None, 1.0, FAKE, FAKE, FAKE, FAKE, 16, 0, FAKE, 1 << 20,
+            None, None]
+    for i, bad in ((2, -1), (4, 8), (7, 0.0), (8, None), (12, 8), (1, 7), (3, 0)):
+        a = list(good)
+        a[i] = bad
+        assert f(*a) == _lib.SLP_ERR_INVALID_ARG, (i, bad)
+    a = list(good)
+    a[2] = 0
+    assert f(*a) == _lib.SLP_OK  # N = 0: nothing to do
+
+
+def test_host_streaming_workspace_size(lib):
+    ws = lib.slp_forward_backward_host_workspace_size
+    assert ws(-1, 10, 0, 0) == 0 and ws(10, 0, 0, 0) == 0 and ws(10, 10, 5, 0) == 0
+    V = 151936
+    row = V * 2
+
+    def slot(r, esize=2):  # one chunk of logits and one of gradient
+        return 2 * ((r * V * esize + 255) // 256 * 256)
+
+    def vectors(n):  # t, g, mask, logprob, lse of every row
+        return sum((n * b + 255) // 256 * 256 for b in (4, 4, 1, 4, 4))
+
+    R = (64 << 20) // row  # default plan: equal chunks of about 64 MB of logits
+    assert ws(R, V, 0, 0) == vectors(R) + slot(R)                 # one chunk: one slot
+    assert ws(2 * R, V, 0, 0) == vectors(2 * R) + 2 * slot(R)
+    assert ws(4096, V, 0, 0) == vectors(4096) + 3 * slot(R)       # three slots in the ring
+    assert ws(100, V, 0, 0) == vectors(100) + slot(100)           # fewer rows than a chunk
+    assert ws(100, V, 1, 25) == vectors(100) + 3 * slot(25, 4)   # equal chunks of 25 rows

@@ -156,6 +156,45 @@ int slp_forward_backward(const void* x, int dtype, int64_t N, int64_t V, int64_t
                                                   static_cast<cudaStream_t>(stream)));
 }
 
+size_t slp_forward_backward_host_workspace_size(int64_t N, int64_t V, int dtype,
+                                                int64_t rows_per_chunk) {
+  if (N < 0 || V <= 0 || V > INT32_MAX || (dtype != SLP_BF16 && dtype != SLP_F32)) return 0;
+  return slp::forward_backward_host_workspace_size(N, V, dtype == SLP_BF16 ? 2 : 4,
+                                                   rows_per_chunk);
+}
+
+int slp_forward_backward_host(const void* x_host, int dtype, int64_t N, int64_t V, int64_t ld,
+                              const int32_t* t_host, const uint8_t* mask_host, float T,
+                              const float* g_host, float* logprob_host, float* lse_host,
+                              void* grad_x_host, int64_t ld_grad, int64_t rows_per_chunk,
+                              void* ws, size_t ws_bytes, int32_t* err, void* stream) {
+  int st = check_logits_args(x_host, dtype, N, V, ld, t_host, T);
+  if (st != SLP_OK) return st;
+  if (ld_grad < V) return SLP_ERR_INVALID_ARG;
+  if (N == 0) return SLP_OK;
+  if (g_host == nullptr || logprob_host == nullptr || lse_host == nullptr || grad_x_host == nullptr)
+    return SLP_ERR_INVALID_ARG;
+  // every host buffer must be page-locked (asynchronous copies)
+  const void* host_ptrs[7] = {x_host, t_host, mask_host, g_host, logprob_host, lse_host,
+                              grad_x_host};
+  for (const void* hp : host_ptrs) {
+    if (hp == nullptr) continue;
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, hp) != cudaSuccess) {
+      cudaGetLastError();
+      return SLP_ERR_INVALID_ARG;
+    }
+    if (a.type != cudaMemoryTypeHost) return SLP_ERR_INVALID_ARG;
+  }
+  const size_t need = slp::forward_backward_host_workspace_size(
+      N, V, dtype == SLP_BF16 ? 2 : 4, rows_per_chunk);
+  if (ws == nullptr || ws_bytes < need) return SLP_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(ws) & 255u) return SLP_ERR_MISALIGNED;
+  return cuda_status(slp::launch_forward_backward_host(
+      x_host, dtype, N, V, ld, t_host, mask_host, T, g_host, logprob_host, lse_host, grad_x_host,
+      ld_grad, rows_per_chunk, ws, err, static_cast<cudaStream_t>(stream)));
+}
+
 size_t slp_lmhead_workspace_size(int64_t N, int64_t V, int64_t d) {
   if (N < 0 || V <= 0 || d <= 0 || V > INT32_MAX || N > INT32_MAX || d > INT32_MAX) return 0;
   return slp::lmhead_workspace_size(N, V, d);

@@ -39,6 +39,16 @@ cudaError_t launch_forward_backward(const void* x, int dtype, int64_t N, int64_t
                                     void* grad_x, int64_t ld_grad, int32_t* err,
                                     cudaStream_t stream);
 
+// Host-resident logits streamed through slp_forward_backward (slp_host.cu).
+size_t forward_backward_host_workspace_size(int64_t N, int64_t V, int esize,
+                                            int64_t rows_per_chunk);
+cudaError_t launch_forward_backward_host(const void* x_host, int dtype, int64_t N, int64_t V,
+                                         int64_t ld, const int32_t* t_host,
+                                         const uint8_t* mask_host, float T, const float* g_host,
+                                         float* lp_host, float* lse_host, void* gx_host,
+                                         int64_t ld_grad, int64_t rows_per_chunk, void* ws,
+                                         int32_t* err, cudaStream_t stream);
+
 // Top-k forward KL (slp_topk.cu).
 int64_t topk_kl_max_k();
 cudaError_t launch_topk_kl_forward(const void* x, int dtype, int64_t N, int64_t V, int64_t ld,
