@@ -322,12 +322,15 @@ __global__ void __launch_bounds__(kBwdThreads)
 
 // ---- fused forward + backward (upstream gradient known at forward time) ----
 //
-// A cluster of C CTAs holds one row in shared memory (each CTA a contiguous
-// segment of at most kFbMaxSeg bytes), loaded once with bulk copies.  The
-// log-sum-exp is folded as the chunks land and merged across the cluster
-// through distributed shared memory: every CTA merges all partials in rank
-// order, so all of them hold the same state.  Each CTA then writes its
-// segment of g/T * (1[v == t] - p) straight from shared memory.  That is one
+// A cluster of C CTAs holds one row on chip, each CTA a contiguous segment:
+// its last kFbRV vectors per thread in registers (plain 16-byte loads), the
+// rest in shared memory (bulk copies).  Holding part of the row in registers
+// lets four CTAs share an SM instead of three, so more rows are in flight
+// while each row's CTAs wait for one another.  The log-sum-exp is folded as
+// the data lands and merged across the cluster through distributed shared
+// memory: every CTA merges all partials in rank order, so all of them hold
+// the same state.  Each CTA then writes its segment of
+// g/T * (1[v == t] - p) straight from registers and shared memory.  That is one
 // HBM read of the active rows plus one write of the gradient, instead of the
 // two reads of a separate forward and backward (NeMo-RL PR #4222, "Changes":
 // recompute the softmax instead of storing it; here the row stays on chip
@@ -337,13 +340,16 @@ constexpr int kFbThreads = 256;
 constexpr int kFbChunk = 16384;
 constexpr int kFbMaxChunks = 6;
 constexpr int kFbMaxSeg = kFbChunk * kFbMaxChunks;  // 96 KB per CTA
-// Largest segment that keeps three CTAs resident per SM: 228 KB of shared
-// memory per SM, less 1 KB reserved and 256 B of static shared memory per CTA.
-constexpr int kFbSegTarget = 233472 / 3 - 1024 - 256;
+// Register part: kFbRV 16-byte vectors per thread.  With at most 64 registers
+// per thread and 233472 / 4 - 1024 - 256 bytes of shared memory, four CTAs
+// stay resident per SM (228 KB of shared memory per SM, less 1 KB reserved and
+// 256 B static per CTA); kFbRegSeg is the segment that fits.
+constexpr int kFbRV = 5;
+constexpr int kFbRegSeg = 233472 / 4 - 1024 - 256 + kFbRV * kFbThreads * 16;
 constexpr int kFbMaxCluster = 8;
 
-template <typename Elt>
-__global__ void __launch_bounds__(kFbThreads)
+template <typename Elt, int kRV>
+__global__ void __launch_bounds__(kFbThreads, kRV > 0 ? 4 : 1)
     slp_fwd_bwd_kernel(const Elt* __restrict__ x, int64_t V, int64_t ld,
                        const int32_t* __restrict__ t, const uint8_t* __restrict__ mask, float T,
                        float c, float invT, const float* __restrict__ g,
@@ -364,6 +370,11 @@ __global__ void __launch_bounds__(kFbThreads)
   const int64_t v0 = nvec * rank / C;
   const int64_t v1 = nvec * (rank + 1) / C;
   const int nv = static_cast<int>(v1 - v0);  // vectors of this segment
+  // the last kRV * kFbThreads vectors of the segment stay in registers (kRV
+  // per thread), the rest in shared memory
+  constexpr int kRegVec = kRV * kFbThreads;
+  const int nv_s = nv > kRegVec ? nv - kRegVec : 0;
+  const Elt* tag = nullptr;
   uint4* gv = reinterpret_cast<uint4*>(gx + row * ldg) + v0;
 
   // Inactive rows: every CTA of the cluster writes zeros and leaves; none of
@@ -388,7 +399,7 @@ __global__ void __launch_bounds__(kFbThreads)
   if (rank == 0 && threadIdx.x == 0 && tvalid) xt = E::load1(xr + tt);
   const float gT = tvalid ? g[row] * invT : __int_as_float(0x7FC00000);
 
-  const int seg_bytes = nv * 16;
+  const int seg_bytes = nv_s * 16;
   const int nch = (seg_bytes + kFbChunk - 1) / kFbChunk;
   const uint32_t sbase = sm100::smem_u32(seg);
   const uint32_t bbase = sm100::smem_u32(full);
@@ -409,11 +420,21 @@ __global__ void __launch_bounds__(kFbThreads)
     }
   }
 
+  const uint4 pad = make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord, E::kNegInfWord);
+  uint4 rv[kRV > 0 ? kRV : 1];  // the register part, loaded while the chunks stream in
+  if constexpr (kRV > 0) {
+    const uint4* xv = reinterpret_cast<const uint4*>(xr) + v0;
+#pragma unroll
+    for (int u = 0; u < kRV; ++u) {
+      const int i = nv_s + u * kFbThreads + threadIdx.x;
+      rv[u] = i < nv ? ld_stream(xv + i) : pad;
+    }
+  }
+
   // pass 1: online log-sum-exp over the segment as its chunks land
   Lse2 st = lse2_empty();
   const uint4* q = reinterpret_cast<const uint4*>(seg);
   constexpr int kPer = kFbChunk / 16 / kFbThreads;
-  const uint4 pad = make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord, E::kNegInfWord);
   bool ok = true;
   for (int k = 0; k < nch; ++k) {
     const bool got =
@@ -426,10 +447,11 @@ __global__ void __launch_bounds__(kFbThreads)
 #pragma unroll
     for (int u = 0; u < kPer; ++u) {
       const int i = k * (kFbChunk / 16) + u * kFbThreads + threadIdx.x;
-      vv[u] = i < nv ? q[i] : pad;
+      vv[u] = i < nv_s ? q[i] : pad;
     }
-    lse2_fold_vec<kPer>(st, vv, c, static_cast<const Elt*>(nullptr));
+    lse2_fold_vec<kPer>(st, vv, c, tag);
   }
+  if constexpr (kRV > 0) lse2_fold_vec<kRV>(st, rv, c, tag);
   if (!ok && threadIdx.x == 0) {
     if (err != nullptr) atomicOr(err, SLP_DEVICE_ERR_TIMEOUT);
     for (int k = 0; k < nch; ++k)  // let every copy land before the CTA moves on
@@ -496,14 +518,22 @@ __global__ void __launch_bounds__(kFbThreads)
   const float a = -gT;
   const float no1 = log2f(fabsf(a)) - off;
   const float2 cc = make_float2(c, c), no = make_float2(no1, no1);
-  const uint32_t sgn = sign_mask(a, static_cast<const Elt*>(nullptr));
+  const uint32_t sgn = sign_mask(a, tag);
   const int64_t rel0 = static_cast<int64_t>(tt) - v0 * kVec;  // target offset in segment
   const int64_t tvec = rel0 >= 0 ? rel0 / kVec : -1;
-  for (int i = threadIdx.x; i < nv; i += kFbThreads) {
-    st_stream(gv + i, scaled_exp2_vec(q[i], cc, no, sgn, static_cast<const Elt*>(nullptr)));
+  auto put = [&](int i, const uint4& v) {
+    st_stream(gv + i, scaled_exp2_vec(v, cc, no, sgn, tag));
     if (i == tvec) {
       const float p = ex2(fmaf(E::load1(xr + tt), c, -off));
       E::store1(gx + row * ldg + tt, fmaf(a, p, gT));
+    }
+  };
+  for (int i = threadIdx.x; i < nv_s; i += kFbThreads) put(i, q[i]);
+  if constexpr (kRV > 0) {
+#pragma unroll
+    for (int u = 0; u < kRV; ++u) {
+      const int i = nv_s + u * kFbThreads + threadIdx.x;
+      if (i < nv) put(i, rv[u]);
     }
   }
   if (rank == C - 1) {
@@ -602,16 +632,20 @@ cudaError_t fwd_bwd_typed(const Elt* x, int64_t N, int64_t V, int64_t ld, const 
   if (!aligned16(x, ld, sizeof(Elt)) || !aligned16(gx, ldg, sizeof(Elt)))
     return cudaErrorNotSupported;
   const int64_t nvec = V / kVec;
-  // Segments of at most kFbSegTarget bytes keep three CTAs resident per SM;
-  // longer rows take up to kFbMaxSeg per CTA (two per SM).
-  int64_t C = (nvec * 16 + kFbSegTarget - 1) / kFbSegTarget;
-  if (C > kFbMaxCluster) C = (nvec * 16 + kFbMaxSeg - 1) / kFbMaxSeg;
+  // Segments of at most kFbRegSeg bytes (kFbRV vectors per thread in
+  // registers, the rest in shared memory) keep four CTAs resident per SM.
+  // Longer rows take up to kFbMaxSeg of shared memory per CTA (two per SM).
+  const bool regs = (nvec * 16 + kFbRegSeg - 1) / kFbRegSeg <= kFbMaxCluster;
+  int64_t C = regs ? (nvec * 16 + kFbRegSeg - 1) / kFbRegSeg
+                   : (nvec * 16 + kFbMaxSeg - 1) / kFbMaxSeg;
   if (C < 1) C = 1;
   if (C > kFbMaxCluster) return cudaErrorNotSupported;
   if (N * C > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
-  const int smem = static_cast<int>((nvec + C - 1) / C) * 16;
-  cudaError_t e = cudaFuncSetAttribute(slp_fwd_bwd_kernel<Elt>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kFbMaxSeg);
+  const int64_t per = (nvec + C - 1) / C;  // vectors of the longest segment
+  const int64_t in_smem = regs ? (per > kFbRV * kFbThreads ? per - kFbRV * kFbThreads : 0) : per;
+  const int smem = static_cast<int>(in_smem * 16);
+  auto kern = regs ? slp_fwd_bwd_kernel<Elt, kFbRV> : slp_fwd_bwd_kernel<Elt, 0>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kFbMaxSeg);
   if (e != cudaSuccess) return e;
   const float c = static_cast<float>(1.4426950408889634 / static_cast<double>(T));
   const float invT = 1.0f / T;
@@ -629,8 +663,8 @@ cudaError_t fwd_bwd_typed(const Elt* x, int64_t N, int64_t V, int64_t ld, const 
   attr[1].val.clusterSchedulingPolicyPreference = cudaClusterSchedulingPolicyLoadBalancing;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, slp_fwd_bwd_kernel<Elt>, x, V, ld, t, mask, T, c, invT, g,
-                            logprob, lse, gx, ldg, err, static_cast<int>(C));
+  return cudaLaunchKernelEx(&cfg, kern, x, V, ld, t, mask, T, c, invT, g, logprob, lse, gx, ldg,
+                            err, static_cast<int>(C));
 }
 
 }  // namespace
