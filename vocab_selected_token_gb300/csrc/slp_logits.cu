@@ -30,9 +30,16 @@ namespace slp {
 
 constexpr int kFwdThreads = 256;
 constexpr int kFwdUnroll = 4;  // elements per thread per batch on the scalar path
-constexpr int kFwdStages = 4;  // shared-memory ring of the vector path
 constexpr int kFwdChunk = 16384;  // bytes per bulk copy (4 vectors per thread)
-constexpr int kFwdSmem = kFwdStages * kFwdChunk;
+// Shared-memory ring of the vector path, in chunks: four (64 KB, three CTAs
+// per SM) for the plain log-sum-exp; two (32 KB, six CTAs per SM) with the
+// entropy accumulator, whose fold has more arithmetic per byte and gains more
+// from extra warps than from a deeper ring (measured: 0.196 -> 0.183 ms on
+// c151k; the plain fold is the same with three or four stages).
+template <typename St>
+constexpr int fwd_stages() { return sizeof(St) == sizeof(Lse3) ? 2 : 4; }
+template <typename St>
+constexpr int fwd_smem() { return fwd_stages<St>() * kFwdChunk; }
 constexpr uint64_t kFwdWaitNs = 2000000000ull;
 constexpr int kBwdThreads = 256;
 constexpr int kBwdUnroll = 4;
@@ -50,6 +57,7 @@ __global__ void __launch_bounds__(kFwdThreads)
   constexpr int kVec = E::kVec;
   constexpr int kWarps = kFwdThreads / 32;
   constexpr bool kEnt = sizeof(St) == sizeof(Lse3);
+  constexpr int kFwdStages = fwd_stages<St>();
   __shared__ St warp_part[kWarps];
   __shared__ float cta_part[4];
 
@@ -576,11 +584,11 @@ cudaError_t fwd_typed(const Elt* x, int64_t N, int64_t V, int64_t ld, const int3
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(N * splits), 1, 1);
   cfg.blockDim = dim3(kFwdThreads, 1, 1);
-  cfg.dynamicSmemBytes = vec ? kFwdSmem : 0;
+  cfg.dynamicSmemBytes = vec ? fwd_smem<St>() : 0;
   cfg.stream = stream;
   if (vec) {
     cudaError_t e = cudaFuncSetAttribute(slp_fwd_kernel<Elt, true, St>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kFwdSmem);
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, fwd_smem<St>());
     if (e != cudaSuccess) return e;
   }
   cudaLaunchAttribute attr[1];
