@@ -37,9 +37,9 @@ constexpr int kFwdChunk = 16384;  // bytes per bulk copy (4 vectors per thread)
 // from extra warps than from a deeper ring (measured: 0.196 -> 0.183 ms on
 // c151k; the plain fold is the same with three or four stages).
 template <typename St>
-constexpr int fwd_stages() { return sizeof(St) == sizeof(Lse3) ? 2 : 4; }
+__host__ __device__ constexpr int fwd_stages() { return sizeof(St) == sizeof(Lse3) ? 2 : 4; }
 template <typename St>
-constexpr int fwd_smem() { return fwd_stages<St>() * kFwdChunk; }
+__host__ __device__ constexpr int fwd_smem() { return fwd_stages<St>() * kFwdChunk; }
 constexpr uint64_t kFwdWaitNs = 2000000000ull;
 constexpr int kBwdThreads = 256;
 constexpr int kBwdUnroll = 4;
@@ -218,8 +218,10 @@ __global__ void __launch_bounds__(kFwdThreads)
 
 // kEnt adds the entropy term -gH p_v (log p_v + H) / T (H, gH per row; g and
 // gH may then be NULL, meaning zero).
+// With the entropy term the register count would leave three or four CTAs
+// per SM; capping it for six measured 0.375 -> 0.360 ms on c151k.
 template <typename Elt, bool kVecPath, bool kEnt>
-__global__ void __launch_bounds__(kBwdThreads)
+__global__ void __launch_bounds__(kBwdThreads, kEnt ? 6 : 1)
     slp_bwd_kernel(const Elt* __restrict__ x, int64_t V, int64_t ld,
                    const int32_t* __restrict__ t, const uint8_t* __restrict__ mask, float invT,
                    float c, const float* __restrict__ lse, const float* __restrict__ g,
