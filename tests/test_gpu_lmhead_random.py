@@ -55,6 +55,8 @@ EDGES = [
     (700, 1, 64, 0.7, 1.0, 20.0),
     (1, 33000, 2560, 1.0, 1.0, 5.0),    # a single row, the workload's hidden size
     (129, 257, 64, 1.3, 1.0, 20.0),     # one row and one column past a tile
+    (70, 70001, 64, 1.0, 0.5, 5.0),     # two backward vocabulary chunks, the second ragged
+    (300, 140000, 128, 0.8, 0.9, 1.0),  # three chunks
 ]
 
 

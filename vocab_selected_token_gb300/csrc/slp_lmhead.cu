@@ -58,7 +58,7 @@ constexpr int kSmemBytes = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barrier
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr int kSlabCap = 256;  // most vocabulary slabs per row (forward partials)
 constexpr int kKSplitCap = 24;  // most K splits of the dh GEMM
-constexpr int kVChunk = 32768;  // vocabulary columns per backward chunk
+constexpr int kVChunk = 65536;  // vocabulary columns per backward chunk
 
 enum Epi { EPI_LSE = 0, EPI_DZ = 1, EPI_F32 = 2, EPI_BF16 = 3, EPI_ACC32 = 4 };
 
