@@ -273,7 +273,9 @@ int slp_forward_backward_host(const void* x_host, int dtype, int64_t N, int64_t 
  * alone needs (compacted hidden rows and per-slab log-sum-exp partials).
  *
  * The backward workspace holds the compacted rows, a bf16 dz buffer of
- * roundup(N,128) x roundup(V,64) elements and float32 split-K partials of dh.
+ * roundup(N,128) x min(V, 65536) elements (the backward runs in vocabulary
+ * chunks of at most 65536 columns), float32 split-K partials of dh and a
+ * float32 dh accumulator.
  */
 size_t slp_lmhead_workspace_size(int64_t N, int64_t V, int64_t d);
 size_t slp_lmhead_forward_workspace_size(int64_t N, int64_t V, int64_t d);
