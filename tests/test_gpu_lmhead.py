@@ -172,3 +172,30 @@ def test_backward_accumulate_into_fp32_dW():
         _, rlse = O.lmhead_forward(to64(m.h), to64(m.W), t, mk, m.T)
         refs.append(O.lmhead_backward(to64(m.h), to64(m.W), t, mk, m.T, rlse, to64(m.g))[1])
     grad_ok(to64(acc - acc0), refs[0] + refs[1], "accumulated dW")
+
+
+def test_lmhead_matches_logits_path():
+    """Fused against unfused: the LM head's logprob and lse equal those of
+    slp_forward on the materialised fp32 logits h W^T, and its gradients equal
+    the logits path's fp32 gradient pushed through the projection."""
+    dev = device()
+    a = W.make_lmhead_inputs(device=dev, N=500, V=9000, d=320, p_mask=0.7, seed=43)
+    a.W = (a.W.float() * 8).to(torch.bfloat16)  # logits of a few units
+    lp, lse = slp.slp_lmhead_forward(a.h, a.W, a.t, a.mask, a.T)
+    dh, dW = slp.slp_lmhead_backward(a.h, a.W, a.t, a.mask, a.T, lse, a.g)
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    try:
+        x = a.h.float() @ a.W.float().t()  # fp32 logits, no TF32
+        lp2, lse2 = slp.slp_forward(x, a.t, a.mask, a.T)
+        gx = slp.slp_backward(x, a.t, a.mask, a.T, lse2, a.g)
+        dh2 = gx @ a.W.float()
+        dW2 = gx.t() @ a.h.float()
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+    torch.cuda.synchronize()
+    assert float((lp - lp2).abs().max()) <= 1e-4 and float((lse - lse2).abs().max()) <= 1e-4
+    for got, ref, what in ((dh.float(), dh2, "dh"), (dW.float(), dW2, "dW")):
+        cos = float((got * ref).sum() / (got.norm() * ref.norm()))
+        frob = float((got - ref).norm() / ref.norm())
+        assert cos >= 0.9999 and frob <= 1e-2, f"{what}: cosine {cos:.6f} frob {frob:.3e}"
