@@ -489,7 +489,7 @@ __global__ void __launch_bounds__(kFbThreads, kRV > 0 ? 4 : 1)
       cta_part[2] = v.s;
     }
   }
-  cluster_sync_all();
+  cluster_sync_from_thread0();  // thread 0 wrote cta_part
   __shared__ Lse2 row_state;
   if (warp == 0) {
     // lane r fetches rank r's partial (the C remote reads overlap), then
@@ -514,9 +514,9 @@ __global__ void __launch_bounds__(kFbThreads, kRV > 0 ? 4 : 1)
       if (rank == 0) write_row_result(acc, xt, tvalid, T, c, logprob, lse, err, row);
     }
   }
-  // no CTA may leave before the others have read its partial: arrive now,
-  // wait at the end
-  asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+  // no CTA may leave before the others have read its partial: arrive now
+  // (relaxed: the reads above have returned their values), wait at the end
+  asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
   __syncthreads();
   const Lse2 rs = row_state;
 
