@@ -33,7 +33,10 @@
  *    reaches that point.  The calls contain no host-device synchronisation and
  *    no allocation, so they may be captured in a CUDA graph.
  *  - Matrices are row-major.  `ld` is the row stride in elements (ld >= V).
- *  - Outputs are overwritten, never accumulated into.
+ *  - Outputs are overwritten, never accumulated into (except the fp32 dW of
+ *    slp_lmhead_backward_accumulate), and must not overlap any input: in
+ *    particular grad_x may not share memory with x (the target's element
+ *    is recomputed from x after the row's gradient has been stored).
  *  - `mask` is optional (NULL = every row active).  mask[n] == 0 makes row n
  *    inactive: its logprob and lse are +0.0 and its gradient row is +0.0,
  *    bit for bit (Megatron-LM issue #6700, "Prototype correctness": masked
