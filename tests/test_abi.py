@@ -157,3 +157,18 @@ def test_host_streaming_workspace_size(lib):
     assert ws(4096, V, 0, 0) == vectors(4096) + 3 * slot(R)       # three slots in the ring
     assert ws(100, V, 0, 0) == vectors(100) + slot(100)           # fewer rows than a chunk
     assert ws(100, V, 1, 25) == vectors(100) + 3 * slot(25, 4)   # equal chunks of 25 rows
+
+
+def test_binding_refuses_overlapping_outputs():
+    """The binding rejects an output that shares memory with an input before
+    anything reaches the library (slp.h: outputs must not overlap inputs)."""
+    import torch
+
+    import vocab_selected_token_gb300 as slp
+    x = torch.zeros(4, 8)
+    with pytest.raises(ValueError):
+        slp._check_disjoint("grad_x", x, x)
+    with pytest.raises(ValueError):
+        slp._check_disjoint("grad_x", x[1:], x)
+    slp._check_disjoint("grad_x", torch.zeros(4, 8), x)
+    slp._check_disjoint("dW", torch.zeros(3, 2), None, torch.zeros(5))

@@ -52,3 +52,4 @@ def test_lmhead_small():
     assert a.h.shape == (64, 128) and a.W.shape == (300, 128)
     assert a.h.dtype == torch.bfloat16 and a.W.dtype == torch.bfloat16
     assert a.mask.dtype == torch.uint8
+

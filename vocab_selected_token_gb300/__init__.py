@@ -57,6 +57,26 @@ def _check_vec(name, v, N, dtype):
     return v
 
 
+def _span(t):
+    """[first, last) byte address range a strided tensor touches."""
+    if t.numel() == 0:
+        return (t.data_ptr(), t.data_ptr())
+    last = sum((n - 1) * st for n, st in zip(t.shape, t.stride()))
+    return (t.data_ptr(), t.data_ptr() + (last + 1) * t.element_size())
+
+
+def _check_disjoint(out_name, out, *inputs):
+    """Outputs may not share memory with inputs (slp.h).  Compares address
+    ranges, so it also refuses interleaved views of one buffer."""
+    a = _span(out)
+    for v in inputs:
+        if v is None:
+            continue
+        b = _span(v)
+        if a[0] < b[1] and b[0] < a[1]:
+            raise ValueError(f"{out_name} must not overlap the inputs")
+
+
 def _logits_layout(x):
     if x.dim() != 2 or x.dtype not in _DTYPES:
         raise ValueError("x must be a 2-D bfloat16 or float32 tensor")
@@ -99,6 +119,7 @@ def slp_backward(x, t, mask, T: float, lse, grad_out, grad_x=None, err=None, str
     if grad_x.shape != (N, V) or grad_x.dtype != x.dtype or (N > 0 and V > 0 and grad_x.stride(1) != 1):
         raise ValueError("grad_x must be [N, V] with x's dtype and unit column stride")
     ldg = grad_x.stride(0) if N > 1 else max(V, 1)
+    _check_disjoint("grad_x", grad_x, x)
     _lib.call("slp_backward", _ptr(x), _DTYPES[x.dtype], N, V, ld, _ptr(t), _ptr(mask), float(T),
               _ptr(lse), _ptr(grad_out), _ptr(grad_x), ldg, _ptr(err), _stream_handle(stream))
     return grad_x
@@ -136,6 +157,7 @@ def slp_backward_entropy(x, t, mask, T: float, lse, entropy, grad_out=None, grad
     if grad_x is None:
         grad_x = torch.empty((N, V), dtype=x.dtype, device=x.device)
     ldg = grad_x.stride(0) if N > 1 else max(V, 1)
+    _check_disjoint("grad_x", grad_x, x)
     _lib.call("slp_backward_entropy", _ptr(x), _DTYPES[x.dtype], N, V, ld, _ptr(t), _ptr(mask),
               float(T), _ptr(lse), _ptr(entropy), _ptr(grad_out), _ptr(grad_entropy),
               _ptr(grad_x), ldg, _ptr(err), _stream_handle(stream))
@@ -201,6 +223,7 @@ def slp_topk_kl_backward(x, ids, teacher_logp, mask, T: float, clamp_min: float,
     if grad_x is None:
         grad_x = torch.empty((N, V), dtype=x.dtype, device=x.device)
     ldg = grad_x.stride(0) if N > 1 else max(V, 1)
+    _check_disjoint("grad_x", grad_x, x)
     _lib.call("slp_topk_kl_backward", _ptr(x), _DTYPES[x.dtype], N, V, ld, _ptr(ids),
               _ptr(teacher_logp), K, _ptr(mask), float(T), float(clamp_min), _ptr(lse),
               _ptr(grad_kl), _ptr(grad_x), ldg, _ptr(err), _stream_handle(stream))
@@ -227,6 +250,7 @@ def slp_forward_backward(x, t, mask, T: float, grad_out, logprob=None, lse=None,
     if grad_x.shape != (N, V) or grad_x.dtype != x.dtype or (N > 0 and V > 0 and grad_x.stride(1) != 1):
         raise ValueError("grad_x must be [N, V] with x's dtype and unit column stride")
     ldg = grad_x.stride(0) if N > 1 else max(V, 1)
+    _check_disjoint("grad_x", grad_x, x)
     _lib.call("slp_forward_backward", _ptr(x), _DTYPES[x.dtype], N, V, ld, _ptr(t), _ptr(mask),
               float(T), _ptr(grad_out), _ptr(logprob), _ptr(lse), _ptr(grad_x), ldg, _ptr(err),
               _stream_handle(stream))
@@ -304,6 +328,8 @@ def slp_lmhead_backward(h, W, t, mask, T: float, lse, grad_out, dh=None, dW=None
     if dW is None:
         dW = torch.empty((V, d), dtype=torch.bfloat16, device=h.device)
     ws, nbytes = _workspace(N, V, d, ws, h.device)
+    _check_disjoint("dh", dh, h, W)
+    _check_disjoint("dW", dW, h, W)
     _lib.call("slp_lmhead_backward", _ptr(h), _ptr(W), N, V, d, _ptr(t), _ptr(mask), float(T),
               _ptr(lse), _ptr(grad_out), _ptr(dh), _ptr(dW), _ptr(ws), nbytes, _ptr(err),
               _stream_handle(stream))
