@@ -571,16 +571,26 @@ __global__ void __launch_bounds__(1024)
                     int32_t* __restrict__ pos, int32_t* __restrict__ idx,
                     int32_t* __restrict__ row_cnt, int n_row_cnt, float* __restrict__ lp0,
                     float* __restrict__ lse0) {
-  for (int j = threadIdx.x; j < n_row_cnt; j += blockDim.x) row_cnt[j] = 0;
+  // One CTA; each thread takes kRows consecutive rows per pass, so a pass
+  // covers 8192 rows with one block-wide scan of the per-thread counts.
+  constexpr int kRows = 8;
   __shared__ int warp_sums[32];
   __shared__ int carry;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int j = threadIdx.x; j < n_row_cnt; j += blockDim.x) row_cnt[j] = 0;
   if (threadIdx.x == 0) carry = 0;
   __syncthreads();
-  for (int base = 0; base < N; base += 1024) {
-    const int r = base + threadIdx.x;
-    const int f = (r < N) && (mask == nullptr || mask[r] != 0) ? 1 : 0;
-    int v = f;
+  for (int base = 0; base < N; base += 1024 * kRows) {
+    const int r0 = base + threadIdx.x * kRows;
+    int f[kRows];
+    int cnt = 0;
+#pragma unroll
+    for (int e = 0; e < kRows; ++e) {
+      const int r = r0 + e;
+      f[e] = (r < N) && (mask == nullptr || mask[r] != 0) ? 1 : 0;
+      cnt += f[e];
+    }
+    int v = cnt;  // inclusive scan of the counts across the warp
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xFFFFFFFFu, v, o);
@@ -598,13 +608,21 @@ __global__ void __launch_bounds__(1024)
       warp_sums[lane] = w;
     }
     __syncthreads();
-    const int excl = carry + (warp > 0 ? warp_sums[warp - 1] : 0) + v - f;
-    if (r < N) {
-      pos[r] = f ? excl : -1;
-      if (f) idx[excl] = r;
-      if (!f && lp0 != nullptr) {  // forward: inactive rows give zeros
-        lp0[r] = 0.f;
-        lse0[r] = 0.f;
+    int excl = carry + (warp > 0 ? warp_sums[warp - 1] : 0) + v - cnt;
+#pragma unroll
+    for (int e = 0; e < kRows; ++e) {
+      const int r = r0 + e;
+      if (r >= N) break;
+      if (f[e]) {
+        pos[r] = excl;
+        idx[excl] = r;
+        ++excl;
+      } else {
+        pos[r] = -1;
+        if (lp0 != nullptr) {  // forward: inactive rows give zeros
+          lp0[r] = 0.f;
+          lse0[r] = 0.f;
+        }
       }
     }
     __syncthreads();
@@ -614,28 +632,41 @@ __global__ void __launch_bounds__(1024)
   if (threadIdx.x == 0) counters[0] = carry;
 }
 
-// CTA b < N copies active row b of h to its compact slot; CTA N + j zeroes
-// compact row Na + j when it lies below roundup(Na, BM).
-__global__ void __launch_bounds__(256)
+// Warp w of the grid copies active row w of h to its compact slot; warps
+// N .. N+BM-1 zero compact rows Na .. roundup(Na, BM)-1.
+constexpr int kGatherWarps = 8;
+__global__ void __launch_bounds__(32 * kGatherWarps)
     lmh_gather_kernel(const __nv_bfloat16* __restrict__ h, int N, int d,
                       const int32_t* __restrict__ counters, const int32_t* __restrict__ pos,
                       __nv_bfloat16* __restrict__ hc) {
-  const int b = blockIdx.x;
+  const int w = static_cast<int>(blockIdx.x) * kGatherWarps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
   const int nv = d / 8;  // 16-byte vectors per row
   int dst_row;
   const uint4* src = nullptr;
-  if (b < N) {
-    dst_row = pos[b];
+  if (w < N) {
+    dst_row = pos[w];
     if (dst_row < 0) return;
-    src = reinterpret_cast<const uint4*>(h + static_cast<long long>(b) * d);
-  } else {
+    src = reinterpret_cast<const uint4*>(h + static_cast<long long>(w) * d);
+  } else if (w < N + BM) {
     const int Na = counters[0];
-    dst_row = Na + (b - N);
+    dst_row = Na + (w - N);
     if (dst_row >= cdiv(Na, BM) * BM) return;
+  } else {
+    return;
   }
   uint4* dst = reinterpret_cast<uint4*>(hc + static_cast<long long>(dst_row) * d);
-  for (int i = threadIdx.x; i < nv; i += blockDim.x)
-    dst[i] = src ? src[i] : make_uint4(0u, 0u, 0u, 0u);
+  for (int i0 = lane; i0 < nv; i0 += 32 * 4) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + 32 * u;
+      v[u] = (src != nullptr && i < nv) ? src[i] : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (i0 + 32 * u < nv) dst[i0 + 32 * u] = v[u];
+  }
 }
 
 // ---- dh: the final scatter ---------------------------------------------------------
@@ -809,7 +840,8 @@ cudaError_t prepare(const void* h, int64_t N, int64_t V, int64_t d, const int32_
   p.T = T;
   lmh_scan_kernel<<<1, 1024, 0, stream>>>(mask, p.N, counters, P.pos, idx, p.row_cnt,
                                           (P.L.Mcap / BM) * 4, logprob, lse);
-  lmh_gather_kernel<<<p.N + BM, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(h), p.N,
+  lmh_gather_kernel<<<cdiv(p.N + BM, kGatherWarps), 32 * kGatherWarps, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(h), p.N,
                                                  p.d, counters, P.pos, P.hc);
   return cudaGetLastError();
 }
