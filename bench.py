@@ -397,7 +397,8 @@ def main():
                      "algorithmic_bytes_per_launch": k_bytes, "peak_source": peak_src},
         "clocks": res["clocks"],
         "gpu_launches": res["launches"],
-        "peak_extra_device_bytes": int(extra_mem),
+        "peak_extra_device_bytes": int(extra_mem),  # beyond the inputs, outputs included
+        "peak_workspace_bytes": int(extra_mem - (2 * N * 4 + N * V * inp.x.element_size())),
     }
     if rank == 0:
         line["e2e"] = e2e_logits(inp, args.e2e_steps, device)
