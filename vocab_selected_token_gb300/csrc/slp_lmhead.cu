@@ -14,8 +14,8 @@
 //                epilogue warp that stores the last slab of its 32 rows merges
 //                their partials in slab order and writes logprob/lse to the
 //                original rows.
-// Backward, per vocabulary chunk of at most kVChunk columns (the survey's
-// per-V-chunk form: bounded workspace instead of a [rows, V] buffer)
+// Backward, per vocabulary chunk of at most kVChunk columns (a bounded
+// workspace instead of a [rows, V] buffer)
 //   1-2. scan + gather as above (once)
 //   3. GEMM (recompute): the chunk's tiles; the epilogue writes
 //        dz = g/T (1[v == t] - 2^(x*c - lse*log2 e)) as bf16 (rows >= Na: 0)
