@@ -75,7 +75,9 @@ def test_full_size_sampled():
     of logprob / dh and sampled rows of dW against the oracle."""
     dev = device()
     a = W.make_lmhead_inputs(device=dev)
-    lp, lse, dh, dW = run_fwd_bwd(a)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    lp, lse, dh, dW = run_fwd_bwd(a, err=err)
+    assert int(err.item()) == 0  # no data error and no pipeline wait that gave up
     h64, W64 = to64(a.h), to64(a.W)
     t, m, g = a.t.cpu().numpy(), a.mask.cpu().numpy(), to64(a.g)
     act = np.nonzero(m)[0]

@@ -263,9 +263,11 @@ def test_fused_forward_backward_full_size(name):
     dev = device()
     a = W.make_logits_inputs(name, device=dev)
     N = a.x.shape[0]
-    lp, lse, gx = slp.slp_forward_backward(a.x, a.t, a.mask, a.T, a.g)
-    lp2, lse2 = slp.slp_forward(a.x, a.t, a.mask, a.T)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    lp, lse, gx = slp.slp_forward_backward(a.x, a.t, a.mask, a.T, a.g, err=err)
+    lp2, lse2 = slp.slp_forward(a.x, a.t, a.mask, a.T, err=err)
     torch.cuda.synchronize()
+    assert int(err.item()) == 0  # no data error and no wait that gave up
     rows = set(np.random.default_rng(23).choice(N, 24, replace=False).tolist()) | {0, N - 1}
     check_rows(a.x, a.t, a.mask, a.T, a.g, lp, lse, gx, rows)
     # same quantity as the separate forward, every row

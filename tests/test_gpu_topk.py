@@ -70,7 +70,11 @@ def test_topk_fp32_masked_repeated_ids():
 def test_topk_full_size_sampled():
     dev = device()
     a = W.make_topk_inputs(device=dev)
-    kl, sm, tm, lse, gx = run(a, a.clamp)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    kl, sm, tm, lse = slp.slp_topk_kl_forward(a.x, a.ids, a.lt, a.mask, a.T, a.clamp, err=err)
+    gx = slp.slp_topk_kl_backward(a.x, a.ids, a.lt, a.mask, a.T, a.clamp, lse, a.g, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0  # no data error and no wait that gave up
     N = a.x.shape[0]
     rows = set(np.random.default_rng(31).choice(N, 16, replace=False).tolist()) | {0, N - 1}
     check(a, kl, sm, tm, lse, gx, rows, a.clamp)

@@ -14,11 +14,19 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ uint64_t global_timer_ns() {
+// This SM's cycle counter, for the bounded waits.  It only counts up for the
+// waiting thread; %globaltimer is kept in step with the host's time and may
+// jump, and a step backwards turns an unsigned difference into a huge
+// elapsed time (a spurious give-up).
+__device__ __forceinline__ uint64_t sm_cycles() {
   uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  asm volatile("mov.u64 %0, %%clock64;" : "=l"(t));
   return t;
 }
+
+// Cycles per nanosecond used to turn a wait limit into cycles: about the
+// highest SM clock (2.07 GHz), so a limit lasts at least as long as stated.
+constexpr uint64_t kCyclesPerNs = 2;
 
 // ---- mbarrier ---------------------------------------------------------------
 
@@ -52,18 +60,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait until the phase with the given parity has completed, giving up after
-// `limit_ns` of wall time or as soon as *abort is set by another thread
-// (abort may be NULL: then only the time limit applies).  Returns false when
-// it gave up; a wait that timed out also sets *abort.
+// about `limit_ns` (counted in this SM's cycles, at least that long at any
+// clock) or as soon as *abort is set by another thread (abort may be NULL:
+// then only the limit applies).  Returns false when it gave up; a wait that
+// ran out also sets *abort.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   volatile int* abort, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
+  const uint64_t t0 = sm_cycles();
+  const uint64_t limit = limit_ns * kCyclesPerNs;
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 0) {
       if (abort != nullptr && *abort) return false;
-      if (global_timer_ns() - t0 > limit_ns) {
+      if (sm_cycles() - t0 > limit) {
         if (abort != nullptr) *abort = 1;
         return false;
       }
