@@ -44,7 +44,7 @@ def parse():
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["slp", "reference"], default="slp")
     p.add_argument("--config", default="c151k", choices=["c151k", "packed", "stability", "tiny"])
-    p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--no-extra", action="store_true", help="skip the other workloads' lines")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--lmhead-only", action="store_true",
@@ -258,7 +258,7 @@ def e2e_logits(inp, steps, device):
         forward_backward_from_host(xh, th, gh, mh, inp.T, logprob=lp_h, lse=lse_h, grad_x=gx_h,
                                    device=device)
 
-    for _ in range(2):
+    for _ in range(3):
         step()
     torch.cuda.synchronize(device)
     t0 = time.perf_counter()
