@@ -447,9 +447,9 @@ __global__ void __launch_bounds__(kFbThreads, kRV > 0 ? 4 : 1)
   constexpr int kPer = kFbChunk / 16 / kFbThreads;
   bool ok = true;
   for (int k = 0; k < nch; ++k) {
-    const bool got =
-        sm100::mbar_wait_bounded(bbase + 8 * k, 0, &abort_flag, kFwdWaitNs);
-    if (__syncthreads_or(!got)) {
+    // each thread waits on its own; one that gives up sets abort_flag, which
+    // ends the others' waits, and the CTA agrees on `ok` after the loop
+    if (!sm100::mbar_wait_bounded(bbase + 8 * k, 0, &abort_flag, kFwdWaitNs)) {
       ok = false;
       break;
     }
@@ -461,6 +461,7 @@ __global__ void __launch_bounds__(kFbThreads, kRV > 0 ? 4 : 1)
     }
     lse2_fold_vec<kPer>(st, vv, c, tag);
   }
+  ok = !__syncthreads_or(!ok);
   if constexpr (kRV > 0) lse2_fold_vec<kRV>(st, rv, c, tag);
   if (!ok && threadIdx.x == 0) {
     if (err != nullptr) atomicOr(err, SLP_DEVICE_ERR_TIMEOUT);
