@@ -284,6 +284,18 @@ size_t slp_lmhead_workspace_size(int64_t N, int64_t V, int64_t d);
 size_t slp_lmhead_forward_workspace_size(int64_t N, int64_t V, int64_t d);
 
 /*
+ * slp_lmhead_workspace_size_max - bytes of workspace with which the LM-head
+ * backward runs the whole vocabulary as one chunk.  Given a larger workspace
+ * than slp_lmhead_workspace_size, the backward uses the widest chunk that fits:
+ * the whole vocabulary, else 131072 columns, else 65536.  Fewer chunks mean
+ * fewer GEMM launches.  At N=8192, V=151936, d=2560 this takes 3.96 GB
+ * instead of 1.86 GB and is about 2 % faster.  Results agree within the
+ * LM-head tolerances, not bit for bit: the dh sums are regrouped.  Returns 0
+ * for invalid sizes.
+ */
+size_t slp_lmhead_workspace_size_max(int64_t N, int64_t V, int64_t d);
+
+/*
  * slp_lmhead_forward - selected-token log-probabilities through the LM head,
  * logits never stored.
  *

@@ -172,3 +172,15 @@ def test_binding_refuses_overlapping_outputs():
         slp._check_disjoint("grad_x", x[1:], x)
     slp._check_disjoint("grad_x", torch.zeros(4, 8), x)
     slp._check_disjoint("dW", torch.zeros(3, 2), None, torch.zeros(5))
+
+
+def test_lmhead_workspace_size_max(lib):
+    """The whole-vocabulary workspace is at least the default one, equal to it
+    when the vocabulary fits one default chunk, and 0 for invalid sizes."""
+    big = lib.slp_lmhead_workspace_size_max(8192, 151936, 2560)
+    dflt = lib.slp_lmhead_workspace_size(8192, 151936, 2560)
+    assert big > dflt > lib.slp_lmhead_forward_workspace_size(8192, 151936, 2560)
+    assert lib.slp_lmhead_workspace_size_max(300, 60000, 256) == \
+        lib.slp_lmhead_workspace_size(300, 60000, 256)
+    assert lib.slp_lmhead_workspace_size_max(-1, 100, 64) == 0
+    assert lib.slp_lmhead_workspace_size_max(10, 100, 0) == 0

@@ -201,3 +201,30 @@ def test_lmhead_matches_logits_path():
         cos = float((got * ref).sum() / (got.norm() * ref.norm()))
         frob = float((got - ref).norm() / ref.norm())
         assert cos >= 0.9999 and frob <= 1e-2, f"{what}: cosine {cos:.6f} frob {frob:.3e}"
+
+
+@pytest.mark.parametrize("extra", ["max", "middle"])
+def test_backward_wider_chunks_from_larger_workspace(extra):
+    """A workspace of slp_lmhead_workspace_size_max runs the backward as one
+    vocabulary chunk, one a little smaller as 131072 + the rest; both agree
+    with the oracle and with the default chunking."""
+    dev = device()
+    N, V, d = 200, 140000, 128
+    a = W.make_lmhead_inputs(device=dev, N=N, V=V, d=d, p_mask=0.8, seed=44)
+    a.W = (a.W.float() * 5).to(torch.bfloat16)
+    lp, lse = slp.slp_lmhead_forward(a.h, a.W, a.t, a.mask, a.T)
+    big = slp.slp_lmhead_workspace_size_max(N, V, d)
+    assert big > slp.slp_lmhead_workspace_size(N, V, d)
+    nbytes = big if extra == "max" else big - 256
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    dh, dW = slp.slp_lmhead_backward(a.h, a.W, a.t, a.mask, a.T, lse, a.g, ws=ws)
+    dh0, dW0 = slp.slp_lmhead_backward(a.h, a.W, a.t, a.mask, a.T, lse, a.g)
+    torch.cuda.synchronize()
+    h64, W64 = to64(a.h), to64(a.W)
+    t, m, g = a.t.cpu().numpy(), a.mask.cpu().numpy(), to64(a.g)
+    _, rlse = O.lmhead_forward(h64, W64, t, m, a.T)
+    rdh, rdW = O.lmhead_backward(h64, W64, t, m, a.T, rlse, g)
+    grad_ok(to64(dh), rdh, "dh")
+    grad_ok(to64(dW), rdW, "dW")
+    grad_ok(to64(dh), to64(dh0), "dh against the default chunking")
+    grad_ok(to64(dW), to64(dW0), "dW against the default chunking")

@@ -262,6 +262,12 @@ def slp_lmhead_workspace_size(N: int, V: int, d: int) -> int:
     return int(_lib.load().slp_lmhead_workspace_size(int(N), int(V), int(d)))
 
 
+def slp_lmhead_workspace_size_max(N: int, V: int, d: int) -> int:
+    """Bytes of workspace with which slp_lmhead_backward runs the whole
+    vocabulary as one chunk (fewer launches; the default is 65536 columns)."""
+    return int(_lib.load().slp_lmhead_workspace_size_max(int(N), int(V), int(d)))
+
+
 def slp_lmhead_forward_workspace_size(N: int, V: int, d: int) -> int:
     """Bytes of workspace slp_lmhead_forward alone needs."""
     return int(_lib.load().slp_lmhead_forward_workspace_size(int(N), int(V), int(d)))

@@ -200,6 +200,11 @@ size_t slp_lmhead_workspace_size(int64_t N, int64_t V, int64_t d) {
   return slp::lmhead_workspace_size(N, V, d);
 }
 
+size_t slp_lmhead_workspace_size_max(int64_t N, int64_t V, int64_t d) {
+  if (N < 0 || V <= 0 || d <= 0 || V > INT32_MAX || N > INT32_MAX || d > INT32_MAX) return 0;
+  return slp::lmhead_workspace_size_max(N, V, d);
+}
+
 size_t slp_lmhead_forward_workspace_size(int64_t N, int64_t V, int64_t d) {
   if (N < 0 || V <= 0 || d <= 0 || V > INT32_MAX || N > INT32_MAX || d > INT32_MAX) return 0;
   return slp::lmhead_forward_workspace_size(N, V, d);
@@ -230,7 +235,8 @@ int slp_lmhead_backward(const void* h, const void* W, int64_t N, int64_t V, int6
   if ((reinterpret_cast<uintptr_t>(dh) & 15u) || (reinterpret_cast<uintptr_t>(dW) & 15u))
     return SLP_ERR_MISALIGNED;
   return cuda_status(slp::launch_lmhead_backward(h, W, N, V, d, t, mask, T, lse, grad_out, dh,
-                                                 dW, ws, err, static_cast<cudaStream_t>(stream)));
+                                                 dW, ws, ws_bytes, err,
+                                                 static_cast<cudaStream_t>(stream)));
 }
 
 int slp_lmhead_backward_accumulate(const void* h, const void* W, int64_t N, int64_t V, int64_t d,
@@ -247,7 +253,7 @@ int slp_lmhead_backward_accumulate(const void* h, const void* W, int64_t N, int6
   if ((reinterpret_cast<uintptr_t>(dh) & 15u) || (reinterpret_cast<uintptr_t>(dW_accum) & 15u))
     return SLP_ERR_MISALIGNED;
   return cuda_status(slp::launch_lmhead_backward(h, W, N, V, d, t, mask, T, lse, grad_out, dh,
-                                                 dW_accum, ws, err,
+                                                 dW_accum, ws, ws_bytes, err,
                                                  static_cast<cudaStream_t>(stream), true));
 }
 

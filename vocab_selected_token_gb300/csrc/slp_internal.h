@@ -64,6 +64,7 @@ cudaError_t launch_topk_kl_backward(const void* x, int dtype, int64_t N, int64_t
 
 // Fused LM-head path (slp_lmhead.cu).
 size_t lmhead_workspace_size(int64_t N, int64_t V, int64_t d);
+size_t lmhead_workspace_size_max(int64_t N, int64_t V, int64_t d);
 size_t lmhead_forward_workspace_size(int64_t N, int64_t V, int64_t d);
 
 cudaError_t launch_lmhead_forward(const void* h, const void* W, int64_t N, int64_t V, int64_t d,
@@ -74,7 +75,7 @@ cudaError_t launch_lmhead_forward(const void* h, const void* W, int64_t N, int64
 cudaError_t launch_lmhead_backward(const void* h, const void* W, int64_t N, int64_t V, int64_t d,
                                    const int32_t* t, const uint8_t* mask, float T,
                                    const float* lse, const float* grad_out, void* dh, void* dW,
-                                   void* ws, int32_t* err, cudaStream_t stream,
+                                   void* ws, size_t ws_bytes, int32_t* err, cudaStream_t stream,
                                    bool accumulate_f32 = false);
 
 }  // namespace slp

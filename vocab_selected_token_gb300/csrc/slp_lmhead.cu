@@ -754,10 +754,12 @@ size_t max_partial_floats(int Mcap, int V, int vchunk, int d, int G) {
   return best;
 }
 
-Layout layout(int64_t N, int64_t V, int64_t d) {
+// vchunk: the backward's vocabulary chunk width (the whole vocabulary when
+// V is smaller).
+Layout layout(int64_t N, int64_t V, int64_t d, int64_t vchunk = kVChunk) {
   Layout L{};
   L.Mcap = static_cast<int>(cdiv(static_cast<int>(N), BM) * BM);
-  L.vchunk = V < kVChunk ? static_cast<int>(V) : kVChunk;
+  L.vchunk = V < vchunk ? static_cast<int>(V) : static_cast<int>(vchunk);
   L.ld_dz = (L.vchunk + 63) / 64 * 64;
   size_t o = 0;
   L.off_counters = o; o += 256;
@@ -798,13 +800,23 @@ struct Prepared {
   __nv_bfloat16* hc;
 };
 
+// The widest backward chunk whose workspace fits in ws_bytes: the whole
+// vocabulary, two default chunks, or the default chunk.
+int64_t chunk_for(int64_t N, int64_t V, int64_t d, size_t ws_bytes) {
+  const int64_t widths[2] = {V, 2ll * kVChunk};
+  for (int64_t w : widths)
+    if (w > kVChunk && layout(N, V, d, w).bwd_end <= ws_bytes) return w;
+  return kVChunk;
+}
+
 // logprob / lse: the forward's outputs (their inactive rows are zeroed here),
 // NULL for the backward.
 cudaError_t prepare(const void* h, int64_t N, int64_t V, int64_t d, const int32_t* t,
                     const uint8_t* mask, float T, void* ws, int32_t* err, cudaStream_t stream,
-                    Prepared* out, float* logprob = nullptr, float* lse = nullptr) {
+                    Prepared* out, float* logprob = nullptr, float* lse = nullptr,
+                    int64_t vchunk = kVChunk) {
   Prepared& P = *out;
-  P.L = layout(N, V, d);
+  P.L = layout(N, V, d, vchunk);
   uint8_t* w = static_cast<uint8_t*>(ws);
   int32_t* counters = reinterpret_cast<int32_t*>(w + P.L.off_counters);
   P.pos = reinterpret_cast<int32_t*>(w + P.L.off_pos);
@@ -856,6 +868,10 @@ size_t lmhead_workspace_size(int64_t N, int64_t V, int64_t d) {
   return lmh::layout(N, V, d).bwd_end;
 }
 
+size_t lmhead_workspace_size_max(int64_t N, int64_t V, int64_t d) {
+  return lmh::layout(N, V, d, V).bwd_end;
+}
+
 cudaError_t launch_lmhead_forward(const void* h, const void* W, int64_t N, int64_t V, int64_t d,
                                   const int32_t* t, const uint8_t* mask, float T, float* logprob,
                                   float* lse, void* ws, int32_t* err, cudaStream_t stream) {
@@ -873,11 +889,12 @@ cudaError_t launch_lmhead_forward(const void* h, const void* W, int64_t N, int64
 cudaError_t launch_lmhead_backward(const void* h, const void* W, int64_t N, int64_t V, int64_t d,
                                    const int32_t* t, const uint8_t* mask, float T,
                                    const float* lse, const float* grad_out, void* dh, void* dW,
-                                   void* ws, int32_t* err, cudaStream_t stream,
+                                   void* ws, size_t ws_bytes, int32_t* err, cudaStream_t stream,
                                    bool accumulate_f32) {
   using namespace lmh;
   Prepared P;
-  cudaError_t e = prepare(h, N, V, d, t, mask, T, ws, err, stream, &P);
+  cudaError_t e = prepare(h, N, V, d, t, mask, T, ws, err, stream, &P, nullptr, nullptr,
+                          chunk_for(N, V, d, ws_bytes));
   if (e != cudaSuccess) return e;
   P.p.g = grad_out;
   P.p.lse = lse;
