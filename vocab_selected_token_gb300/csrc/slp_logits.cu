@@ -194,26 +194,35 @@ __global__ void __launch_bounds__(kFwdThreads)
   }
   if (splits == 1) return;
 
-  // Cluster merge: CTA rank 0 reads the other ranks' states, in rank order,
-  // from their shared memory; the second barrier keeps every CTA resident
-  // until those reads are done.
-  cluster_sync_all();
-  if (rank == 0 && threadIdx.x == 0) {
-    St acc;
-    float* af = reinterpret_cast<float*>(&acc);
+  // Cluster merge: in CTA rank 0, lane r of warp 0 reads rank r's state over
+  // DSMEM (the reads overlap) and lane 0 merges them in rank order.  Only
+  // thread 0 of each CTA wrote its state, so only it fences before the
+  // barrier.  The second barrier keeps every CTA resident until those reads
+  // are done.
+  constexpr int kF = static_cast<int>(sizeof(St) / 4);
+  cluster_sync_from_thread0();
+  if (rank == 0 && warp == 0) {
+    St o;
+    st_empty(o);
+    float* of = reinterpret_cast<float*>(&o);
+    if (lane < splits) {
 #pragma unroll
-    for (int k = 0; k < static_cast<int>(sizeof(St) / 4); ++k) af[k] = cta_part[k];
-    for (int r = 1; r < splits; ++r) {
-      St o;
-      float* of = reinterpret_cast<float*>(&o);
-#pragma unroll
-      for (int k = 0; k < static_cast<int>(sizeof(St) / 4); ++k)
-        of[k] = ld_shared_cluster_f32(map_shared_rank(&cta_part[k], r));
-      acc = st_merge(acc, o);
+      for (int k = 0; k < kF; ++k) of[k] = ld_shared_cluster_f32(map_shared_rank(&cta_part[k], lane));
     }
-    finish(acc);
+    St acc;
+    st_empty(acc);
+    for (int r = 0; r < splits; ++r) {
+      St pr;
+      float* pf = reinterpret_cast<float*>(&pr);
+#pragma unroll
+      for (int k = 0; k < kF; ++k) pf[k] = __shfl_sync(0xFFFFFFFFu, of[k], r);
+      acc = st_merge(acc, pr);
+    }
+    if (lane == 0) finish(acc);
   }
-  cluster_sync_all();
+  asm volatile("barrier.cluster.arrive.relaxed;\n\t"
+               "barrier.cluster.wait.acquire;" ::
+                   : "memory");
 }
 
 // kEnt adds the entropy term -gH p_v (log p_v + H) / T (H, gH per row; g and
