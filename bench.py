@@ -613,6 +613,9 @@ def time_lmhead(device, steps=10, warmup=3, N=None):
     res["step_frac"] = res["step_tflops"] / peak
     res["bwd_frac_sustained"] = res["bwd_tflops"] / peak_sus
     res["step_frac_sustained"] = res["step_tflops"] / peak_sus
+    # NVIDIA's dense bf16 figure for one GB300 (half its 2:4-sparse figure)
+    res["peak_bf16_tflops_datasheet"] = 2250.0
+    res["step_frac_datasheet"] = res["step_tflops"] / 2250.0
     del a, ws, dh, dW
     torch.cuda.empty_cache()
     return res
