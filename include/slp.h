@@ -216,7 +216,8 @@ int slp_topk_kl_backward(const void* x, int dtype, int64_t N, int64_t V, int64_t
  *
  * Defined by: the two calls above (same definitions, same results within
  * their tolerances).  Each row is read from HBM once and kept on chip (a
- * thread-block cluster splits it across up to 8 CTAs' shared memory) between
+ * thread-block cluster splits it across up to 8 CTAs' registers and shared
+ * memory) between
  * the log-sum-exp and the gradient pass, so the row's bytes are read once
  * instead of twice (NeMo-RL PR #4222, "Changes": recompute the softmax rather
  * than store it).  Rows that are not 16-byte aligned, or longer than
