@@ -137,6 +137,22 @@ def test_split_invariance():
                *slp.slp_forward(big.x[:4], big.t[:4], None, 1.0), None, range(4))
 
 
+def test_short_rows_both_forward_kernels():
+    """Rows of 60 KB take the warp-per-row forward when there are many rows
+    and the ring kernel when there are few; the same rows agree across the
+    two and with the oracle (logits path tolerances)."""
+    dev = device()
+    big = W.make_logits_inputs("c151k", device=dev, N=4000, V=30000)
+    lp_many, lse_many = slp.slp_forward(big.x, big.t, None, 1.0)
+    lp_few, lse_few = slp.slp_forward(big.x[:1000], big.t[:1000], None, 1.0)
+    torch.cuda.synchronize()
+    assert float((lp_many[:1000] - lp_few).abs().max()) <= TOL_LP
+    assert float((lse_many[:1000] - lse_few).abs().max()) <= TOL_LP
+    rows = [0, 1, 517, 999, 1000, 3999]
+    gx = slp.slp_backward(big.x, big.t, None, 1.0, lse_many, big.g)
+    check_rows(big.x, big.t, None, 1.0, big.g, lp_many, lse_many, gx, rows)
+
+
 def test_deterministic():
     dev = device()
     a = W.make_logits_inputs("c151k", device=dev, N=512)
