@@ -256,7 +256,7 @@ def test_autograd_and_side_stream():
 # ---- fused forward + backward (slp_forward_backward) -------------------------
 
 FB_SCALED = [
-    ("tiny", None, None),             # one CTA per row
+    ("tiny", None, None),             # 4 KB rows: one warp per row
     ("c151k", 48, 151936),            # cluster of 4
     ("c151k", 33, 151936 - 5),        # ragged tail: rows not 16-byte aligned -> separate kernels
     ("packed", 3000, 20016),
@@ -302,6 +302,56 @@ def test_fused_forward_backward_long_rows(V):
     lp, lse, gx = slp.slp_forward_backward(a.x, a.t, a.mask, a.T, a.g)
     torch.cuda.synchronize()
     check_rows(a.x, a.t, a.mask, a.T, a.g, lp, lse, gx, range(5))
+
+
+# Short rows (at most 32 KB) take the warp-per-row fused kernel: V chosen so
+# that each register width (1, 2, 4, 8, 16 vectors per lane) and the
+# shared-memory slot (rows above 8 KB) is used, some with a scalar tail.
+FB_ROWS = [
+    ("packed", 70, 200),        # bf16, 1 vector per lane, masked spans
+    ("tiny", 37, 504),          # 2 per lane
+    ("packed", 65, 1000),       # 4 per lane
+    ("tiny", 33, 4096),         # 16 per lane, all in registers
+    ("c151k", 41, 4104),        # 16 per lane + one vector per lane in shared memory
+    ("c151k", 64, 8192),        # 8 KB in registers, 8 KB in shared memory
+    ("packed", 300, 16384),     # the longest row: 8 KB + 24 KB
+    ("stability", 29, 2048),    # fp32, 16 per lane, inf/-inf rows
+    ("stability", 22, 8192),    # fp32, 32 KB
+]
+
+
+@pytest.mark.parametrize("name,N,V", FB_ROWS, ids=lambda v: str(v))
+def test_fused_short_rows_all_rows(name, N, V):
+    dev = device()
+    a = W.make_logits_inputs(name, device=dev, N=N, V=V)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    lp, lse, gx = slp.slp_forward_backward(a.x, a.t, a.mask, a.T, a.g, err=err)
+    lp2, lse2 = slp.slp_forward(a.x, a.t, a.mask, a.T)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    check_rows(a.x, a.t, a.mask, a.T, a.g, lp, lse, gx, range(N))
+    assert_close_nan(to64(lp), to64(lp2), TOL_LP, "logprob vs separate forward")
+    if a.mask is not None:
+        assert bool((gx[a.mask == 0].view(torch.int16 if gx.dtype == torch.bfloat16
+                                          else torch.int32) == 0).all())
+
+
+@pytest.mark.parametrize("V", [4101, 16381])
+def test_fused_short_rows_ragged_tail(V):
+    """Rows of V not a multiple of 8 on a 16-byte-aligned stride: the scalar
+    tail of the warp-per-row kernel, targets in the tail included, and
+    grad_x's padding columns left untouched."""
+    dev = device()
+    Vp = (V + 7) // 8 * 8
+    a = W.make_logits_inputs("c151k", device=dev, N=48, V=Vp)
+    x = a.x[:, :V]
+    t = a.t % V
+    t[:8] = V - 1 - torch.arange(8, dtype=torch.int32, device=dev) % (V % 8)
+    gx = torch.full((48, Vp), 7.0, dtype=torch.bfloat16, device=dev)
+    lp, lse, _ = slp.slp_forward_backward(x, t, None, a.T, a.g, grad_x=gx[:, :V])
+    torch.cuda.synchronize()
+    assert bool((gx[:, V:] == 7.0).all())
+    check_rows(x, t, None, a.T, a.g, lp, lse, gx[:, :V], range(48))
 
 
 def test_fused_forward_backward_bad_target():

@@ -633,6 +633,136 @@ __global__ void __launch_bounds__(kFbThreads, kRV > 0 ? 4 : 1)
   asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
 }
 
+// ---- fused forward + backward, short rows: one warp per row ----------------
+//
+// A warp holds its row on chip: the first 32 * kNV vectors in registers (kNV
+// per lane, plain 16-byte loads), the rest of a row longer than 8 KB in the
+// warp's own slot of shared memory, filled by one bulk copy that lane 0
+// issues before the register loads.  The lanes fold the log-sum-exp, merge by
+// butterfly shuffles (every lane ends with the same state) and write the
+// gradient from registers and shared memory.  No CTA barrier and no cluster:
+// for short rows the per-row set-up of the cluster kernel above (barrier
+// initialisation, CTA and cluster merges) costs more than the row's own
+// traffic, and one CTA of 256 threads per 8 KB row keeps too few bytes in
+// flight.
+constexpr int kFbRowsWarps = 4;
+constexpr int kFbRowsMaxNV = 16;                // register vectors per lane (8 KB per warp)
+constexpr int kFbRowsMaxSlot = 24 * 1024;       // shared-memory part per warp
+constexpr int kFbRowsMaxBytes = kFbRowsMaxNV * 32 * 16 + kFbRowsMaxSlot;  // 32 KB rows
+
+template <typename Elt, int kNV>
+__global__ void __launch_bounds__(32 * kFbRowsWarps, kNV >= 16 ? 4 : 8)
+    slp_fwd_bwd_rows_kernel(const Elt* __restrict__ x, int64_t N, int64_t V, int64_t ld,
+                            const int32_t* __restrict__ t, const uint8_t* __restrict__ mask,
+                            float T, float c, float invT, const float* __restrict__ g,
+                            float* __restrict__ logprob, float* __restrict__ lse,
+                            Elt* __restrict__ gx, int64_t ldg, int32_t* __restrict__ err,
+                            int slot_bytes) {
+  using E = Elem<Elt>;
+  constexpr int kVec = E::kVec;
+  extern __shared__ __align__(128) uint8_t slots[];
+  __shared__ __align__(8) uint64_t full[kFbRowsWarps];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kFbRowsWarps + w;
+  if (row >= N) return;
+  const int64_t nvec = V / kVec;
+  Elt* gr = gx + row * ldg;
+  uint4* gv = reinterpret_cast<uint4*>(gr);
+  if (mask != nullptr && mask[row] == 0) {
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    for (int64_t i = lane; i < nvec; i += 32) st_stream(gv + i, z);
+    for (int64_t e = nvec * kVec + lane; e < V; e += 32) E::store1(gr + e, 0.f);
+    if (lane == 0) {
+      logprob[row] = 0.f;
+      lse[row] = 0.f;
+    }
+    return;
+  }
+  const Elt* xr = x + row * ld;
+  const uint4* xv = reinterpret_cast<const uint4*>(xr);
+  const int nreg = static_cast<int>(nvec < 32 * kNV ? nvec : 32 * kNV);
+  const int ns = static_cast<int>(nvec - nreg);  // vectors in shared memory (<= slot_bytes / 16)
+  const uint32_t slot = sm100::smem_u32(slots) + static_cast<uint32_t>(w * slot_bytes);
+  const uint32_t bar = sm100::smem_u32(&full[w]);
+  if (ns > 0) {
+    if (lane == 0) {
+      sm100::mbar_init(bar, 1);
+      sm100::fence_mbar_init();
+      sm100::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(ns) * 16u);
+      sm100::bulk_load(slot, xv + nreg, static_cast<uint32_t>(ns) * 16u, bar);
+    }
+    __syncwarp();  // the barrier's initialisation is seen by every lane
+  }
+  const int32_t tt = t[row];
+  const bool tvalid = tt >= 0 && static_cast<int64_t>(tt) < V;
+  const float gT = tvalid ? g[row] * invT : __int_as_float(0x7FC00000);
+  const uint4 pad = make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord, E::kNegInfWord);
+  uint4 rv[kNV];
+#pragma unroll
+  for (int u = 0; u < kNV; ++u) {
+    const int i = u * 32 + lane;
+    rv[u] = i < nreg ? ld_stream(xv + i) : pad;
+  }
+  const Elt* tag = nullptr;
+  Lse2 st = lse2_empty();
+  lse2_fold_vec<kNV>(st, rv, c, tag);
+  const uint4* q = reinterpret_cast<const uint4*>(slots + w * slot_bytes);
+  if (ns > 0) {
+    bool ok = sm100::mbar_wait_bounded(bar, 0, nullptr, kFwdWaitNs);
+    ok = __all_sync(0xFFFFFFFFu, ok);
+    if (!ok && lane == 0) {
+      if (err != nullptr) atomicOr(err, SLP_DEVICE_ERR_TIMEOUT);
+      sm100::mbar_wait_bounded(bar, 0, nullptr, kFwdWaitNs);  // let the copy land
+    }
+    constexpr int kPer = 4;
+    for (int i0 = lane; i0 < ns; i0 += 32 * kPer) {
+      uint4 vv[kPer];
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        const int i = i0 + 32 * u;
+        vv[u] = i < ns ? q[i] : pad;
+      }
+      lse2_fold_vec<kPer>(st, vv, c, tag);
+    }
+  }
+  for (int64_t e = nvec * kVec + lane; e < V; e += 32) {  // fewer than kVec trailing elements
+    float f1[1] = {E::load1(xr + e)};
+    lse2_fold<1>(st, f1, c);
+  }
+  st = lse2_warp_reduce(st);
+  if (lane == 0) {
+    const float xt = tvalid ? E::load1(xr + tt) : 0.f;
+    write_row_result(st, xt, tvalid, T, c, logprob, lse, err, row);
+  }
+
+  // gradient, as in the cluster kernel: a p = sign(a) 2^(x c - off + log2 |a|)
+  // per vector, the target's element rewritten by the lane that stored it
+  const float off = (st.m == -INFINITY || !(st.s > 0.f)) ? __int_as_float(0x7FC00000)
+                                                          : st.mc + log2f(st.s);
+  const float a = -gT;
+  const float no1 = log2f(fabsf(a)) - off;
+  const float2 cc = make_float2(c, c), no = make_float2(no1, no1);
+  const uint32_t sgn = sign_mask(a, tag);
+  const int64_t tvec = tvalid ? static_cast<int64_t>(tt) / kVec : -1;
+  auto put = [&](int64_t i, const uint4& v) {
+    st_stream(gv + i, scaled_exp2_vec(v, cc, no, sgn, tag));
+    if (i == tvec) {
+      const float p = ex2(fmaf(E::load1(xr + tt), c, -off));
+      E::store1(gr + tt, fmaf(a, p, gT));
+    }
+  };
+#pragma unroll
+  for (int u = 0; u < kNV; ++u) {
+    const int i = u * 32 + lane;
+    if (i < nreg) put(i, rv[u]);
+  }
+  for (int i = lane; i < ns; i += 32) put(nreg + i, q[i]);
+  for (int64_t e = nvec * kVec + lane; e < V; e += 32) {
+    const float p = ex2(fmaf(E::load1(xr + e), c, -off));
+    E::store1(gr + e, (e == tt) ? fmaf(a, p, gT) : a * p);
+  }
+}
+
 namespace {
 
 bool aligned16(const void* p, int64_t ld, int esize) {
@@ -717,6 +847,54 @@ cudaError_t bwd_typed(const Elt* x, int64_t N, int64_t V, int64_t ld, const int3
   return cudaGetLastError();
 }
 
+__host__ __device__ constexpr bool use_fb_rows_kernel(int64_t N, int64_t row_bytes) {
+  return row_bytes <= kFbRowsMaxBytes && N > 0;
+}
+
+template <typename Elt, int kNV>
+cudaError_t fwd_bwd_rows_launch(const Elt* x, int64_t N, int64_t V, int64_t ld, const int32_t* t,
+                                const uint8_t* mask, float T, const float* g, float* logprob,
+                                float* lse, Elt* gx, int64_t ldg, int32_t* err,
+                                cudaStream_t stream) {
+  constexpr int kVec = Elem<Elt>::kVec;
+  const int64_t nvec = V / kVec;
+  const int64_t ns = nvec > 32 * kNV ? nvec - 32 * kNV : 0;
+  const int slot_bytes = static_cast<int>(ns * 16);
+  if (slot_bytes > kFbRowsMaxSlot) return cudaErrorInvalidValue;
+  const int smem = slot_bytes * kFbRowsWarps;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(slp_fwd_bwd_rows_kernel<Elt, kNV>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kFbRowsMaxSlot * kFbRowsWarps);
+    if (e != cudaSuccess) return e;
+  }
+  const int64_t blocks = (N + kFbRowsWarps - 1) / kFbRowsWarps;
+  if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
+  const float c = static_cast<float>(1.4426950408889634 / static_cast<double>(T));
+  slp_fwd_bwd_rows_kernel<Elt, kNV>
+      <<<static_cast<unsigned>(blocks), 32 * kFbRowsWarps, smem, stream>>>(
+          x, N, V, ld, t, mask, T, c, 1.0f / T, g, logprob, lse, gx, ldg, err, slot_bytes);
+  return cudaGetLastError();
+}
+
+// Register vectors per lane: the smallest power of two that holds the row,
+// at most kFbRowsMaxNV (the rest then goes to shared memory).
+template <typename Elt>
+cudaError_t fwd_bwd_rows_typed(const Elt* x, int64_t N, int64_t V, int64_t ld, const int32_t* t,
+                               const uint8_t* mask, float T, const float* g, float* logprob,
+                               float* lse, Elt* gx, int64_t ldg, int32_t* err,
+                               cudaStream_t stream) {
+  const int64_t per_lane = (V / Elem<Elt>::kVec + 31) / 32;
+#define SLP_FB_ROWS(NV) \
+  fwd_bwd_rows_launch<Elt, NV>(x, N, V, ld, t, mask, T, g, logprob, lse, gx, ldg, err, stream)
+  if (per_lane <= 1) return SLP_FB_ROWS(1);
+  if (per_lane <= 2) return SLP_FB_ROWS(2);
+  if (per_lane <= 4) return SLP_FB_ROWS(4);
+  if (per_lane <= 8) return SLP_FB_ROWS(8);
+  return SLP_FB_ROWS(16);
+#undef SLP_FB_ROWS
+}
+
 // Fused forward + backward: needs 16-byte-aligned rows and rows short enough
 // to fit a cluster of at most 8 CTAs x 96 KB; returns cudaErrorNotSupported
 // otherwise (the caller then runs the separate kernels).
@@ -728,6 +906,8 @@ cudaError_t fwd_bwd_typed(const Elt* x, int64_t N, int64_t V, int64_t ld, const 
   if (!aligned16(x, ld, sizeof(Elt)) || !aligned16(gx, ldg, sizeof(Elt)))
     return cudaErrorNotSupported;
   const int64_t nvec = V / kVec;
+  if (use_fb_rows_kernel(N, V * static_cast<int64_t>(sizeof(Elt))))
+    return fwd_bwd_rows_typed(x, N, V, ld, t, mask, T, g, logprob, lse, gx, ldg, err, stream);
   // Segments of at most kFbRegSeg bytes (kFbRV vectors per thread in
   // registers, the rest in shared memory) keep four CTAs resident per SM.
   // Longer rows take up to kFbMaxSeg of shared memory per CTA (two per SM).
