@@ -215,10 +215,11 @@ int slp_topk_kl_backward(const void* x, int dtype, int64_t N, int64_t V, int64_t
  * g = -advantage for a plain policy-gradient loss).
  *
  * Defined by: the two calls above (same definitions, same results within
- * their tolerances).  Each row is read from HBM once and kept on chip (a
- * thread-block cluster splits it across up to 8 CTAs' registers and shared
- * memory) between
- * the log-sum-exp and the gradient pass, so the row's bytes are read once
+ * their tolerances).  Each row is read from HBM once and kept on chip
+ * between the log-sum-exp and the gradient pass: a row of at most 32 KB by
+ * one warp (registers plus a shared-memory slot), a longer one by a
+ * thread-block cluster that splits it across up to 8 CTAs' registers and
+ * shared memory.  So the row's bytes are read once
  * instead of twice (NeMo-RL PR #4222, "Changes": recompute the softmax rather
  * than store it).  Rows that are not 16-byte aligned, or longer than
  * 8 x 96 KB, are served by slp_forward followed by slp_backward.
