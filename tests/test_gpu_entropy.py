@@ -39,7 +39,8 @@ def check_entropy_rows(a, gH, lp, lse, H, gx, rows):
 
 
 CASES = [("tiny", None, None), ("c151k", 48, 151936), ("packed", 3000, 20016),
-         ("stability", 256, 131072), ("tiny", 300, 2047), ("c151k", 6, 151936)]
+         ("stability", 256, 131072), ("tiny", 300, 2047), ("c151k", 6, 151936),
+         ("stability", 40, 3000), ("packed", 90, 600)]
 
 
 @pytest.mark.parametrize("name,N,V", CASES, ids=lambda v: str(v))

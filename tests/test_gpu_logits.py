@@ -83,6 +83,50 @@ def test_ragged_tail_on_vector_path():
     check_rows(x, a.t % V, None, a.T, a.g, lp, lse, gx[:, :V], range(40))
 
 
+# Short rows through the separate kernels: the warp-per-row forward and, where
+# the backward's 16 KB tiles would be under 90 % full, the warp-per-row
+# backward (including a 40 KB row, masked spans and fp32).
+SHORT = [
+    ("packed", 70, 200),
+    ("tiny", 37, 1000),
+    ("c151k", 41, 6144),
+    ("c151k", 24, 20480),
+    ("stability", 29, 2048),
+    ("stability", 20, 5000),
+]
+
+
+@pytest.mark.parametrize("name,N,V", SHORT, ids=lambda v: str(v))
+def test_short_rows_all_rows(name, N, V):
+    dev = device()
+    a = W.make_logits_inputs(name, device=dev, N=N, V=V)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    lp, lse = slp.slp_forward(a.x, a.t, a.mask, a.T, err=err)
+    gx = slp.slp_backward(a.x, a.t, a.mask, a.T, lse, a.g, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    check_rows(a.x, a.t, a.mask, a.T, a.g, lp, lse, gx, range(N))
+    if a.mask is not None:
+        assert bool((gx[a.mask == 0].view(torch.int16) == 0).all())
+
+
+def test_short_rows_ragged_tail_targets_in_tail():
+    """8 KB rows with V not a multiple of 8 on a 16-byte-aligned stride, some
+    targets among the trailing elements; grad_x's padding left untouched."""
+    dev = device()
+    V, Vp = 4101, 4104
+    a = W.make_logits_inputs("c151k", device=dev, N=48, V=Vp)
+    x = a.x[:, :V]
+    t = a.t % V
+    t[:8] = V - 1 - torch.arange(8, dtype=torch.int32, device=dev) % 5
+    gx = torch.full((48, Vp), 7.0, dtype=torch.bfloat16, device=dev)
+    lp, lse = slp.slp_forward(x, t, None, a.T)
+    slp.slp_backward(x, t, None, a.T, lse, a.g, grad_x=gx[:, :V])
+    torch.cuda.synchronize()
+    assert bool((gx[:, V:] == 7.0).all())
+    check_rows(x, t, None, a.T, a.g, lp, lse, gx[:, :V], range(48))
+
+
 FULL = ["c151k", "packed", "stability"]
 
 

@@ -293,8 +293,62 @@ __global__ void __launch_bounds__(32 * kRowsWarps)
   }
 }
 
-// kEnt adds the entropy term -gH p_v (log p_v + H) / T (H, gH per row; g and
-// gH may then be NULL, meaning zero).
+// Per-row terms of the backward.  Off the target an element's gradient is
+// a p with a = -g/T, or with the entropy term (kEnt; H and gH per row, g and
+// gH may then be NULL, meaning zero) p (a - gH/T ln 2 (log2 p + H log2 e)) =
+// p (a2 + gHl log2 p); the target's element adds g/T.  vec() does a 16-byte
+// vector of off-target elements in paired arithmetic (scaled_exp2_vec /
+// entropy_grad_vec), one() a single element in full.  log2 p is clamped at
+// -256 with the entropy term, so a -inf logit gives p = 0 and a finite
+// factor.
+template <typename Elt, bool kEnt>
+struct BwdRow {
+  float gT, L2, Hl2, gHl, a;
+  int64_t tt;
+  float2 cc, no, gHl2, a2;
+  uint32_t sgn;
+
+  // report: this thread flags a bad target in *err (one thread per row)
+  __device__ __forceinline__ void init(int64_t row, int64_t V, const int32_t* t, float invT,
+                                       float c, const float* lse, const float* g, const float* H,
+                                       const float* gH, int32_t* err, bool report) {
+    const Elt* tag = nullptr;
+    tt = t[row];
+    gT = (kEnt && g == nullptr) ? 0.f : g[row] * invT;
+    L2 = lse[row] * kLog2e;
+    float gHT = 0.f;
+    Hl2 = 0.f;
+    if (kEnt) {
+      gHT = gH == nullptr ? 0.f : gH[row] * invT;
+      Hl2 = H[row] * kLog2e;  // log p_v + H = ln 2 (log2 p_v + H log2 e)
+    }
+    if (tt < 0 || tt >= V) {
+      if (err != nullptr && report) atomicOr(err, SLP_DATA_ERR_TARGET);
+      gT = __int_as_float(0x7FC00000);
+    }
+    a = -gT;
+    gHl = -gHT * kLn2;
+    cc = make_float2(c, c);
+    const float no1 = kEnt ? -L2 : log2f(fabsf(a)) - L2;  // -(L2 - log2 |a|) without entropy
+    no = make_float2(no1, no1);
+    sgn = sign_mask(a, tag);
+    gHl2 = make_float2(gHl, gHl);
+    const float a2s = fmaf(gHl, Hl2, a);
+    a2 = make_float2(a2s, a2s);
+  }
+  __device__ __forceinline__ uint4 vec(const uint4& v) const {
+    const Elt* tag = nullptr;
+    return kEnt ? entropy_grad_vec(v, cc, no, gHl2, a2, tag) : scaled_exp2_vec(v, cc, no, sgn, tag);
+  }
+  __device__ __forceinline__ float one(float x, float c, bool is_t) const {
+    float l2p = fmaf(x, c, -L2);
+    if (kEnt) l2p = fmaxf(l2p, -256.f);
+    const float p = ex2(l2p);
+    const float w = kEnt ? fmaf(gHl, l2p + Hl2, a) : a;
+    return is_t ? fmaf(w, p, gT) : w * p;
+  }
+};
+
 // With the entropy term the register count would leave three or four CTAs
 // per SM; capping it for six measured 0.375 -> 0.360 ms on c151k.
 template <typename Elt, bool kVecPath, bool kEnt>
@@ -315,32 +369,8 @@ __global__ void __launch_bounds__(kBwdThreads, kEnt ? 6 : 1)
   const Elt* xr = x + row * ld;
   Elt* gr = gx + row * ldg;
   const int64_t e_tile = tile * kTileElems;
-
-  float gT = 0.f, L2 = 0.f, gHT = 0.f, Hl2 = 0.f;
-  int64_t tt = -1;
-  if (active) {
-    tt = t[row];
-    gT = (kEnt && g == nullptr) ? 0.f : g[row] * invT;
-    L2 = lse[row] * kLog2e;
-    if (kEnt) {
-      gHT = gH == nullptr ? 0.f : gH[row] * invT;
-      Hl2 = H[row] * kLog2e;  // log p_v + H = ln 2 (log2 p_v + H log2 e)
-    }
-    if (tt < 0 || tt >= V) {
-      if (err != nullptr && tile == 0 && threadIdx.x == 0) atomicOr(err, SLP_DATA_ERR_TARGET);
-      gT = __int_as_float(0x7FC00000);
-    }
-  }
-  const float a = -gT;
-  // gradient element from log2 p (the exponent l2p, clamped at -256 so a -inf
-  // logit gives p = 0 and a finite entropy factor), p and the target flag
-  auto clamp_ent = [](float u) { return kEnt ? fmaxf(u, -256.f) : u; };
-  const float gHl = -gHT * kLn2;
-  auto grad = [&](float l2p, float p, bool is_t) {
-    // p (a - gH/T ln2 (log2 p + H log2 e)), plus g/T on the target
-    const float w = kEnt ? fmaf(gHl, l2p + Hl2, a) : a;
-    return is_t ? fmaf(w, p, gT) : w * p;
-  };
+  BwdRow<Elt, kEnt> b;
+  if (active) b.init(row, V, t, invT, c, lse, g, H, gH, err, tile == 0 && threadIdx.x == 0);
 
   if constexpr (kVecPath) {
     uint4* gv = reinterpret_cast<uint4*>(gr);
@@ -364,46 +394,73 @@ __global__ void __launch_bounds__(kBwdThreads, kEnt ? 6 : 1)
       const int64_t e = e_tile + (static_cast<int64_t>(u) * kBwdThreads + threadIdx.x) * kVec;
       if (e + kVec <= V) buf[u] = ld_stream(xv + e / kVec);
     }
-    // Off-target elements in paired arithmetic (scaled_exp2_vec /
-    // entropy_grad_vec); the thread whose vector holds the target stores that
-    // element again, in full, after the vector (same thread: it lands last).
-    const Elt* tag = nullptr;
-    const float2 cc = make_float2(c, c);
-    const float no1 = kEnt ? -L2 : log2f(fabsf(a)) - L2;  // -(L2 - log2 |a|) without entropy
-    const float2 no = make_float2(no1, no1);
-    const uint32_t sgn = sign_mask(a, tag);
-    const float2 gHl2 = make_float2(gHl, gHl);
-    const float a2s = fmaf(gHl, Hl2, a);
-    const float2 a2 = make_float2(a2s, a2s);
+    // The thread whose vector holds the target stores that element again, in
+    // full, after the vector (same thread: it lands last).
 #pragma unroll
     for (int u = 0; u < kBwdUnroll; ++u) {
       const int64_t e = e_tile + (static_cast<int64_t>(u) * kBwdThreads + threadIdx.x) * kVec;
       if (e + kVec <= V) {
-        const uint4 out = kEnt ? entropy_grad_vec(buf[u], cc, no, gHl2, a2, tag)
-                               : scaled_exp2_vec(buf[u], cc, no, sgn, tag);
-        st_stream(gv + e / kVec, out);
-        if (tt >= e && tt < e + kVec) {
-          const float l2p = clamp_ent(fmaf(E::load1(xr + tt), c, -L2));
-          E::store1(gr + tt, grad(l2p, ex2(l2p), true));
-        }
+        st_stream(gv + e / kVec, b.vec(buf[u]));
+        if (b.tt >= e && b.tt < e + kVec) E::store1(gr + b.tt, b.one(E::load1(xr + b.tt), c, true));
       } else {
-        for (int64_t k = e; k < V; ++k) {
-          const float l2p = clamp_ent(fmaf(E::load1(xr + k), c, -L2));
-          E::store1(gr + k, grad(l2p, ex2(l2p), k == tt));
-        }
+        for (int64_t k = e; k < V; ++k) E::store1(gr + k, b.one(E::load1(xr + k), c, k == b.tt));
       }
     }
   } else {
     const int64_t e_end = min(V, e_tile + kTileElems);
-    for (int64_t e = e_tile + threadIdx.x; e < e_end; e += kBwdThreads) {
-      float out = 0.f;
-      if (active) {
-        const float l2p = clamp_ent(fmaf(E::load1(xr + e), c, -L2));
-        out = grad(l2p, ex2(l2p), e == tt);
+    for (int64_t e = e_tile + threadIdx.x; e < e_end; e += kBwdThreads)
+      E::store1(gr + e, active ? b.one(E::load1(xr + e), c, e == b.tt) : 0.f);
+  }
+}
+
+// Short rows: the backward with one warp per row (the grid above gives each
+// row tiles of 8192 elements, which a short row leaves mostly idle).  Same
+// per-element arithmetic as slp_bwd_kernel, so the same bits.
+template <typename Elt, bool kEnt>
+__global__ void __launch_bounds__(32 * kRowsWarps)
+    slp_bwd_rows_kernel(const Elt* __restrict__ x, int64_t N, int64_t V, int64_t ld,
+                        const int32_t* __restrict__ t, const uint8_t* __restrict__ mask,
+                        float invT, float c, const float* __restrict__ lse,
+                        const float* __restrict__ g, const float* __restrict__ H,
+                        const float* __restrict__ gH, Elt* __restrict__ gx, int64_t ldg,
+                        int32_t* __restrict__ err) {
+  using E = Elem<Elt>;
+  constexpr int kVec = E::kVec;
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kRowsWarps + (threadIdx.x >> 5);
+  if (row >= N) return;
+  const int64_t nvec = V / kVec;
+  Elt* gr = gx + row * ldg;
+  uint4* gv = reinterpret_cast<uint4*>(gr);
+  if (mask != nullptr && mask[row] == 0) {
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    for (int64_t i = lane; i < nvec; i += 32) st_stream(gv + i, z);
+    for (int64_t e = nvec * kVec + lane; e < V; e += 32) E::store1(gr + e, 0.f);
+    return;
+  }
+  const Elt* xr = x + row * ld;
+  const uint4* xv = reinterpret_cast<const uint4*>(xr);
+  BwdRow<Elt, kEnt> b;
+  b.init(row, V, t, invT, c, lse, g, H, gH, err, lane == 0);
+  for (int64_t i0 = lane; i0 < nvec; i0 += 32 * kRowsUnroll) {
+    uint4 v[kRowsUnroll];
+#pragma unroll
+    for (int u = 0; u < kRowsUnroll; ++u) {
+      const int64_t i = i0 + 32 * u;
+      if (i < nvec) v[u] = ld_stream(xv + i);
+    }
+#pragma unroll
+    for (int u = 0; u < kRowsUnroll; ++u) {
+      const int64_t i = i0 + 32 * u;
+      if (i < nvec) {
+        st_stream(gv + i, b.vec(v[u]));
+        const int64_t e = i * kVec;
+        if (b.tt >= e && b.tt < e + kVec) E::store1(gr + b.tt, b.one(E::load1(xr + b.tt), c, true));
       }
-      E::store1(gr + e, out);
     }
   }
+  for (int64_t e = nvec * kVec + lane; e < V; e += 32)  // fewer than kVec trailing elements
+    E::store1(gr + e, b.one(E::load1(xr + e), c, e == b.tt));
 }
 
 
@@ -825,6 +882,18 @@ cudaError_t fwd_typed(const Elt* x, int64_t N, int64_t V, int64_t ld, const int3
                             lse, entropy, err, splits);
 }
 
+// Rows of at most 64 KB that fill less than 90 % of their tiles of the
+// backward's (row, tile) grid (16 KB tiles) take one warp per row.  Measured
+// (bf16, N = 65536, TB/s, warp per row against the tile grid): 8 KB rows 6.78
+// against 5.11, 12 KB 6.78 / 6.07, 20 KB 6.80 / 5.86, 40 KB 6.80 / 6.52; with
+// full tiles the grid is ahead (16 KB 6.80 / 6.78 is a tie, 48 KB 6.67 / 6.87
+// and 64 KB 6.60 / 6.92 at N = 16384).
+constexpr bool use_bwd_rows_kernel(int64_t N, int64_t row_bytes) {
+  constexpr int64_t kTileBytes = static_cast<int64_t>(kBwdThreads) * kBwdUnroll * 16;
+  const int64_t tiles = (row_bytes + kTileBytes - 1) / kTileBytes;
+  return N > 0 && row_bytes <= 64 * 1024 && row_bytes * 10 < tiles * kTileBytes * 9;
+}
+
 template <typename Elt, bool kEnt>
 cudaError_t bwd_typed(const Elt* x, int64_t N, int64_t V, int64_t ld, const int32_t* t,
                       const uint8_t* mask, float T, const float* lse, const float* g,
@@ -838,6 +907,12 @@ cudaError_t bwd_typed(const Elt* x, int64_t N, int64_t V, int64_t ld, const int3
   const float invT = 1.0f / T;
   const float c = static_cast<float>(1.4426950408889634 / static_cast<double>(T));
   const bool vec = aligned16(x, ld, sizeof(Elt)) && aligned16(gx, ldg, sizeof(Elt));
+  if (vec && use_bwd_rows_kernel(N, V * static_cast<int64_t>(sizeof(Elt)))) {
+    const int64_t rblocks = (N + kRowsWarps - 1) / kRowsWarps;
+    slp_bwd_rows_kernel<Elt, kEnt><<<static_cast<unsigned>(rblocks), 32 * kRowsWarps, 0, stream>>>(
+        x, N, V, ld, t, mask, invT, c, lse, g, H, gH, gx, ldg, err);
+    return cudaGetLastError();
+  }
   if (vec)
     slp_bwd_kernel<Elt, true, kEnt><<<static_cast<unsigned>(blocks), kBwdThreads, 0, stream>>>(
         x, V, ld, t, mask, invT, c, lse, g, H, gH, gx, ldg, err, tiles);
