@@ -207,6 +207,21 @@ def test_deterministic():
                            v.view(torch.int16) if v.dtype == torch.bfloat16 else v.view(torch.int32))
 
 
+def test_deterministic_full_size():
+    """Forward and backward twice at full size (c151k), bit-identical: every
+    row's ring of bulk copies is reused 4-5 times per row."""
+    dev = device()
+    a = W.make_logits_inputs("c151k", device=dev)
+    lp1, lse1 = slp.slp_forward(a.x, a.t, a.mask, a.T)
+    lp2, lse2 = slp.slp_forward(a.x, a.t, a.mask, a.T)
+    gx1 = slp.slp_backward(a.x, a.t, a.mask, a.T, lse1, a.g)
+    gx2 = slp.slp_backward(a.x, a.t, a.mask, a.T, lse1, a.g)
+    torch.cuda.synchronize()
+    assert torch.equal(lp1.view(torch.int32), lp2.view(torch.int32))
+    assert torch.equal(lse1.view(torch.int32), lse2.view(torch.int32))
+    assert torch.equal(gx1.view(torch.int16), gx2.view(torch.int16))
+
+
 def test_empty_and_degenerate():
     dev = device()
     # N = 0

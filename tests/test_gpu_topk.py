@@ -43,7 +43,10 @@ def run(a, clamp):
     return kl, sm, tm, lse, gx
 
 
-CASES = [(192, 2048, 32), (64, 20016, 128), (33, 2047, 16), (40, 151936, 64)]
+# (192, 2048, 32) and (64, 20016, 128) take the warp-per-row backward, the
+# others one CTA per row (unaligned rows, a 297 KB row, K above 256).
+CASES = [(192, 2048, 32), (64, 20016, 128), (33, 2047, 16), (40, 151936, 64),
+         (24, 4096, 300)]
 
 
 @pytest.mark.parametrize("N,V,K", CASES, ids=lambda v: str(v))
@@ -92,3 +95,39 @@ def test_topk_bad_id_flagged():
     assert int(err.item()) & 1
     assert np.isnan(float(kl[2])) and bool(torch.isnan(gx[2].float()).all())
     check(a, kl, sm, tm, lse, gx, [0, 1, 3, 4, 5, 6, 7], -10.0)
+
+
+def test_topk_short_rows_ragged_tail():
+    """Warp-per-row backward on rows whose V is not a multiple of 8 (16-byte
+    aligned stride): ids in the scalar tail, repeated ids from the wrap, and
+    grad_x's padding columns left untouched."""
+    dev = device()
+    V, Vp = 4101, 4104
+    a = W.make_topk_inputs(device=dev, N=40, V=Vp, K=32)
+    a.x = a.x[:, :V]
+    a.ids = a.ids % V
+    a.ids[:, 0] = V - 1
+    a.ids[:, 1] = V - 4
+    kl, sm, tm, lse = slp.slp_topk_kl_forward(a.x, a.ids, a.lt, None, a.T, -10.0)
+    gx = torch.full((40, Vp), 7.0, dtype=torch.bfloat16, device=dev)
+    slp.slp_topk_kl_backward(a.x, a.ids, a.lt, None, a.T, -10.0, lse, a.g, grad_x=gx[:, :V])
+    torch.cuda.synchronize()
+    assert bool((gx[:, V:] == 7.0).all())
+    check(a, kl, sm, tm, lse, gx[:, :V], range(40), -10.0)
+
+
+def test_topk_backward_deterministic_full_size():
+    """Three backward runs at full size are bit-identical.  Guards the ring of
+    the CTA-per-row kernel: each thread fences its shared-memory reads of a
+    stage against the bulk copy that refills it (without the fence a read
+    still queued behind the kernel's own stores could return the next
+    chunk's bytes in a few rows per run)."""
+    dev = device()
+    a = W.make_topk_inputs(device=dev)
+    kl, sm, tm, lse = slp.slp_topk_kl_forward(a.x, a.ids, a.lt, a.mask, a.T, a.clamp)
+    first = slp.slp_topk_kl_backward(a.x, a.ids, a.lt, a.mask, a.T, a.clamp, lse, a.g)
+    for _ in range(2):
+        again = slp.slp_topk_kl_backward(a.x, a.ids, a.lt, a.mask, a.T, a.clamp, lse, a.g)
+        torch.cuda.synchronize()
+        assert torch.equal(first.view(torch.int16), again.view(torch.int16))
+        del again

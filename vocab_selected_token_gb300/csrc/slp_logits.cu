@@ -129,6 +129,7 @@ __global__ void __launch_bounds__(kFwdThreads)
         const int i = u * kFwdThreads + threadIdx.x;
         vv[u] = i < nv ? q[i] : pad;
       }
+      sm100::fence_proxy_async_smem();  // these reads precede the refill below
       __syncthreads();  // stage s fully read: thread 0 may refill it
       if (threadIdx.x == 0 && ch + kFwdStages < nch) issue(ch + kFwdStages);
       if constexpr (kEnt)

@@ -81,6 +81,14 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   }
 }
 
+// Orders this thread's earlier generic-proxy accesses to shared memory before
+// later async-proxy accesses (a bulk copy into the same bytes) that follow a
+// CTA barrier.  Without it a shared-memory load still queued when the barrier
+// completes may observe a refill that the barrier was meant to precede.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ---- TMA ------------------------------------------------------------------
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int32_t c0, int32_t c1,

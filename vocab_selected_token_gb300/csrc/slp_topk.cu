@@ -199,6 +199,7 @@ __global__ void __launch_bounds__(kTkThreads)
         const int i = u * kTkThreads + threadIdx.x;
         if (i < nv) vv[u] = q[i];
       }
+      sm100::fence_proxy_async_smem();  // these reads precede the refill below
       __syncthreads();  // stage read: refill it while this chunk is written
       if (threadIdx.x == 0 && ch + kTkStages < nch) issue(ch + kTkStages);
 #pragma unroll
@@ -244,9 +245,145 @@ __global__ void __launch_bounds__(kTkThreads)
   }
 }
 
+// Short rows: the backward with one warp per row.  A CTA per row spends
+// longer on its set-up (ring barriers, the K-entry table, CTA barriers) than
+// on a row of a few KB.  Each warp keeps its row's K teacher entries (id,
+// kept p) in its own slot of shared memory, padded to K4 = K rounded up to 4
+// with id -2, streams the dense part with 16-byte loads (kTkRowsUnroll per
+// lane in flight), then rewrites the elements that carry teacher entries as
+// the CTA kernel does (same sums in the same order).  The search for other
+// entries with the same id, K^2 / 32 steps per lane, reads the table four
+// ids at a time.
+constexpr int kTkRowsWarps = 8;
+constexpr int kTkRowsUnroll = 8;
+constexpr int kTkRowsMaxK = 256;  // 2 KB of entries per warp
+
+template <typename Elt>
+__global__ void __launch_bounds__(32 * kTkRowsWarps)
+    slp_topk_kl_bwd_rows_kernel(const Elt* __restrict__ x, int64_t N, int64_t V, int64_t ld,
+                                const int32_t* __restrict__ ids, const float* __restrict__ lt,
+                                int K, const uint8_t* __restrict__ mask, float invT, float c,
+                                float clamp_min, const float* __restrict__ lse,
+                                const float* __restrict__ g, Elt* __restrict__ gx, int64_t ldg,
+                                int32_t* __restrict__ err) {
+  using E = Elem<Elt>;
+  constexpr int kVec = E::kVec;
+  extern __shared__ __align__(16) int tk_rows_smem[];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kTkRowsWarps + w;
+  if (row >= N) return;
+  const Elt* xr = x + row * ld;
+  Elt* gr = gx + row * ldg;
+  uint4* gv = reinterpret_cast<uint4*>(gr);
+  const int64_t nvec = V / kVec;
+  if (mask != nullptr && mask[row] == 0) {
+    for (int64_t i = lane; i < nvec; i += 32) st_stream(gv + i, make_uint4(0, 0, 0, 0));
+    for (int64_t e = nvec * kVec + lane; e < V; e += 32) E::store1(gr + e, 0.f);
+    return;
+  }
+  const int K4 = (K + 3) & ~3;
+  int* sid = tk_rows_smem + static_cast<int64_t>(w) * 2 * K4;
+  float* sp = reinterpret_cast<float*>(sid + K4);
+  for (int k = K + lane; k < K4; k += 32) {
+    sid[k] = -2;
+    sp[k] = 0.f;
+  }
+  // the first batch of the dense pass is loaded before the entries are
+  // gathered, so its latency overlaps the gather's dependent loads
+  const uint4* xv = reinterpret_cast<const uint4*>(xr);
+  uint4 v[kTkRowsUnroll];
+#pragma unroll
+  for (int u = 0; u < kTkRowsUnroll; ++u) {
+    const int64_t i = lane + 32 * u;
+    if (i < nvec) v[u] = ld_stream(xv + i);
+  }
+  const float L = lse[row];
+  const float L2 = L * kLog2e;
+  float gT = g[row] * invT;
+  float pl = 0.f;
+  bool bad = false;
+  for (int k = lane; k < K; k += 32) {
+    const int id = ids[row * K + k];
+    float p = 0.f;
+    if (id < 0 || static_cast<int64_t>(id) >= V) {
+      bad = true;
+      sid[k] = -1;
+    } else {
+      const float ls = fmaf(E::load1(xr + id), invT, -L);
+      p = ls >= clamp_min ? expf(lt[row * K + k]) : 0.f;
+      sid[k] = id;
+    }
+    sp[k] = p;
+    pl += p;
+  }
+  const float P = warp_sum(pl);  // every lane holds the same sum
+  if (__any_sync(0xFFFFFFFFu, bad)) {
+    if (lane == 0 && err != nullptr) atomicOr(err, SLP_DATA_ERR_TARGET);
+    gT = __int_as_float(0x7FC00000);
+  }
+  const float dense = gT * P;
+
+  // pass 1: the dense part g/T P q[v] for every element
+  const Elt* tag = nullptr;
+  const float2 cc = make_float2(c, c);
+  const float no1 = log2f(fabsf(dense)) - L2;
+  const float2 no = make_float2(no1, no1);
+  const uint32_t sgn = sign_mask(dense, tag);
+  for (int64_t i0 = lane; i0 < nvec; i0 += 32 * kTkRowsUnroll) {
+    if (i0 > lane) {
+#pragma unroll
+      for (int u = 0; u < kTkRowsUnroll; ++u) {
+        const int64_t i = i0 + 32 * u;
+        if (i < nvec) v[u] = ld_stream(xv + i);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kTkRowsUnroll; ++u) {
+      const int64_t i = i0 + 32 * u;
+      if (i < nvec) st_stream(gv + i, scaled_exp2_vec(v[u], cc, no, sgn, tag));
+    }
+  }
+  for (int64_t e = nvec * kVec + lane; e < V; e += 32)
+    E::store1(gr + e, dense * ex2(fmaf(E::load1(xr + e), c, -L2)));
+
+  // pass 2 as in the CTA kernel; the fence and the warp barrier order every
+  // lane's pass-1 stores before the rewrites, and make the table visible
+  __threadfence_block();
+  __syncwarp();
+  const int4* sid4 = reinterpret_cast<const int4*>(sid);
+  for (int k = lane; k < K; k += 32) {
+    const int id = sid[k];
+    if (id < 0) continue;
+    bool first = true;
+    float tot = 0.f;
+    for (int j4 = 0; j4 < K4 / 4; ++j4) {
+      const int4 q = sid4[j4];
+      if (q.x == id || q.y == id || q.z == id || q.w == id) {  // the entry itself, or a repeat
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const int j = 4 * j4 + jj;
+          if (sid[j] == id) {
+            if (j < k) first = false;
+            tot += sp[j];
+          }
+        }
+      }
+    }
+    if (first) {
+      const float q = ex2(fmaf(E::load1(xr + id), c, -L2));
+      E::store1(gr + id, gT * fmaf(P, q, -tot));
+    }
+  }
+}
+
 bool aligned16(const void* p, int64_t ld, int esize) {
   return (reinterpret_cast<uintptr_t>(p) & 15u) == 0 && ((ld * esize) & 15) == 0;
 }
+
+// Measured (bf16, N = 32768, warp per row against CTA per row): 2 KB rows
+// 39 against 261 us, 8 KB 120 / 344 us, 16 KB 265 / 439 us, 32 KB 507 /
+// 517 us; 64 KB rows 906 / 722 us.
+constexpr bool use_topk_rows_kernel(int64_t row_bytes) { return row_bytes <= 32 * 1024; }
 
 template <typename Elt>
 cudaError_t topk_bwd_typed(const Elt* x, int64_t N, int64_t V, int64_t ld, const int32_t* ids,
@@ -258,6 +395,14 @@ cudaError_t topk_bwd_typed(const Elt* x, int64_t N, int64_t V, int64_t ld, const
   const float invT = 1.0f / T;
   const float c = static_cast<float>(1.4426950408889634 / static_cast<double>(T));
   const bool vec = aligned16(x, ld, sizeof(Elt)) && aligned16(gx, ldg, sizeof(Elt));
+  if (vec && K <= kTkRowsMaxK && use_topk_rows_kernel(V * static_cast<int64_t>(sizeof(Elt)))) {
+    const int64_t blocks = (N + kTkRowsWarps - 1) / kTkRowsWarps;
+    const size_t smem = static_cast<size_t>(kTkRowsWarps) * ((K + 3) & ~3) * 8;
+    slp_topk_kl_bwd_rows_kernel<Elt><<<static_cast<unsigned>(blocks), 32 * kTkRowsWarps, smem,
+                                       stream>>>(x, N, V, ld, ids, lt, K, mask, invT, c,
+                                                 clamp_min, lse, g, gx, ldg, err);
+    return cudaGetLastError();
+  }
   auto k = vec ? slp_topk_kl_bwd_kernel<Elt, true> : slp_topk_kl_bwd_kernel<Elt, false>;
   const int64_t smem = vec ? tables + kTkRing : tables;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
