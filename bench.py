@@ -436,9 +436,54 @@ def other_workloads(device, hbm):
         del inp, r
         torch.cuda.empty_cache()
     out["fused_fwd_bwd"] = time_fused(device, hbm)
+    out["short_rows"] = time_short_rows(device, hbm)
     out["entropy"] = time_entropy(device, hbm)
     out["topk_kl"] = time_topk(device, hbm)
     out["lmhead"] = time_lmhead(device)
+    return out
+
+
+def time_short_rows(device, hbm, steps=30, warmup=3):
+    """Small vocabularies (c151k recipe at V = 4096 and 32768, 1 GB of bf16
+    logits each): the separate forward + backward step and the fused call.
+    Rows of a few KB run on the warp-per-row kernels."""
+    import vocab_selected_token_gb300 as slp
+    from vocab_selected_token_gb300 import workloads as W
+    out = {}
+    s = torch.cuda.current_stream(device)
+    for V, N in ((4096, 131072), (32768, 16384)):
+        inp = W.make_logits_inputs("c151k", device=device, N=N, V=V)
+        nb = N * V * inp.x.element_size()
+        lp = torch.empty(N, device=device)
+        lse = torch.empty(N, device=device)
+        gx = torch.empty_like(inp.x)
+
+        def sep():
+            slp.slp_forward(inp.x, inp.t, None, inp.T, logprob=lp, lse=lse)
+            slp.slp_backward(inp.x, inp.t, None, inp.T, lse, inp.g, grad_x=gx)
+
+        def fused():
+            slp.slp_forward_backward(inp.x, inp.t, None, inp.T, inp.g, logprob=lp, lse=lse,
+                                     grad_x=gx)
+
+        res = {"N": N, "V": V}
+        for key, fn, passes in (("step", sep, 3), ("fused", fused, 2)):
+            for _ in range(warmup):
+                fn()
+            torch.cuda.synchronize(device)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            for _ in range(steps):
+                fn()
+            e1.record(s)
+            torch.cuda.synchronize(device)
+            ms = e0.elapsed_time(e1) / steps
+            gbs = passes * nb / (ms * 1e-3) / 1e9
+            res[key] = {"ms": ms, "tokens_per_s": N * 1000.0 / ms, "gbs": gbs,
+                        "frac_of_measured": gbs / hbm}
+        out[f"V{V}"] = res
+        del inp, gx
+        torch.cuda.empty_cache()
     return out
 
 
