@@ -426,6 +426,25 @@ def test_fused_forward_backward_bad_target():
     check_rows(a.x, t, None, 1.0, a.g, lp, lse, gx, [0, 1, 3, 4, 5, 6, 7])
 
 
+def test_fused_short_rows_bad_target():
+    """A bad target on the warp-per-row fused kernel: the error bit, NaN
+    logprob, lse and gradient for that row, the other rows exact to the
+    oracle."""
+    dev = device()
+    a = W.make_logits_inputs("c151k", device=dev, N=40, V=8192)
+    t = a.t.clone()
+    t[5] = 8192
+    t[17] = -3
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    lp, lse, gx = slp.slp_forward_backward(a.x, t, None, 1.0, a.g, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & 1
+    for r in (5, 17):
+        assert np.isnan(float(lp[r])) and bool(torch.isnan(gx[r].float()).all())
+    good = [i for i in range(40) if i not in (5, 17)]
+    check_rows(a.x, t, None, 1.0, a.g, lp, lse, gx, good)
+
+
 def test_fused_forward_backward_ragged_tail():
     """V not a multiple of 8 with a 16-byte-aligned stride: the cluster path's
     scalar tail, and grad_x's padding columns left untouched."""

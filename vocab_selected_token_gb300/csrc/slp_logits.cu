@@ -16,6 +16,14 @@
 // Backward: a flat grid of (row, column-tile) CTAs; each thread handles
 // kBwdUnroll 16-byte vectors, recomputes p = 2^(x*c - lse*log2 e) and writes
 // g/T * (1[v == t] - p) with streaming stores.  Inactive rows only write zeros.
+//
+// Fused forward + backward (the upstream gradient known at forward time): a
+// cluster of CTAs holds each row on chip between the two passes, so the row
+// is read from HBM once.
+//
+// Short rows (a few KB, small vocabularies) take kernels with one warp per
+// row instead, for the forward, the backward and the fused call: one CTA per
+// row spends more on its set-up than on such a row's traffic.
 
 #include "slp.h"
 #include "slp_device.cuh"

@@ -15,7 +15,8 @@
 // row streams the row once through a bulk-copy ring, writing the dense part
 // g/T P q[v] everywhere; then the K elements that carry teacher entries are
 // rewritten in full (recomputed in fp32 and rounded once), so the streaming
-// pass stays a plain elementwise pass.
+// pass stays a plain elementwise pass.  Rows of at most 32 KB (with K <= 256)
+// take the same backward with one warp per row.
 
 #include "slp.h"
 #include "slp_device.cuh"
