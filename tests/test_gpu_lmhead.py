@@ -142,6 +142,18 @@ def test_deterministic():
         assert torch.equal(u, v)
 
 
+def test_deterministic_full_size():
+    """Forward and backward twice on the full lmhead workload (3 vocabulary
+    chunks, split-K dh folded in order), bit-identical."""
+    dev = device()
+    a = W.make_lmhead_inputs(device=dev)
+    r1 = run_fwd_bwd(a)
+    r2 = run_fwd_bwd(a)
+    for u, v in zip(r1, r2):
+        assert torch.equal(u.view(torch.int16) if u.dtype == torch.bfloat16 else u.view(torch.int32),
+                           v.view(torch.int16) if v.dtype == torch.bfloat16 else v.view(torch.int32))
+
+
 def test_autograd():
     dev = device()
     a = W.make_lmhead_inputs(device=dev, N=128, V=2000, d=128)

@@ -352,6 +352,19 @@ def test_fused_forward_backward_full_size(name):
         assert bool((gx[off].view(torch.int16) == 0).all())
 
 
+def test_fused_forward_backward_deterministic_full_size():
+    """The fused call twice on c151k at full size (clusters of 4 CTAs per row,
+    merged through distributed shared memory), bit-identical."""
+    dev = device()
+    a = W.make_logits_inputs("c151k", device=dev)
+    r1 = slp.slp_forward_backward(a.x, a.t, a.mask, a.T, a.g)
+    r2 = slp.slp_forward_backward(a.x, a.t, a.mask, a.T, a.g)
+    torch.cuda.synchronize()
+    assert torch.equal(r1[0].view(torch.int32), r2[0].view(torch.int32))
+    assert torch.equal(r1[1].view(torch.int32), r2[1].view(torch.int32))
+    assert torch.equal(r1[2].view(torch.int16), r2[2].view(torch.int16))
+
+
 @pytest.mark.parametrize("V", [400008, 420000])
 def test_fused_forward_backward_long_rows(V):
     """Rows longer than one cluster holds (8 x 96 KB) take the separate
