@@ -62,3 +62,31 @@ def test_reference_arm_other_ranks_print_nothing(capsys):
         config, rows, steps, warmup, gpus = "tiny", 8, 1, 0, 2
     bench.run_reference(A, 2, 1)      # rank 1 of 2: exits without work
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_rank0_line(capsys):
+    """Rank 0 of the reference arm prints one JSON line: the oracle on every
+    host core, with the contract's keys."""
+    import json
+    sys.path.insert(0, ROOT)
+    import bench
+
+    class A:
+        config, rows, steps, warmup, gpus = "tiny", 64, 1, 0, 1
+    bench.run_reference(A, 1, 0)
+    out = capsys.readouterr().out.strip().splitlines()
+    assert len(out) == 1
+    d = json.loads(out[0])
+    assert d["impl"] == "reference" and d["value"] > 0 and d["higher_is_better"] is True
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_cpu_baseline_all_cores_runs_every_thread():
+    sys.path.insert(0, ROOT)
+    import bench
+    from vocab_selected_token_gb300 import workloads as W
+    inp = W.make_logits_inputs("tiny", device="cpu", N=64)
+    v, rows, secs, cores = bench.oracle_rows_per_second_all_cores(inp, 0.2, rows_per_thread=4)
+    assert cores >= 1 and rows >= 4 * cores and v > 0 and secs >= 0.2
