@@ -458,6 +458,40 @@ def test_fused_short_rows_bad_target():
     check_rows(a.x, t, None, 1.0, a.g, lp, lse, gx, good)
 
 
+@pytest.mark.parametrize("V,dtype", [(1, torch.bfloat16), (3, torch.bfloat16), (7, torch.bfloat16),
+                                     (1, torch.float32), (3, torch.float32)])
+def test_rows_shorter_than_one_vector(V, dtype):
+    """Rows of fewer elements than one 16-byte vector on an aligned stride:
+    every warp-per-row kernel runs its scalar tail only (forward, backward,
+    fused, entropy); the padding columns stay untouched."""
+    dev = device()
+    ld = 16 // (2 if dtype == torch.bfloat16 else 4)
+    N = 50
+    gen = torch.Generator(device=dev).manual_seed(5)
+    full = (torch.randn((N, ld), generator=gen, device=dev) * 3).to(dtype)
+    x = full[:, :V]
+    t = torch.randint(0, V, (N,), generator=gen, device=dev, dtype=torch.int32)
+    g = torch.rand(N, generator=gen, device=dev) * 2 - 1
+    mask = (torch.arange(N, device=dev) % 4 != 1).to(torch.uint8)
+    for T in (1.0, 0.6):
+        gx = torch.full((N, ld), 7.0, dtype=dtype, device=dev)
+        lp, lse = slp.slp_forward(x, t, mask, T)
+        slp.slp_backward(x, t, mask, T, lse, g, grad_x=gx[:, :V])
+        gxf = torch.full((N, ld), 7.0, dtype=dtype, device=dev)
+        lpf, lsef, _ = slp.slp_forward_backward(x, t, mask, T, g, grad_x=gxf[:, :V])
+        lpe, lsee, H = slp.slp_forward_entropy(x, t, mask, T)
+        torch.cuda.synchronize()
+        assert bool((gx[:, V:] == 7.0).all()) and bool((gxf[:, V:] == 7.0).all())
+        # the fp32 lse floor: at V = 1 the exact gradient is 0 and 1 - p is
+        # one ulp of |x/T| + |lse| (x here reaches ~10)
+        check_rows(x, t, mask, T, g, lp, lse, gx[:, :V], range(N), fp32_floor=True)
+        check_rows(x, t, mask, T, g, lpf, lsef, gxf[:, :V], range(N), fp32_floor=True)
+        assert float((lpe - lp).abs().max()) <= TOL_LP
+        if V == 1:
+            act = mask != 0
+            assert bool((lp[act].abs() <= TOL_LP).all()) and bool((H[act].abs() <= 1e-5).all())
+
+
 def test_fused_forward_backward_ragged_tail():
     """V not a multiple of 8 with a 16-byte-aligned stride: the cluster path's
     scalar tail, and grad_x's padding columns left untouched."""
