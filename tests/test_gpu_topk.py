@@ -131,3 +131,20 @@ def test_topk_backward_deterministic_full_size():
         torch.cuda.synchronize()
         assert torch.equal(first.view(torch.int16), again.view(torch.int16))
         del again
+
+
+def test_topk_rows_shorter_than_one_vector():
+    """V = 7 on a 16-byte stride (bf16): the warp-per-row backward runs its
+    scalar tail only; K = 3 with a repeated id in half of the rows."""
+    dev = device()
+    a = W.make_topk_inputs(device=dev, N=30, V=8, K=3)
+    V = 7
+    a.x = a.x[:, :V]
+    a.ids = a.ids % V
+    a.ids[::2, 2] = a.ids[::2, 0]
+    kl, sm, tm, lse = slp.slp_topk_kl_forward(a.x, a.ids, a.lt, None, a.T, -10.0)
+    gx = torch.full((30, 8), 7.0, dtype=torch.bfloat16, device=dev)
+    slp.slp_topk_kl_backward(a.x, a.ids, a.lt, None, a.T, -10.0, lse, a.g, grad_x=gx[:, :V])
+    torch.cuda.synchronize()
+    assert bool((gx[:, V:] == 7.0).all())
+    check(a, kl, sm, tm, lse, gx[:, :V], range(30), -10.0)
