@@ -584,11 +584,29 @@ def time_entropy(device, hbm, steps=30, warmup=3):
     e1.record(s)
     torch.cuda.synchronize(device)
     ms = e0.elapsed_time(e1) / steps
+
+    def fused():
+        slp.slp_forward_backward_entropy(inp.x, inp.t, None, inp.T, inp.g, gH, logprob=lp,
+                                         lse=lse, entropy=H, grad_x=gx)
+
+    for _ in range(warmup):
+        fused()
+    torch.cuda.synchronize(device)
+    e0.record(s)
+    for _ in range(steps):
+        fused()
+    e1.record(s)
+    torch.cuda.synchronize(device)
+    ms_f = e0.elapsed_time(e1) / steps
+    fb = 2 * N * V * inp.x.element_size()  # one read of the logits, one write of the gradient
     del inp, gx
     torch.cuda.empty_cache()
     return {"workload": "c151k", "ms_per_step": ms, "tokens_per_s": N * 1000.0 / ms,
             "gbs": (fwd_b + bwd_b) / (ms * 1e-3) / 1e9,
-            "frac_of_measured": (fwd_b + bwd_b) / (ms * 1e-3) / 1e9 / hbm}
+            "frac_of_measured": (fwd_b + bwd_b) / (ms * 1e-3) / 1e9 / hbm,
+            "fused": {"ms_per_step": ms_f, "tokens_per_s": N * 1000.0 / ms_f,
+                      "algorithmic_bytes": fb, "gbs": fb / (ms_f * 1e-3) / 1e9,
+                      "frac_of_measured": fb / (ms_f * 1e-3) / 1e9 / hbm}}
 
 
 def time_topk(device, hbm, steps=20, warmup=3):

@@ -235,6 +235,32 @@ int slp_forward_backward(const void* x, int dtype, int64_t N, int64_t V, int64_t
                          void* grad_x, int64_t ld_grad, int32_t* err, void* stream);
 
 /*
+ * slp_forward_backward_entropy - slp_forward_entropy and slp_backward_entropy
+ * in one pass, for a loss whose per-token weights are known when the forward
+ * runs: sum_n g[n] logprob[n] + gH[n] H[n] (for example a policy-gradient
+ * term with an entropy bonus, gH = -beta).
+ *
+ * Defined by: the two entropy calls above (same definitions, same results
+ * within their tolerances).  The row is kept on chip as in
+ * slp_forward_backward, so it is read from HBM once instead of twice.  The
+ * gradient is computed from the lse and entropy this call writes, with the
+ * same per-element arithmetic as slp_backward_entropy.  Rows that are not
+ * 16-byte aligned, or longer than 8 x 96 KB, are served by
+ * slp_forward_entropy followed by slp_backward_entropy.
+ *
+ *   x, dtype, N, V, ld, t, mask, T   as for slp_forward.
+ *   grad_out, grad_entropy  [N] float32 upstream gradients of logprob and of
+ *                  the entropy; either may be NULL, meaning zero.
+ *   logprob, lse, entropy  [N] float32 out, as from slp_forward_entropy.
+ *   grad_x, ld_grad, err, stream     as for slp_backward.
+ */
+int slp_forward_backward_entropy(const void* x, int dtype, int64_t N, int64_t V, int64_t ld,
+                                 const int32_t* t, const uint8_t* mask, float T,
+                                 const float* grad_out, const float* grad_entropy, float* logprob,
+                                 float* lse, float* entropy, void* grad_x, int64_t ld_grad,
+                                 int32_t* err, void* stream);
+
+/*
  * slp_forward_backward_host - slp_forward_backward for logits that live in
  * pinned host memory (for example after an offload), streamed through the GPU
  * in row chunks.  No counterpart in the pages: it only moves the rows of the

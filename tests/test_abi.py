@@ -83,6 +83,19 @@ def test_backward_argument_errors(lib):
                             None) == _lib.SLP_OK
 
 
+def test_forward_backward_entropy_argument_errors(lib):
+    f = lib.slp_forward_backward_entropy
+    # (x, dtype, N, V, ld, t, mask, T, g, gH, lp, lse, H, gx, ld_grad, err, stream)
+    assert f(FAKE, 0, 4, 10, 10, FAKE, None, 1.0, None, None, FAKE, FAKE, FAKE, FAKE, 9, None,
+             None) == _lib.SLP_ERR_INVALID_ARG                                  # ld_grad < V
+    assert f(FAKE, 0, 4, 10, 10, FAKE, None, 1.0, None, None, FAKE, FAKE, None, FAKE, 10, None,
+             None) == _lib.SLP_ERR_INVALID_ARG                                  # no entropy out
+    assert f(FAKE, 0, 4, 10, 10, FAKE, None, -1.0, None, None, FAKE, FAKE, FAKE, FAKE, 10, None,
+             None) == _lib.SLP_ERR_INVALID_ARG                                  # T <= 0
+    assert f(None, 1, 0, 10, 10, None, None, 1.0, None, None, None, None, None, None, 10, None,
+             None) == _lib.SLP_OK                                               # N = 0: no-op
+
+
 def test_lmhead_argument_errors(lib):
     N, V, d = 64, 1000, 128
     need_b = lib.slp_lmhead_workspace_size(N, V, d)

@@ -106,3 +106,85 @@ def test_entropy_autograd():
     ref = slp.slp_backward_entropy(a.x, a.t, None, a.T, lse, H2, a.g, gH)
     torch.cuda.synchronize()
     assert torch.equal(x.grad, ref)
+
+
+# ---- fused forward + backward with the entropy (slp_forward_backward_entropy) ----
+
+FB_ENT = [
+    ("tiny", None, None),          # 4 KB rows: one warp per row
+    ("packed", 90, 600),           # short rows with masked spans
+    ("stability", 40, 3000),       # fp32 short rows
+    ("c151k", 48, 151936),         # cluster of 4 CTAs per row
+    ("packed", 300, 20016),        # 40 KB rows: cluster
+    ("stability", 256, 131072),    # fp32, rows with -inf columns
+    ("tiny", 300, 2047),           # unaligned rows: the separate kernels
+]
+
+
+@pytest.mark.parametrize("name,N,V", FB_ENT, ids=lambda v: str(v))
+def test_fused_entropy_all_rows(name, N, V):
+    dev = device()
+    a = W.make_logits_inputs(name, device=dev, N=N, V=V)
+    gH = torch.rand(a.x.shape[0], device=dev) * 2 - 1
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    lp, lse, H, gx = slp.slp_forward_backward_entropy(a.x, a.t, a.mask, a.T, a.g, gH, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    check_entropy_rows(a, gH, lp, lse, H, gx, range(a.x.shape[0]))
+    if a.mask is not None:
+        off = a.mask == 0
+        zero = gx[off].view(torch.int16 if gx.dtype == torch.bfloat16 else torch.int32) == 0
+        assert bool((H[off] == 0).all()) and bool(zero.all())
+
+
+def test_fused_entropy_full_size():
+    """c151k at full size: sampled rows against the oracle, and every row's
+    logprob, lse and entropy against the separate entropy forward."""
+    dev = device()
+    a = W.make_logits_inputs("c151k", device=dev)
+    N = a.x.shape[0]
+    gH = torch.rand(N, device=dev) * 2 - 1
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    lp, lse, H, gx = slp.slp_forward_backward_entropy(a.x, a.t, a.mask, a.T, a.g, gH, err=err)
+    lp2, lse2, H2 = slp.slp_forward_entropy(a.x, a.t, a.mask, a.T)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    rows = set(np.random.default_rng(41).choice(N, 20, replace=False).tolist()) | {0, N - 1}
+    check_entropy_rows(a, gH, lp, lse, H, gx, rows)
+    assert float((lp - lp2).abs().max()) <= TOL_LP and float((lse - lse2).abs().max()) <= TOL_LP
+    assert float((H - H2).abs().max()) <= 5e-5 + 1e-5 * float(H2.abs().max())
+
+
+@pytest.mark.parametrize("V", [4096, 151936])
+def test_fused_entropy_null_weights(V):
+    """grad_entropy = NULL leaves the plain gradient; grad_out = NULL leaves
+    only the entropy term (both against the oracle)."""
+    dev = device()
+    a = W.make_logits_inputs("c151k", device=dev, N=40, V=V)
+    lp, lse, H, gx = slp.slp_forward_backward_entropy(a.x, a.t, None, 1.0, a.g, None)
+    torch.cuda.synchronize()
+    check_entropy_rows(a, torch.zeros_like(a.g), lp, lse, H, gx, range(40))
+    gH = torch.rand(40, device=dev)
+    lp, lse, H, gx = slp.slp_forward_backward_entropy(a.x, a.t, None, 1.0, None, gH)
+    torch.cuda.synchronize()
+    a.g = torch.zeros_like(a.g)
+    check_entropy_rows(a, gH, lp, lse, H, gx, range(40))
+
+
+@pytest.mark.parametrize("V", [8192, 151936])
+def test_fused_entropy_bad_target(V):
+    dev = device()
+    a = W.make_logits_inputs("c151k", device=dev, N=24, V=V)
+    t = a.t.clone()
+    t[3] = V
+    t[11] = -2
+    a.t = t
+    gH = torch.rand(24, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    lp, lse, H, gx = slp.slp_forward_backward_entropy(a.x, t, None, 1.0, a.g, gH, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & 1
+    for r in (3, 11):
+        assert np.isnan(float(lp[r])) and np.isnan(float(H[r]))
+        assert bool(torch.isnan(gx[r].float()).all())
+    check_entropy_rows(a, gH, lp, lse, H, gx, [i for i in range(24) if i not in (3, 11)])

@@ -25,7 +25,8 @@ from ._lib import SlpError
 
 __all__ = [
     "SlpError", "slp_forward", "slp_backward", "slp_forward_backward",
-    "slp_forward_entropy", "slp_backward_entropy", "selected_logprob_and_entropy",
+    "slp_forward_entropy", "slp_backward_entropy", "slp_forward_backward_entropy",
+    "selected_logprob_and_entropy",
     "slp_topk_kl_forward", "slp_topk_kl_backward",
     "slp_lmhead_workspace_size",
     "slp_lmhead_forward_workspace_size", "slp_lmhead_forward_noalloc",
@@ -255,6 +256,36 @@ def slp_forward_backward(x, t, mask, T: float, grad_out, logprob=None, lse=None,
               float(T), _ptr(grad_out), _ptr(logprob), _ptr(lse), _ptr(grad_x), ldg, _ptr(err),
               _stream_handle(stream))
     return logprob, lse, grad_x
+
+
+def slp_forward_backward_entropy(x, t, mask, T: float, grad_out=None, grad_entropy=None,
+                                 logprob=None, lse=None, entropy=None, grad_x=None, err=None,
+                                 stream=None):
+    """Forward with the entropy and the gradient of sum(g * logprob + gH *
+    entropy) in one pass, for weights known at forward time (either may be
+    None, meaning zero).  Returns (logprob, lse, entropy, grad_x)."""
+    N, V, ld = _logits_layout(x)
+    _check_vec("t", t, N, torch.int32)
+    if mask is not None:
+        _check_vec("mask", mask, N, torch.uint8)
+    for name, v in (("grad_out", grad_out), ("grad_entropy", grad_entropy)):
+        if v is not None:
+            _check_vec(name, v, N, torch.float32)
+    out = []
+    for v in (logprob, lse, entropy):
+        v = torch.empty(N, dtype=torch.float32, device=x.device) if v is None else v
+        _check_vec("output", v, N, torch.float32)
+        out.append(v)
+    if grad_x is None:
+        grad_x = torch.empty((N, V), dtype=x.dtype, device=x.device)
+    if grad_x.shape != (N, V) or grad_x.dtype != x.dtype or (N > 0 and V > 0 and grad_x.stride(1) != 1):
+        raise ValueError("grad_x must be [N, V] with x's dtype and unit column stride")
+    ldg = grad_x.stride(0) if N > 1 else max(V, 1)
+    _check_disjoint("grad_x", grad_x, x)
+    _lib.call("slp_forward_backward_entropy", _ptr(x), _DTYPES[x.dtype], N, V, ld, _ptr(t),
+              _ptr(mask), float(T), _ptr(grad_out), _ptr(grad_entropy), _ptr(out[0]),
+              _ptr(out[1]), _ptr(out[2]), _ptr(grad_x), ldg, _ptr(err), _stream_handle(stream))
+    return out[0], out[1], out[2], grad_x
 
 
 def slp_lmhead_workspace_size(N: int, V: int, d: int) -> int:

@@ -41,6 +41,8 @@ SIGNATURES = {
                                     _vp, _vp, _vp, _i64, _vp, _vp]),
     "slp_forward_backward": (_int, [_vp, _int, _i64, _i64, _i64, _vp, _vp, _f32, _vp, _vp, _vp,
                                     _vp, _i64, _vp, _vp]),
+    "slp_forward_backward_entropy": (_int, [_vp, _int, _i64, _i64, _i64, _vp, _vp, _f32, _vp,
+                                            _vp, _vp, _vp, _vp, _vp, _i64, _vp, _vp]),
     "slp_forward_backward_host_workspace_size": (_sz, [_i64, _i64, _int, _i64]),
     "slp_forward_backward_host": (_int, [_vp, _int, _i64, _i64, _i64, _vp, _vp, _f32, _vp, _vp,
                                          _vp, _vp, _i64, _i64, _vp, _sz, _vp, _vp]),

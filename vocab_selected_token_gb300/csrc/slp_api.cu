@@ -156,6 +156,22 @@ int slp_forward_backward(const void* x, int dtype, int64_t N, int64_t V, int64_t
                                                   static_cast<cudaStream_t>(stream)));
 }
 
+int slp_forward_backward_entropy(const void* x, int dtype, int64_t N, int64_t V, int64_t ld,
+                                 const int32_t* t, const uint8_t* mask, float T,
+                                 const float* grad_out, const float* grad_entropy, float* logprob,
+                                 float* lse, float* entropy, void* grad_x, int64_t ld_grad,
+                                 int32_t* err, void* stream) {
+  int st = check_logits_args(x, dtype, N, V, ld, t, T);
+  if (st != SLP_OK) return st;
+  if (ld_grad < V) return SLP_ERR_INVALID_ARG;
+  if (N == 0) return SLP_OK;
+  if (logprob == nullptr || lse == nullptr || entropy == nullptr || grad_x == nullptr)
+    return SLP_ERR_INVALID_ARG;
+  return cuda_status(slp::launch_forward_backward_entropy(
+      x, dtype, N, V, ld, t, mask, T, grad_out, grad_entropy, logprob, lse, entropy, grad_x,
+      ld_grad, err, static_cast<cudaStream_t>(stream)));
+}
+
 size_t slp_forward_backward_host_workspace_size(int64_t N, int64_t V, int dtype,
                                                 int64_t rows_per_chunk) {
   if (N < 0 || V <= 0 || V > INT32_MAX || (dtype != SLP_BF16 && dtype != SLP_F32)) return 0;

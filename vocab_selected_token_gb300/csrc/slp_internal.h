@@ -39,6 +39,13 @@ cudaError_t launch_forward_backward(const void* x, int dtype, int64_t N, int64_t
                                     void* grad_x, int64_t ld_grad, int32_t* err,
                                     cudaStream_t stream);
 
+cudaError_t launch_forward_backward_entropy(const void* x, int dtype, int64_t N, int64_t V,
+                                            int64_t ld, const int32_t* t, const uint8_t* mask,
+                                            float T, const float* grad_out,
+                                            const float* grad_entropy, float* logprob, float* lse,
+                                            float* entropy, void* grad_x, int64_t ld_grad,
+                                            int32_t* err, cudaStream_t stream);
+
 // Host-resident logits streamed through slp_forward_backward (slp_host.cu).
 size_t forward_backward_host_workspace_size(int64_t N, int64_t V, int esize,
                                             int64_t rows_per_chunk);

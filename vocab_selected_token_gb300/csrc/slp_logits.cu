@@ -33,6 +33,7 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
+#include <type_traits>
 
 namespace slp {
 
@@ -321,20 +322,28 @@ struct BwdRow {
   __device__ __forceinline__ void init(int64_t row, int64_t V, const int32_t* t, float invT,
                                        float c, const float* lse, const float* g, const float* H,
                                        const float* gH, int32_t* err, bool report) {
-    const Elt* tag = nullptr;
-    tt = t[row];
-    gT = (kEnt && g == nullptr) ? 0.f : g[row] * invT;
-    L2 = lse[row] * kLog2e;
-    float gHT = 0.f;
-    Hl2 = 0.f;
+    const int64_t t0 = t[row];
+    float gT0 = (kEnt && g == nullptr) ? 0.f : g[row] * invT;
+    float gHT = 0.f, Hl20 = 0.f;
     if (kEnt) {
       gHT = gH == nullptr ? 0.f : gH[row] * invT;
-      Hl2 = H[row] * kLog2e;  // log p_v + H = ln 2 (log2 p_v + H log2 e)
+      Hl20 = H[row] * kLog2e;  // log p_v + H = ln 2 (log2 p_v + H log2 e)
     }
-    if (tt < 0 || tt >= V) {
+    if (t0 < 0 || t0 >= V) {
       if (err != nullptr && report) atomicOr(err, SLP_DATA_ERR_TARGET);
-      gT = __int_as_float(0x7FC00000);
+      gT0 = __int_as_float(0x7FC00000);
     }
+    set(t0, gT0, lse[row] * kLog2e, gHT, Hl20, c);
+  }
+  // From the row's values: gT0 = g/T (NaN for a bad target), L20 = lse log2 e,
+  // gHT = gH/T, Hl20 = H log2 e (the last two unused without kEnt).
+  __device__ __forceinline__ void set(int64_t t0, float gT0, float L20, float gHT, float Hl20,
+                                      float c) {
+    const Elt* tag = nullptr;
+    tt = t0;
+    gT = gT0;
+    L2 = L20;
+    Hl2 = kEnt ? Hl20 : 0.f;
     a = -gT;
     gHl = -gHT * kLn2;
     cc = make_float2(c, c);
@@ -501,20 +510,27 @@ constexpr int kFbRV = 5;
 constexpr int kFbRegSeg = 233472 / 4 - 1024 - 256 + kFbRV * kFbThreads * 16;
 constexpr int kFbMaxCluster = 8;
 
-template <typename Elt, int kRV>
+// kEnt adds the entropy: the state carries the entropy accumulator, the row
+// results include H (`entropy`), and the gradient gains the entropy term
+// -gH p (log p + H) / T computed from the lse and H written here, exactly as
+// slp_bwd_kernel computes it from the saved ones (g and gH may then be NULL,
+// meaning zero).
+template <typename Elt, int kRV, bool kEnt>
 __global__ void __launch_bounds__(kFbThreads, kRV > 0 ? 4 : 1)
     slp_fwd_bwd_kernel(const Elt* __restrict__ x, int64_t V, int64_t ld,
                        const int32_t* __restrict__ t, const uint8_t* __restrict__ mask, float T,
                        float c, float invT, const float* __restrict__ g,
-                       float* __restrict__ logprob, float* __restrict__ lse,
+                       const float* __restrict__ gH, float* __restrict__ logprob,
+                       float* __restrict__ lse, float* __restrict__ entropy,
                        Elt* __restrict__ gx, int64_t ldg, int32_t* __restrict__ err, int C) {
   using E = Elem<Elt>;
+  using St = typename std::conditional<kEnt, Lse3, Lse2>::type;
   constexpr int kVec = E::kVec;
   constexpr int kWarps = kFbThreads / 32;
   extern __shared__ __align__(128) uint8_t seg[];
   __shared__ __align__(8) uint64_t full[kFbMaxChunks];
-  __shared__ Lse2 warp_part[kWarps];
-  __shared__ float cta_part[3];
+  __shared__ St warp_part[kWarps];
+  __shared__ float cta_part[4];
   __shared__ int abort_flag;
 
   const int64_t row = blockIdx.x / C;
@@ -541,6 +557,7 @@ __global__ void __launch_bounds__(kFbThreads, kRV > 0 ? 4 : 1)
     if (rank == 0 && threadIdx.x == 0) {
       logprob[row] = 0.f;
       lse[row] = 0.f;
+      if (kEnt) entropy[row] = 0.f;
     }
     return;
   }
@@ -550,7 +567,8 @@ __global__ void __launch_bounds__(kFbThreads, kRV > 0 ? 4 : 1)
   const bool tvalid = tt >= 0 && static_cast<int64_t>(tt) < V;
   float xt = 0.f;
   if (rank == 0 && threadIdx.x == 0 && tvalid) xt = E::load1(xr + tt);
-  const float gT = tvalid ? g[row] * invT : __int_as_float(0x7FC00000);
+  const float gT = tvalid ? ((kEnt && g == nullptr) ? 0.f : g[row] * invT)
+                          : __int_as_float(0x7FC00000);
 
   const int seg_bytes = nv_s * 16;
   const int nch = (seg_bytes + kFbChunk - 1) / kFbChunk;
@@ -585,7 +603,8 @@ __global__ void __launch_bounds__(kFbThreads, kRV > 0 ? 4 : 1)
   }
 
   // pass 1: online log-sum-exp over the segment as its chunks land
-  Lse2 st = lse2_empty();
+  St st;
+  st_empty(st);
   const uint4* q = reinterpret_cast<const uint4*>(seg);
   constexpr int kPer = kFbChunk / 16 / kFbThreads;
   bool ok = true;
@@ -602,10 +621,18 @@ __global__ void __launch_bounds__(kFbThreads, kRV > 0 ? 4 : 1)
       const int i = k * (kFbChunk / 16) + u * kFbThreads + threadIdx.x;
       vv[u] = i < nv_s ? q[i] : pad;
     }
-    lse2_fold_vec<kPer>(st, vv, c, tag);
+    if constexpr (kEnt)
+      lse3_fold_vec<kPer>(st, vv, c, tag);
+    else
+      lse2_fold_vec<kPer>(st, vv, c, tag);
   }
   ok = !__syncthreads_or(!ok);
-  if constexpr (kRV > 0) lse2_fold_vec<kRV>(st, rv, c, tag);
+  if constexpr (kRV > 0) {
+    if constexpr (kEnt)
+      lse3_fold_vec<kRV>(st, rv, c, tag);
+    else
+      lse2_fold_vec<kRV>(st, rv, c, tag);
+  }
   if (!ok && threadIdx.x == 0) {
     if (err != nullptr) atomicOr(err, SLP_DEVICE_ERR_TIMEOUT);
     for (int k = 0; k < nch; ++k)  // let every copy land before the CTA moves on
@@ -615,54 +642,101 @@ __global__ void __launch_bounds__(kFbThreads, kRV > 0 ? 4 : 1)
     const int64_t e = nvec * kVec + threadIdx.x;
     if (e < V) {
       float f1[1] = {E::load1(xr + e)};
-      lse2_fold<1>(st, f1, c);
+      st_fold<1>(st, f1, c);
     }
   }
 
   // CTA merge, then cluster merge (every CTA reads all partials)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  st = lse2_warp_reduce(st);
+  st = st_warp_reduce(st);
   if (lane == 0) warp_part[warp] = st;
   __syncthreads();
   if (warp == 0) {
-    Lse2 v = lane < kWarps ? warp_part[lane] : lse2_empty();
-    v = lse2_warp_reduce(v);
+    St v;
+    if (lane < kWarps)
+      v = warp_part[lane];
+    else
+      st_empty(v);
+    v = st_warp_reduce(v);
     if (lane == 0) {
       cta_part[0] = v.m;
       cta_part[1] = v.mc;
       cta_part[2] = v.s;
+      if constexpr (kEnt) cta_part[3] = v.w;
     }
   }
   cluster_sync_from_thread0();  // thread 0 wrote cta_part
-  __shared__ Lse2 row_state;
+  __shared__ St row_state;
   if (warp == 0) {
     // lane r fetches rank r's partial (the C remote reads overlap), then
     // every lane merges them in rank order
-    Lse2 o = lse2_empty();
+    St o;
+    st_empty(o);
     if (lane < C) {
       const uint32_t b = map_shared_rank(&cta_part[0], lane);
       o.m = ld_shared_cluster_f32(b);
       o.mc = ld_shared_cluster_f32(b + 4);
       o.s = ld_shared_cluster_f32(b + 8);
+      if constexpr (kEnt) o.w = ld_shared_cluster_f32(b + 12);
     }
-    Lse2 acc = lse2_empty();
+    St acc;
+    st_empty(acc);
     for (int r = 0; r < C; ++r) {
-      Lse2 pr;
+      St pr;
       pr.m = __shfl_sync(0xFFFFFFFFu, o.m, r);
       pr.mc = __shfl_sync(0xFFFFFFFFu, o.mc, r);
       pr.s = __shfl_sync(0xFFFFFFFFu, o.s, r);
-      acc = lse2_merge(acc, pr);
+      if constexpr (kEnt) pr.w = __shfl_sync(0xFFFFFFFFu, o.w, r);
+      acc = st_merge(acc, pr);
     }
     if (lane == 0) {
       row_state = acc;
-      if (rank == 0) write_row_result(acc, xt, tvalid, T, c, logprob, lse, err, row);
+      if (rank == 0) {
+        if constexpr (kEnt)
+          write_row_result(acc, xt, tvalid, T, c, logprob, lse, entropy, err, row);
+        else
+          write_row_result(acc, xt, tvalid, T, c, logprob, lse, err, row);
+      }
     }
   }
   // no CTA may leave before the others have read its partial: arrive now
   // (relaxed: the reads above have returned their values), wait at the end
   asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
   __syncthreads();
-  const Lse2 rs = row_state;
+  const St rs = row_state;
+  if constexpr (kEnt) {
+    // the entropy gradient from the lse and H just written (the same
+    // expressions as write_row_result), as slp_bwd_kernel takes them
+    float L20 = __int_as_float(0x7FC00000), Hl20 = L20;
+    if (rs.m != -INFINITY && rs.s > 0.f) {
+      const float l = rs.m / T + (log2f(rs.s) - fmaf(rs.m, c, -rs.mc)) * kLn2;
+      const float H = (log2f(rs.s) - rs.w / rs.s) * kLn2;
+      L20 = l * kLog2e;
+      Hl20 = H * kLog2e;
+    }
+    BwdRow<Elt, true> b;
+    b.set(tt, gT, L20, gH != nullptr ? gH[row] * invT : 0.f, Hl20, c);
+    const int64_t rel0 = static_cast<int64_t>(tt) - v0 * kVec;  // target offset in segment
+    const int64_t tvec = rel0 >= 0 ? rel0 / kVec : -1;
+    Elt* gr = gx + row * ldg;
+    auto put = [&](int i, const uint4& v) {
+      st_stream(gv + i, b.vec(v));
+      if (i == tvec) E::store1(gr + tt, b.one(E::load1(xr + tt), c, true));
+    };
+    for (int i = threadIdx.x; i < nv_s; i += kFbThreads) put(i, q[i]);
+    if constexpr (kRV > 0) {
+#pragma unroll
+      for (int u = 0; u < kRV; ++u) {
+        const int i = nv_s + u * kFbThreads + threadIdx.x;
+        if (i < nv) put(i, rv[u]);
+      }
+    }
+    if (rank == C - 1)
+      for (int64_t e = nvec * kVec + threadIdx.x; e < V; e += kFbThreads)
+        E::store1(gr + e, b.one(E::load1(xr + e), c, e == tt));
+    asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+    return;
+  }
 
   // pass 2: gradient from shared memory.  p = 2^(x*c - off), off = mc + log2 s;
   // a p = sign(a) 2^(x*c - off + log2 |a|) (scaled_exp2_vec), the target's
@@ -716,15 +790,19 @@ constexpr int kFbRowsMaxNV = 16;                // register vectors per lane (8 
 constexpr int kFbRowsMaxSlot = 24 * 1024;       // shared-memory part per warp
 constexpr int kFbRowsMaxBytes = kFbRowsMaxNV * 32 * 16 + kFbRowsMaxSlot;  // 32 KB rows
 
-template <typename Elt, int kNV>
-__global__ void __launch_bounds__(32 * kFbRowsWarps, kNV >= 16 ? 4 : 8)
+// kEnt: with the entropy, as in slp_fwd_bwd_kernel (its 8-vector form needs
+// more than 64 registers, so six CTAs per SM instead of eight).
+template <typename Elt, int kNV, bool kEnt>
+__global__ void __launch_bounds__(32 * kFbRowsWarps, kNV >= 16 ? 4 : (kEnt && kNV >= 8 ? 6 : 8))
     slp_fwd_bwd_rows_kernel(const Elt* __restrict__ x, int64_t N, int64_t V, int64_t ld,
                             const int32_t* __restrict__ t, const uint8_t* __restrict__ mask,
                             float T, float c, float invT, const float* __restrict__ g,
-                            float* __restrict__ logprob, float* __restrict__ lse,
+                            const float* __restrict__ gH, float* __restrict__ logprob,
+                            float* __restrict__ lse, float* __restrict__ entropy,
                             Elt* __restrict__ gx, int64_t ldg, int32_t* __restrict__ err,
                             int slot_bytes) {
   using E = Elem<Elt>;
+  using St = typename std::conditional<kEnt, Lse3, Lse2>::type;
   constexpr int kVec = E::kVec;
   extern __shared__ __align__(128) uint8_t slots[];
   __shared__ __align__(8) uint64_t full[kFbRowsWarps];
@@ -741,6 +819,7 @@ __global__ void __launch_bounds__(32 * kFbRowsWarps, kNV >= 16 ? 4 : 8)
     if (lane == 0) {
       logprob[row] = 0.f;
       lse[row] = 0.f;
+      if (kEnt) entropy[row] = 0.f;
     }
     return;
   }
@@ -761,7 +840,8 @@ __global__ void __launch_bounds__(32 * kFbRowsWarps, kNV >= 16 ? 4 : 8)
   }
   const int32_t tt = t[row];
   const bool tvalid = tt >= 0 && static_cast<int64_t>(tt) < V;
-  const float gT = tvalid ? g[row] * invT : __int_as_float(0x7FC00000);
+  const float gT = tvalid ? ((kEnt && g == nullptr) ? 0.f : g[row] * invT)
+                          : __int_as_float(0x7FC00000);
   const uint4 pad = make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord, E::kNegInfWord);
   uint4 rv[kNV];
 #pragma unroll
@@ -770,8 +850,12 @@ __global__ void __launch_bounds__(32 * kFbRowsWarps, kNV >= 16 ? 4 : 8)
     rv[u] = i < nreg ? ld_stream(xv + i) : pad;
   }
   const Elt* tag = nullptr;
-  Lse2 st = lse2_empty();
-  lse2_fold_vec<kNV>(st, rv, c, tag);
+  St st;
+  st_empty(st);
+  if constexpr (kEnt)
+    lse3_fold_vec<kNV>(st, rv, c, tag);
+  else
+    lse2_fold_vec<kNV>(st, rv, c, tag);
   const uint4* q = reinterpret_cast<const uint4*>(slots + w * slot_bytes);
   if (ns > 0) {
     bool ok = sm100::mbar_wait_bounded(bar, 0, nullptr, kFwdWaitNs);
@@ -788,17 +872,50 @@ __global__ void __launch_bounds__(32 * kFbRowsWarps, kNV >= 16 ? 4 : 8)
         const int i = i0 + 32 * u;
         vv[u] = i < ns ? q[i] : pad;
       }
-      lse2_fold_vec<kPer>(st, vv, c, tag);
+      if constexpr (kEnt)
+        lse3_fold_vec<kPer>(st, vv, c, tag);
+      else
+        lse2_fold_vec<kPer>(st, vv, c, tag);
     }
   }
   for (int64_t e = nvec * kVec + lane; e < V; e += 32) {  // fewer than kVec trailing elements
     float f1[1] = {E::load1(xr + e)};
-    lse2_fold<1>(st, f1, c);
+    st_fold<1>(st, f1, c);
   }
-  st = lse2_warp_reduce(st);
+  st = st_warp_reduce(st);  // every lane holds the same state
   if (lane == 0) {
     const float xt = tvalid ? E::load1(xr + tt) : 0.f;
-    write_row_result(st, xt, tvalid, T, c, logprob, lse, err, row);
+    if constexpr (kEnt)
+      write_row_result(st, xt, tvalid, T, c, logprob, lse, entropy, err, row);
+    else
+      write_row_result(st, xt, tvalid, T, c, logprob, lse, err, row);
+  }
+  if constexpr (kEnt) {
+    // the entropy gradient from the lse and H just written, as in
+    // slp_fwd_bwd_kernel
+    float L20 = __int_as_float(0x7FC00000), Hl20 = L20;
+    if (st.m != -INFINITY && st.s > 0.f) {
+      const float l = st.m / T + (log2f(st.s) - fmaf(st.m, c, -st.mc)) * kLn2;
+      const float H = (log2f(st.s) - st.w / st.s) * kLn2;
+      L20 = l * kLog2e;
+      Hl20 = H * kLog2e;
+    }
+    BwdRow<Elt, true> b;
+    b.set(tt, gT, L20, gH != nullptr ? gH[row] * invT : 0.f, Hl20, c);
+    const int64_t tvec = tvalid ? static_cast<int64_t>(tt) / kVec : -1;
+    auto put = [&](int64_t i, const uint4& v) {
+      st_stream(gv + i, b.vec(v));
+      if (i == tvec) E::store1(gr + tt, b.one(E::load1(xr + tt), c, true));
+    };
+#pragma unroll
+    for (int u = 0; u < kNV; ++u) {
+      const int i = u * 32 + lane;
+      if (i < nreg) put(i, rv[u]);
+    }
+    for (int i = lane; i < ns; i += 32) put(nreg + i, q[i]);
+    for (int64_t e = nvec * kVec + lane; e < V; e += 32)
+      E::store1(gr + e, b.one(E::load1(xr + e), c, e == tt));
+    return;
   }
 
   // gradient, as in the cluster kernel: a p = sign(a) 2^(x c - off + log2 |a|)
@@ -935,11 +1052,12 @@ __host__ __device__ constexpr bool use_fb_rows_kernel(int64_t N, int64_t row_byt
   return row_bytes <= kFbRowsMaxBytes && N > 0;
 }
 
-template <typename Elt, int kNV>
+// gH and entropy are used with kEnt only.
+template <typename Elt, int kNV, bool kEnt>
 cudaError_t fwd_bwd_rows_launch(const Elt* x, int64_t N, int64_t V, int64_t ld, const int32_t* t,
-                                const uint8_t* mask, float T, const float* g, float* logprob,
-                                float* lse, Elt* gx, int64_t ldg, int32_t* err,
-                                cudaStream_t stream) {
+                                const uint8_t* mask, float T, const float* g, const float* gH,
+                                float* logprob, float* lse, float* entropy, Elt* gx, int64_t ldg,
+                                int32_t* err, cudaStream_t stream) {
   constexpr int kVec = Elem<Elt>::kVec;
   const int64_t nvec = V / kVec;
   const int64_t ns = nvec > 32 * kNV ? nvec - 32 * kNV : 0;
@@ -947,7 +1065,7 @@ cudaError_t fwd_bwd_rows_launch(const Elt* x, int64_t N, int64_t V, int64_t ld, 
   if (slot_bytes > kFbRowsMaxSlot) return cudaErrorInvalidValue;
   const int smem = slot_bytes * kFbRowsWarps;
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(slp_fwd_bwd_rows_kernel<Elt, kNV>,
+    cudaError_t e = cudaFuncSetAttribute(slp_fwd_bwd_rows_kernel<Elt, kNV, kEnt>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kFbRowsMaxSlot * kFbRowsWarps);
     if (e != cudaSuccess) return e;
@@ -955,22 +1073,24 @@ cudaError_t fwd_bwd_rows_launch(const Elt* x, int64_t N, int64_t V, int64_t ld, 
   const int64_t blocks = (N + kFbRowsWarps - 1) / kFbRowsWarps;
   if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
   const float c = static_cast<float>(1.4426950408889634 / static_cast<double>(T));
-  slp_fwd_bwd_rows_kernel<Elt, kNV>
+  slp_fwd_bwd_rows_kernel<Elt, kNV, kEnt>
       <<<static_cast<unsigned>(blocks), 32 * kFbRowsWarps, smem, stream>>>(
-          x, N, V, ld, t, mask, T, c, 1.0f / T, g, logprob, lse, gx, ldg, err, slot_bytes);
+          x, N, V, ld, t, mask, T, c, 1.0f / T, g, gH, logprob, lse, entropy, gx, ldg, err,
+          slot_bytes);
   return cudaGetLastError();
 }
 
 // Register vectors per lane: the smallest power of two that holds the row,
 // at most kFbRowsMaxNV (the rest then goes to shared memory).
-template <typename Elt>
+template <typename Elt, bool kEnt>
 cudaError_t fwd_bwd_rows_typed(const Elt* x, int64_t N, int64_t V, int64_t ld, const int32_t* t,
-                               const uint8_t* mask, float T, const float* g, float* logprob,
-                               float* lse, Elt* gx, int64_t ldg, int32_t* err,
-                               cudaStream_t stream) {
+                               const uint8_t* mask, float T, const float* g, const float* gH,
+                               float* logprob, float* lse, float* entropy, Elt* gx, int64_t ldg,
+                               int32_t* err, cudaStream_t stream) {
   const int64_t per_lane = (V / Elem<Elt>::kVec + 31) / 32;
-#define SLP_FB_ROWS(NV) \
-  fwd_bwd_rows_launch<Elt, NV>(x, N, V, ld, t, mask, T, g, logprob, lse, gx, ldg, err, stream)
+#define SLP_FB_ROWS(NV)                                                                       \
+  fwd_bwd_rows_launch<Elt, NV, kEnt>(x, N, V, ld, t, mask, T, g, gH, logprob, lse, entropy, gx, \
+                                     ldg, err, stream)
   if (per_lane <= 1) return SLP_FB_ROWS(1);
   if (per_lane <= 2) return SLP_FB_ROWS(2);
   if (per_lane <= 4) return SLP_FB_ROWS(4);
@@ -981,17 +1101,20 @@ cudaError_t fwd_bwd_rows_typed(const Elt* x, int64_t N, int64_t V, int64_t ld, c
 
 // Fused forward + backward: needs 16-byte-aligned rows and rows short enough
 // to fit a cluster of at most 8 CTAs x 96 KB; returns cudaErrorNotSupported
-// otherwise (the caller then runs the separate kernels).
-template <typename Elt>
+// otherwise (the caller then runs the separate kernels).  gH and entropy are
+// used with kEnt only.
+template <typename Elt, bool kEnt>
 cudaError_t fwd_bwd_typed(const Elt* x, int64_t N, int64_t V, int64_t ld, const int32_t* t,
-                          const uint8_t* mask, float T, const float* g, float* logprob,
-                          float* lse, Elt* gx, int64_t ldg, int32_t* err, cudaStream_t stream) {
+                          const uint8_t* mask, float T, const float* g, const float* gH,
+                          float* logprob, float* lse, float* entropy, Elt* gx, int64_t ldg,
+                          int32_t* err, cudaStream_t stream) {
   constexpr int kVec = Elem<Elt>::kVec;
   if (!aligned16(x, ld, sizeof(Elt)) || !aligned16(gx, ldg, sizeof(Elt)))
     return cudaErrorNotSupported;
   const int64_t nvec = V / kVec;
   if (use_fb_rows_kernel(N, V * static_cast<int64_t>(sizeof(Elt))))
-    return fwd_bwd_rows_typed(x, N, V, ld, t, mask, T, g, logprob, lse, gx, ldg, err, stream);
+    return fwd_bwd_rows_typed<Elt, kEnt>(x, N, V, ld, t, mask, T, g, gH, logprob, lse, entropy,
+                                         gx, ldg, err, stream);
   // Segments of at most kFbRegSeg bytes (kFbRV vectors per thread in
   // registers, the rest in shared memory) keep four CTAs resident per SM.
   // Longer rows take up to kFbMaxSeg of shared memory per CTA (two per SM).
@@ -1004,7 +1127,7 @@ cudaError_t fwd_bwd_typed(const Elt* x, int64_t N, int64_t V, int64_t ld, const 
   const int64_t per = (nvec + C - 1) / C;  // vectors of the longest segment
   const int64_t in_smem = regs ? (per > kFbRV * kFbThreads ? per - kFbRV * kFbThreads : 0) : per;
   const int smem = static_cast<int>(in_smem * 16);
-  auto kern = regs ? slp_fwd_bwd_kernel<Elt, kFbRV> : slp_fwd_bwd_kernel<Elt, 0>;
+  auto kern = regs ? slp_fwd_bwd_kernel<Elt, kFbRV, kEnt> : slp_fwd_bwd_kernel<Elt, 0, kEnt>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kFbMaxSeg);
   if (e != cudaSuccess) return e;
   const float c = static_cast<float>(1.4426950408889634 / static_cast<double>(T));
@@ -1023,8 +1146,8 @@ cudaError_t fwd_bwd_typed(const Elt* x, int64_t N, int64_t V, int64_t ld, const 
   attr[1].val.clusterSchedulingPolicyPreference = cudaClusterSchedulingPolicyLoadBalancing;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, x, V, ld, t, mask, T, c, invT, g, logprob, lse, gx, ldg,
-                            err, static_cast<int>(C));
+  return cudaLaunchKernelEx(&cfg, kern, x, V, ld, t, mask, T, c, invT, g, gH, logprob, lse,
+                            entropy, gx, ldg, err, static_cast<int>(C));
 }
 
 }  // namespace
@@ -1091,17 +1214,44 @@ cudaError_t launch_forward_backward(const void* x, int dtype, int64_t N, int64_t
                                     cudaStream_t stream) {
   cudaError_t e;
   if (dtype == SLP_BF16)
-    e = fwd_bwd_typed(static_cast<const __nv_bfloat16*>(x), N, V, ld, t, mask, T, grad_out,
-                      logprob, lse, static_cast<__nv_bfloat16*>(grad_x), ld_grad, err, stream);
+    e = fwd_bwd_typed<__nv_bfloat16, false>(static_cast<const __nv_bfloat16*>(x), N, V, ld, t,
+                                            mask, T, grad_out, nullptr, logprob, lse, nullptr,
+                                            static_cast<__nv_bfloat16*>(grad_x), ld_grad, err,
+                                            stream);
   else
-    e = fwd_bwd_typed(static_cast<const float*>(x), N, V, ld, t, mask, T, grad_out, logprob, lse,
-                      static_cast<float*>(grad_x), ld_grad, err, stream);
+    e = fwd_bwd_typed<float, false>(static_cast<const float*>(x), N, V, ld, t, mask, T, grad_out,
+                                    nullptr, logprob, lse, nullptr, static_cast<float*>(grad_x),
+                                    ld_grad, err, stream);
   if (e != cudaErrorNotSupported) return e;
   // rows unaligned or too long for one cluster: the separate kernels
   e = launch_forward(x, dtype, N, V, ld, t, mask, T, logprob, lse, err, stream);
   if (e != cudaSuccess) return e;
   return launch_backward(x, dtype, N, V, ld, t, mask, T, lse, grad_out, grad_x, ld_grad, err,
                          stream);
+}
+
+cudaError_t launch_forward_backward_entropy(const void* x, int dtype, int64_t N, int64_t V,
+                                            int64_t ld, const int32_t* t, const uint8_t* mask,
+                                            float T, const float* grad_out,
+                                            const float* grad_entropy, float* logprob, float* lse,
+                                            float* entropy, void* grad_x, int64_t ld_grad,
+                                            int32_t* err, cudaStream_t stream) {
+  cudaError_t e;
+  if (dtype == SLP_BF16)
+    e = fwd_bwd_typed<__nv_bfloat16, true>(static_cast<const __nv_bfloat16*>(x), N, V, ld, t,
+                                           mask, T, grad_out, grad_entropy, logprob, lse, entropy,
+                                           static_cast<__nv_bfloat16*>(grad_x), ld_grad, err,
+                                           stream);
+  else
+    e = fwd_bwd_typed<float, true>(static_cast<const float*>(x), N, V, ld, t, mask, T, grad_out,
+                                   grad_entropy, logprob, lse, entropy,
+                                   static_cast<float*>(grad_x), ld_grad, err, stream);
+  if (e != cudaErrorNotSupported) return e;
+  // rows unaligned or too long for one cluster: the separate kernels
+  e = launch_forward_entropy(x, dtype, N, V, ld, t, mask, T, logprob, lse, entropy, err, stream);
+  if (e != cudaSuccess) return e;
+  return launch_backward_entropy(x, dtype, N, V, ld, t, mask, T, lse, entropy, grad_out,
+                                 grad_entropy, grad_x, ld_grad, err, stream);
 }
 
 }  // namespace slp
