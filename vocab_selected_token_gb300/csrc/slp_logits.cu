@@ -322,21 +322,35 @@ struct BwdRow {
   __device__ __forceinline__ void init(int64_t row, int64_t V, const int32_t* t, float invT,
                                        float c, const float* lse, const float* g, const float* H,
                                        const float* gH, int32_t* err, bool report) {
-    const int64_t t0 = t[row];
-    float gT0 = (kEnt && g == nullptr) ? 0.f : g[row] * invT;
-    float gHT = 0.f, Hl20 = 0.f;
+    const Elt* tag = nullptr;
+    tt = t[row];
+    gT = (kEnt && g == nullptr) ? 0.f : g[row] * invT;
+    L2 = lse[row] * kLog2e;
+    float gHT = 0.f;
+    Hl2 = 0.f;
     if (kEnt) {
       gHT = gH == nullptr ? 0.f : gH[row] * invT;
-      Hl20 = H[row] * kLog2e;  // log p_v + H = ln 2 (log2 p_v + H log2 e)
+      Hl2 = H[row] * kLog2e;  // log p_v + H = ln 2 (log2 p_v + H log2 e)
     }
-    if (t0 < 0 || t0 >= V) {
+    if (tt < 0 || tt >= V) {
       if (err != nullptr && report) atomicOr(err, SLP_DATA_ERR_TARGET);
-      gT0 = __int_as_float(0x7FC00000);
+      gT = __int_as_float(0x7FC00000);
     }
-    set(t0, gT0, lse[row] * kLog2e, gHT, Hl20, c);
+    a = -gT;
+    gHl = -gHT * kLn2;
+    cc = make_float2(c, c);
+    const float no1 = kEnt ? -L2 : log2f(fabsf(a)) - L2;  // -(L2 - log2 |a|) without entropy
+    no = make_float2(no1, no1);
+    sgn = sign_mask(a, tag);
+    gHl2 = make_float2(gHl, gHl);
+    const float a2s = fmaf(gHl, Hl2, a);
+    a2 = make_float2(a2s, a2s);
   }
-  // From the row's values: gT0 = g/T (NaN for a bad target), L20 = lse log2 e,
-  // gHT = gH/T, Hl20 = H log2 e (the last two unused without kEnt).
+  // The same terms from values already in registers (the fused kernels):
+  // gT0 = g/T (NaN for a bad target), L20 = lse log2 e, gHT = gH/T,
+  // Hl20 = H log2 e.  The derived terms repeat init's lines: routing init
+  // through this function instead changed the plain backward's schedule and
+  // cost it 2.5 % (353 -> 362 us on c151k).
   __device__ __forceinline__ void set(int64_t t0, float gT0, float L20, float gHT, float Hl20,
                                       float c) {
     const Elt* tag = nullptr;
@@ -347,7 +361,7 @@ struct BwdRow {
     a = -gT;
     gHl = -gHT * kLn2;
     cc = make_float2(c, c);
-    const float no1 = kEnt ? -L2 : log2f(fabsf(a)) - L2;  // -(L2 - log2 |a|) without entropy
+    const float no1 = kEnt ? -L2 : log2f(fabsf(a)) - L2;
     no = make_float2(no1, no1);
     sgn = sign_mask(a, tag);
     gHl2 = make_float2(gHl, gHl);
