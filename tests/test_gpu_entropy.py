@@ -171,6 +171,19 @@ def test_fused_entropy_null_weights(V):
     check_entropy_rows(a, gH, lp, lse, H, gx, range(40))
 
 
+def test_fused_entropy_96k_segments():
+    """~700 KB rows: the cluster kernel's shared-memory-only form with the
+    entropy."""
+    dev = device()
+    a = W.make_logits_inputs("tiny", device=dev, N=6, V=350000)
+    gH = torch.rand(6, device=dev) * 2 - 1
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    lp, lse, H, gx = slp.slp_forward_backward_entropy(a.x, a.t, None, a.T, a.g, gH, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    check_entropy_rows(a, gH, lp, lse, H, gx, range(6))
+
+
 @pytest.mark.parametrize("V", [8192, 151936])
 def test_fused_entropy_bad_target(V):
     dev = device()

@@ -365,6 +365,23 @@ def test_fused_forward_backward_deterministic_full_size():
     assert torch.equal(r1[2].view(torch.int16), r2[2].view(torch.int16))
 
 
+@pytest.mark.parametrize("V,Vp", [(350000, 350000), (349997, 350000)])
+def test_fused_forward_backward_96k_segments(V, Vp):
+    """Rows of ~700 KB: too long for eight register-tail segments, so the
+    cluster kernel runs its shared-memory-only form (eight 96 KB segments);
+    one case with a scalar tail on an aligned stride."""
+    dev = device()
+    a = W.make_logits_inputs("tiny", device=dev, N=6, V=Vp)
+    x = a.x[:, :V]
+    t = a.t % V
+    t[0] = V - 1
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    lp, lse, gx = slp.slp_forward_backward(x, t, None, a.T, a.g, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    check_rows(x, t, None, a.T, a.g, lp, lse, gx, range(6))
+
+
 @pytest.mark.parametrize("V", [400008, 420000])
 def test_fused_forward_backward_long_rows(V):
     """Rows longer than one cluster holds (8 x 96 KB) take the separate
