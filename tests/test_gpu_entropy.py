@@ -171,11 +171,12 @@ def test_fused_entropy_null_weights(V):
     check_entropy_rows(a, gH, lp, lse, H, gx, range(40))
 
 
-def test_fused_entropy_96k_segments():
-    """~700 KB rows: the cluster kernel's shared-memory-only form with the
-    entropy."""
+@pytest.mark.parametrize("name,V", [("tiny", 350000), ("stability", 175000)])
+def test_fused_entropy_96k_segments(name, V):
+    """~700 KB rows (bf16 and fp32): the cluster kernel's shared-memory-only
+    form with the entropy."""
     dev = device()
-    a = W.make_logits_inputs("tiny", device=dev, N=6, V=350000)
+    a = W.make_logits_inputs(name, device=dev, N=6, V=V)
     gH = torch.rand(6, device=dev) * 2 - 1
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     lp, lse, H, gx = slp.slp_forward_backward_entropy(a.x, a.t, None, a.T, a.g, gH, err=err)

@@ -365,13 +365,14 @@ def test_fused_forward_backward_deterministic_full_size():
     assert torch.equal(r1[2].view(torch.int16), r2[2].view(torch.int16))
 
 
-@pytest.mark.parametrize("V,Vp", [(350000, 350000), (349997, 350000)])
-def test_fused_forward_backward_96k_segments(V, Vp):
+@pytest.mark.parametrize("name,V,Vp", [("tiny", 350000, 350000), ("tiny", 349997, 350000),
+                                       ("stability", 175000, 175000)])
+def test_fused_forward_backward_96k_segments(name, V, Vp):
     """Rows of ~700 KB: too long for eight register-tail segments, so the
     cluster kernel runs its shared-memory-only form (eight 96 KB segments);
-    one case with a scalar tail on an aligned stride."""
+    one bf16 case with a scalar tail on an aligned stride, one fp32 case."""
     dev = device()
-    a = W.make_logits_inputs("tiny", device=dev, N=6, V=Vp)
+    a = W.make_logits_inputs(name, device=dev, N=6, V=Vp)
     x = a.x[:, :V]
     t = a.t % V
     t[0] = V - 1
