@@ -187,6 +187,24 @@ def test_binding_refuses_overlapping_outputs():
     slp._check_disjoint("dW", torch.zeros(3, 2), None, torch.zeros(5))
 
 
+def test_fused_entropy_binding_checks_before_the_library():
+    """slp_forward_backward_entropy's binding rejects bad outputs (overlap
+    with x, wrong shape or dtype) and bad vectors before any library call."""
+    import torch
+
+    import vocab_selected_token_gb300 as slp
+    x = torch.zeros(4, 8, dtype=torch.bfloat16)
+    t = torch.zeros(4, dtype=torch.int32)
+    with pytest.raises(ValueError):
+        slp.slp_forward_backward_entropy(x, t, None, 1.0, grad_x=x)
+    with pytest.raises(ValueError):
+        slp.slp_forward_backward_entropy(x, t, None, 1.0, grad_x=torch.zeros(4, 8))
+    with pytest.raises(ValueError):
+        slp.slp_forward_backward_entropy(x, t, None, 1.0, grad_out=torch.zeros(3))
+    with pytest.raises(ValueError):
+        slp.slp_forward_backward_entropy(x, t.long(), None, 1.0)
+
+
 def test_lmhead_workspace_size_max(lib):
     """The whole-vocabulary workspace is at least the default one, equal to it
     when the vocabulary fits one default chunk, and 0 for invalid sizes."""
