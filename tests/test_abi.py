@@ -187,7 +187,22 @@ def test_binding_refuses_overlapping_outputs():
     slp._check_disjoint("dW", torch.zeros(3, 2), None, torch.zeros(5))
 
 
-def test_fused_entropy_binding_checks_before_the_library():
+@pytest.fixture
+def no_library_call(monkeypatch):
+    """Makes any call into libslp fail the test: the binding's checks must
+    refuse bad tensors before the library sees a pointer."""
+    from vocab_selected_token_gb300 import _lib
+
+    def refuse(name, *args):
+        raise AssertionError(f"{name} reached the library")
+
+    monkeypatch.setattr(_lib, "call", refuse)
+
+
+CUDA_ONLY = "must be CUDA tensors"  # the last check: well-formed CPU tensors end there
+
+
+def test_fused_entropy_binding_checks_before_the_library(no_library_call):
     """slp_forward_backward_entropy's binding rejects bad outputs (overlap
     with x, wrong shape or dtype) and bad vectors before any library call."""
     import torch
@@ -195,14 +210,163 @@ def test_fused_entropy_binding_checks_before_the_library():
     import vocab_selected_token_gb300 as slp
     x = torch.zeros(4, 8, dtype=torch.bfloat16)
     t = torch.zeros(4, dtype=torch.int32)
-    with pytest.raises(ValueError):
+    with pytest.raises(ValueError, match="overlap"):
         slp.slp_forward_backward_entropy(x, t, None, 1.0, grad_x=x)
-    with pytest.raises(ValueError):
+    with pytest.raises(ValueError, match="grad_x must be"):
         slp.slp_forward_backward_entropy(x, t, None, 1.0, grad_x=torch.zeros(4, 8))
-    with pytest.raises(ValueError):
+    with pytest.raises(ValueError, match="grad_out"):
         slp.slp_forward_backward_entropy(x, t, None, 1.0, grad_out=torch.zeros(3))
-    with pytest.raises(ValueError):
+    with pytest.raises(ValueError, match="t must be"):
         slp.slp_forward_backward_entropy(x, t.long(), None, 1.0)
+    with pytest.raises(ValueError, match=CUDA_ONLY):
+        slp.slp_forward_backward_entropy(x, t, None, 1.0)
+
+
+def _bad_grad_x(x):
+    """grad_x tensors the library must never be handed for logits x [N, V]."""
+    import torch
+    N, V = x.shape
+    wide = torch.zeros(N, 2 * V, dtype=x.dtype)
+    return [
+        ("grad_x must be", torch.zeros(N, V + 1, dtype=x.dtype)),       # too many columns
+        ("grad_x must be", torch.zeros(N - 1, V, dtype=x.dtype)),       # too few rows
+        ("grad_x must be", torch.zeros(N, V, dtype=torch.float64)),     # wrong dtype
+        ("grad_x must be", torch.zeros(N * V, dtype=x.dtype)),          # wrong rank
+        ("unit column stride", wide[:, ::2]),                           # strided columns
+        ("must not overlap", torch.zeros(V, dtype=x.dtype).expand(N, V)),  # rows alias
+        ("overlap", x),                                                 # in place of x
+    ]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_logits_backward_bindings_check_grad_x_before_the_library(no_library_call, dtype):
+    """Every logits-path binding that takes a caller's grad_x checks its shape,
+    dtype, column stride, row stride and overlap with x before the call
+    (slp_backward, slp_backward_entropy, slp_topk_kl_backward,
+    slp_forward_backward, slp_forward_backward_entropy); a well-formed CPU
+    grad_x gets as far as the device check."""
+    import torch
+
+    import vocab_selected_token_gb300 as slp
+    N, V, K = 4, 8, 3
+    x = torch.zeros(N, V, dtype=torch.bfloat16 if dtype == "bf16" else torch.float32)
+    t = torch.zeros(N, dtype=torch.int32)
+    v = torch.zeros(N)
+    ids = torch.zeros(N, K, dtype=torch.int32)
+    lt = torch.zeros(N, K)
+    calls = {
+        "slp_backward": lambda gx: slp.slp_backward(x, t, None, 1.0, v, v, grad_x=gx),
+        "slp_backward_entropy": lambda gx: slp.slp_backward_entropy(x, t, None, 1.0, v, v, v, v,
+                                                                    grad_x=gx),
+        "slp_topk_kl_backward": lambda gx: slp.slp_topk_kl_backward(x, ids, lt, None, 1.0, -10.0,
+                                                                    v, v, grad_x=gx),
+        "slp_forward_backward": lambda gx: slp.slp_forward_backward(x, t, None, 1.0, v,
+                                                                    grad_x=gx),
+        "slp_forward_backward_entropy": lambda gx: slp.slp_forward_backward_entropy(
+            x, t, None, 1.0, v, v, grad_x=gx),
+    }
+    for name, call in calls.items():
+        for why, gx in _bad_grad_x(x):
+            with pytest.raises(ValueError, match=why):
+                call(gx)
+        with pytest.raises(ValueError, match=CUDA_ONLY):
+            call(torch.zeros(N, V, dtype=x.dtype))
+        with pytest.raises(ValueError, match=CUDA_ONLY):
+            call(torch.zeros(N, V + 5, dtype=x.dtype)[:, :V])  # padded rows are fine
+
+
+def test_lmhead_backward_bindings_check_outputs_before_the_library(no_library_call):
+    """slp_lmhead_backward checks dh [N, d] and dW [V, d] (bf16, contiguous,
+    disjoint from h, W and each other), slp_lmhead_backward_accumulate checks
+    dh and its float32 dW accumulator, and both check the workspace, before
+    the library is called."""
+    import torch
+
+    import vocab_selected_token_gb300 as slp
+    N, V, d = 4, 16, 64
+    h = torch.zeros(N, d, dtype=torch.bfloat16)
+    W = torch.zeros(V, d, dtype=torch.bfloat16)
+    t = torch.zeros(N, dtype=torch.int32)
+    v = torch.zeros(N)
+    dh_ok = torch.zeros(N, d, dtype=torch.bfloat16)
+    dW_ok = torch.zeros(V, d, dtype=torch.bfloat16)
+    ws = torch.zeros(slp.slp_lmhead_workspace_size(N, V, d), dtype=torch.uint8)
+
+    def bwd(dh=dh_ok, dW=dW_ok, ws=ws):
+        return slp.slp_lmhead_backward(h, W, t, None, 1.0, v, v, dh=dh, dW=dW, ws=ws)
+
+    bad_dh = [torch.zeros(N, d + 64, dtype=torch.bfloat16), torch.zeros(N + 1, d, dtype=torch.bfloat16),
+              torch.zeros(N, d), torch.zeros(N, 2 * d, dtype=torch.bfloat16)[:, ::2]]
+    bad_dW = [torch.zeros(V - 1, d, dtype=torch.bfloat16), torch.zeros(V, d),
+              torch.zeros(d, V, dtype=torch.bfloat16).t()]
+    for dh in bad_dh:
+        with pytest.raises(ValueError, match="dh must be"):
+            bwd(dh=dh)
+    for dW in bad_dW:
+        with pytest.raises(ValueError, match="dW must be"):
+            bwd(dW=dW)
+    with pytest.raises(ValueError, match="overlap"):
+        bwd(dW=W)
+    with pytest.raises(ValueError, match="overlap"):
+        bwd(dh=h)
+    with pytest.raises(ValueError, match="ws must be"):
+        bwd(ws=torch.zeros(2 * ws.numel(), dtype=torch.uint8)[::2])
+    with pytest.raises(ValueError, match=CUDA_ONLY):
+        bwd()
+
+    acc_ok = torch.zeros(V, d)
+
+    def acc(dW_accum=acc_ok, dh=dh_ok):
+        return slp.slp_lmhead_backward_accumulate(h, W, t, None, 1.0, v, v, dW_accum, dh=dh,
+                                                  ws=ws)
+
+    for bad in (torch.zeros(V, d, dtype=torch.bfloat16), torch.zeros(V + 1, d),
+                torch.zeros(d, V).t()):
+        with pytest.raises(ValueError, match="dW_accum must be"):
+            acc(dW_accum=bad)
+    for dh in bad_dh:
+        with pytest.raises(ValueError, match="dh must be"):
+            acc(dh=dh)
+    with pytest.raises(ValueError, match=CUDA_ONLY):
+        acc()
+
+
+def test_lmhead_workspace_bytes_count_the_element_size(monkeypatch):
+    """A caller's workspace is passed with its size in bytes, whatever its
+    dtype, and a non-contiguous one is refused (its numel would overstate the
+    memory the library may write)."""
+    import torch
+
+    import vocab_selected_token_gb300 as slp
+    monkeypatch.setattr(slp, "slp_lmhead_workspace_size", lambda N, V, d: 1)
+    ws, nbytes = slp._workspace(1, 1, 64, torch.zeros(100, dtype=torch.float32), None)
+    assert nbytes == 400
+    ws, nbytes = slp._workspace(1, 1, 64, torch.zeros(100, dtype=torch.uint8), None)
+    assert nbytes == 100
+    with pytest.raises(ValueError, match="ws must be"):
+        slp._workspace(1, 1, 64, torch.zeros(10, 10, dtype=torch.uint8)[:, :5], None)
+
+
+def test_error_word_and_device_checks(no_library_call):
+    """The error word must be an int32 tensor; CPU tensors never reach the
+    library (the no-allocation forward included)."""
+    import torch
+
+    import vocab_selected_token_gb300 as slp
+    N, V, d = 4, 16, 64
+    x = torch.zeros(N, V)
+    t = torch.zeros(N, dtype=torch.int32)
+    with pytest.raises(ValueError, match="err must be"):
+        slp.slp_forward(x, t, err=torch.zeros(1, dtype=torch.int64))
+    with pytest.raises(ValueError, match=CUDA_ONLY):
+        slp.slp_forward(x, t, err=torch.zeros(1, dtype=torch.int32))
+    h = torch.zeros(N, d, dtype=torch.bfloat16)
+    W = torch.zeros(V, d, dtype=torch.bfloat16)
+    lp = torch.zeros(N)
+    with pytest.raises(ValueError, match="lse must be"):
+        slp.slp_lmhead_forward_noalloc(h, W, t, None, 1.0, lp, torch.zeros(N + 1))
+    with pytest.raises(ValueError, match=CUDA_ONLY):
+        slp.slp_lmhead_forward_noalloc(h, W, t, None, 1.0, lp, torch.zeros(N))
 
 
 def test_lmhead_workspace_size_max(lib):

@@ -81,13 +81,60 @@ def _check_disjoint(out_name, out, *inputs):
 def _logits_layout(x):
     if x.dim() != 2 or x.dtype not in _DTYPES:
         raise ValueError("x must be a 2-D bfloat16 or float32 tensor")
-    if not x.is_cuda:
-        raise ValueError("x must be a CUDA tensor")
     N, V = x.shape
     if N > 0 and V > 0 and x.stride(1) != 1:
         raise ValueError("x must have unit column stride")
     ld = x.stride(0) if N > 1 else max(V, 1)
     return N, V, ld
+
+
+def _check_grad_x(grad_x, x, N, V):
+    """A caller's grad_x: [N, V], x's dtype, unit column stride, rows at least
+    V apart (the library writes N rows of V elements at its row stride), and
+    no overlap with x.  Returns its row stride."""
+    if grad_x.dim() != 2 or tuple(grad_x.shape) != (N, V) or grad_x.dtype != x.dtype:
+        raise ValueError(f"grad_x must be an [{N}, {V}] {x.dtype} tensor")
+    if N > 0 and V > 0 and grad_x.stride(1) != 1:
+        raise ValueError("grad_x must have unit column stride")
+    ldg = grad_x.stride(0) if N > 1 else max(V, 1)
+    if ldg < V:
+        raise ValueError("grad_x rows must not overlap (row stride >= V)")
+    _check_disjoint("grad_x", grad_x, x)
+    return ldg
+
+
+def _check_mat(name, v, rows, cols, dtype):
+    """A caller's [rows, cols] output written densely by the library."""
+    if v.dim() != 2 or tuple(v.shape) != (rows, cols) or v.dtype != dtype or not v.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous [{rows}, {cols}] {dtype} tensor")
+    return v
+
+
+def _err_ptr(err):
+    """The optional device error word: an int32 tensor of at least one
+    element (the library ORs status bits into its first element)."""
+    if err is None:
+        return None
+    if err.dtype != torch.int32 or err.numel() < 1 or not err.is_contiguous():
+        raise ValueError("err must be a contiguous int32 tensor of at least one element")
+    return err.data_ptr()
+
+
+def _require_device(*tensors, err=None):
+    """Every tensor handed to the library must live on the current CUDA
+    device: the library launches there, on that device's stream.  Checked
+    last, after the shape checks (the error word's included), so those run on
+    any machine."""
+    _err_ptr(err)
+    tensors = tensors + (err,)
+    for v in tensors:
+        if v is not None and not v.is_cuda:
+            raise ValueError("tensors passed to the library must be CUDA tensors")
+    dev = torch.cuda.current_device()
+    for v in tensors:
+        if v is not None and v.device.index != dev:
+            raise ValueError(f"tensors must be on the current CUDA device (cuda:{dev}), "
+                             f"got {v.device}")
 
 
 def slp_forward(x, t, mask=None, T: float = 1.0, logprob=None, lse=None, err=None, stream=None):
@@ -102,8 +149,9 @@ def slp_forward(x, t, mask=None, T: float = 1.0, logprob=None, lse=None, err=Non
         lse = torch.empty(N, dtype=torch.float32, device=x.device)
     _check_vec("logprob", logprob, N, torch.float32)
     _check_vec("lse", lse, N, torch.float32)
+    _require_device(x, t, mask, logprob, lse, err=err)
     _lib.call("slp_forward", _ptr(x), _DTYPES[x.dtype], N, V, ld, _ptr(t), _ptr(mask), float(T),
-              _ptr(logprob), _ptr(lse), _ptr(err), _stream_handle(stream))
+              _ptr(logprob), _ptr(lse), _err_ptr(err), _stream_handle(stream))
     return logprob, lse
 
 
@@ -117,12 +165,10 @@ def slp_backward(x, t, mask, T: float, lse, grad_out, grad_x=None, err=None, str
     _check_vec("grad_out", grad_out, N, torch.float32)
     if grad_x is None:
         grad_x = torch.empty((N, V), dtype=x.dtype, device=x.device)
-    if grad_x.shape != (N, V) or grad_x.dtype != x.dtype or (N > 0 and V > 0 and grad_x.stride(1) != 1):
-        raise ValueError("grad_x must be [N, V] with x's dtype and unit column stride")
-    ldg = grad_x.stride(0) if N > 1 else max(V, 1)
-    _check_disjoint("grad_x", grad_x, x)
+    ldg = _check_grad_x(grad_x, x, N, V)
+    _require_device(x, t, mask, lse, grad_out, grad_x, err=err)
     _lib.call("slp_backward", _ptr(x), _DTYPES[x.dtype], N, V, ld, _ptr(t), _ptr(mask), float(T),
-              _ptr(lse), _ptr(grad_out), _ptr(grad_x), ldg, _ptr(err), _stream_handle(stream))
+              _ptr(lse), _ptr(grad_out), _ptr(grad_x), ldg, _err_ptr(err), _stream_handle(stream))
     return grad_x
 
 
@@ -138,8 +184,9 @@ def slp_forward_entropy(x, t, mask=None, T: float = 1.0, logprob=None, lse=None,
         v = torch.empty(N, dtype=torch.float32, device=x.device) if v is None else v
         _check_vec("output", v, N, torch.float32)
         out.append(v)
+    _require_device(x, t, mask, *out, err=err)
     _lib.call("slp_forward_entropy", _ptr(x), _DTYPES[x.dtype], N, V, ld, _ptr(t), _ptr(mask),
-              float(T), _ptr(out[0]), _ptr(out[1]), _ptr(out[2]), _ptr(err), _stream_handle(stream))
+              float(T), _ptr(out[0]), _ptr(out[1]), _ptr(out[2]), _err_ptr(err), _stream_handle(stream))
     return tuple(out)
 
 
@@ -157,11 +204,11 @@ def slp_backward_entropy(x, t, mask, T: float, lse, entropy, grad_out=None, grad
             _check_vec(name, v, N, torch.float32)
     if grad_x is None:
         grad_x = torch.empty((N, V), dtype=x.dtype, device=x.device)
-    ldg = grad_x.stride(0) if N > 1 else max(V, 1)
-    _check_disjoint("grad_x", grad_x, x)
+    ldg = _check_grad_x(grad_x, x, N, V)
+    _require_device(x, t, mask, lse, entropy, grad_out, grad_entropy, grad_x, err=err)
     _lib.call("slp_backward_entropy", _ptr(x), _DTYPES[x.dtype], N, V, ld, _ptr(t), _ptr(mask),
               float(T), _ptr(lse), _ptr(entropy), _ptr(grad_out), _ptr(grad_entropy),
-              _ptr(grad_x), ldg, _ptr(err), _stream_handle(stream))
+              _ptr(grad_x), ldg, _err_ptr(err), _stream_handle(stream))
     return grad_x
 
 
@@ -206,9 +253,10 @@ def slp_topk_kl_forward(x, ids, teacher_logp, mask=None, T: float = 1.0,
     if mask is not None:
         _check_vec("mask", mask, N, torch.uint8)
     out = [torch.empty(N, dtype=torch.float32, device=x.device) for _ in range(4)]
+    _require_device(x, ids, teacher_logp, mask, *out, err=err)
     _lib.call("slp_topk_kl_forward", _ptr(x), _DTYPES[x.dtype], N, V, ld, _ptr(ids),
               _ptr(teacher_logp), K, _ptr(mask), float(T), float(clamp_min), _ptr(out[0]),
-              _ptr(out[1]), _ptr(out[2]), _ptr(out[3]), _ptr(err), _stream_handle(stream))
+              _ptr(out[1]), _ptr(out[2]), _ptr(out[3]), _err_ptr(err), _stream_handle(stream))
     return tuple(out)
 
 
@@ -223,11 +271,11 @@ def slp_topk_kl_backward(x, ids, teacher_logp, mask, T: float, clamp_min: float,
     _check_vec("grad_kl", grad_kl, N, torch.float32)
     if grad_x is None:
         grad_x = torch.empty((N, V), dtype=x.dtype, device=x.device)
-    ldg = grad_x.stride(0) if N > 1 else max(V, 1)
-    _check_disjoint("grad_x", grad_x, x)
+    ldg = _check_grad_x(grad_x, x, N, V)
+    _require_device(x, ids, teacher_logp, mask, lse, grad_kl, grad_x, err=err)
     _lib.call("slp_topk_kl_backward", _ptr(x), _DTYPES[x.dtype], N, V, ld, _ptr(ids),
               _ptr(teacher_logp), K, _ptr(mask), float(T), float(clamp_min), _ptr(lse),
-              _ptr(grad_kl), _ptr(grad_x), ldg, _ptr(err), _stream_handle(stream))
+              _ptr(grad_kl), _ptr(grad_x), ldg, _err_ptr(err), _stream_handle(stream))
     return grad_x
 
 
@@ -248,12 +296,10 @@ def slp_forward_backward(x, t, mask, T: float, grad_out, logprob=None, lse=None,
     _check_vec("lse", lse, N, torch.float32)
     if grad_x is None:
         grad_x = torch.empty((N, V), dtype=x.dtype, device=x.device)
-    if grad_x.shape != (N, V) or grad_x.dtype != x.dtype or (N > 0 and V > 0 and grad_x.stride(1) != 1):
-        raise ValueError("grad_x must be [N, V] with x's dtype and unit column stride")
-    ldg = grad_x.stride(0) if N > 1 else max(V, 1)
-    _check_disjoint("grad_x", grad_x, x)
+    ldg = _check_grad_x(grad_x, x, N, V)
+    _require_device(x, t, mask, grad_out, logprob, lse, grad_x, err=err)
     _lib.call("slp_forward_backward", _ptr(x), _DTYPES[x.dtype], N, V, ld, _ptr(t), _ptr(mask),
-              float(T), _ptr(grad_out), _ptr(logprob), _ptr(lse), _ptr(grad_x), ldg, _ptr(err),
+              float(T), _ptr(grad_out), _ptr(logprob), _ptr(lse), _ptr(grad_x), ldg, _err_ptr(err),
               _stream_handle(stream))
     return logprob, lse, grad_x
 
@@ -278,13 +324,11 @@ def slp_forward_backward_entropy(x, t, mask, T: float, grad_out=None, grad_entro
         out.append(v)
     if grad_x is None:
         grad_x = torch.empty((N, V), dtype=x.dtype, device=x.device)
-    if grad_x.shape != (N, V) or grad_x.dtype != x.dtype or (N > 0 and V > 0 and grad_x.stride(1) != 1):
-        raise ValueError("grad_x must be [N, V] with x's dtype and unit column stride")
-    ldg = grad_x.stride(0) if N > 1 else max(V, 1)
-    _check_disjoint("grad_x", grad_x, x)
+    ldg = _check_grad_x(grad_x, x, N, V)
+    _require_device(x, t, mask, grad_out, grad_entropy, *out, grad_x, err=err)
     _lib.call("slp_forward_backward_entropy", _ptr(x), _DTYPES[x.dtype], N, V, ld, _ptr(t),
               _ptr(mask), float(T), _ptr(grad_out), _ptr(grad_entropy), _ptr(out[0]),
-              _ptr(out[1]), _ptr(out[2]), _ptr(grad_x), ldg, _ptr(err), _stream_handle(stream))
+              _ptr(out[1]), _ptr(out[2]), _ptr(grad_x), ldg, _err_ptr(err), _stream_handle(stream))
     return out[0], out[1], out[2], grad_x
 
 
@@ -313,10 +357,14 @@ def _lmhead_check(h, W):
 
 
 def _workspace(N, V, d, ws, device, forward_only=False):
+    """The caller's workspace (any dtype, contiguous) and its size in bytes,
+    or a new one of the size the call needs."""
     need = (slp_lmhead_forward_workspace_size if forward_only else slp_lmhead_workspace_size)(N, V, d)
     if ws is None:
         ws = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
-    return ws, ws.numel()
+    if not ws.is_contiguous():
+        raise ValueError("ws must be a contiguous tensor")
+    return ws, ws.numel() * ws.element_size()
 
 
 def slp_lmhead_forward(h, W, t, mask=None, T: float = 1.0, logprob=None, lse=None, ws=None,
@@ -330,9 +378,12 @@ def slp_lmhead_forward(h, W, t, mask=None, T: float = 1.0, logprob=None, lse=Non
         logprob = torch.empty(N, dtype=torch.float32, device=h.device)
     if lse is None:
         lse = torch.empty(N, dtype=torch.float32, device=h.device)
+    _check_vec("logprob", logprob, N, torch.float32)
+    _check_vec("lse", lse, N, torch.float32)
     ws, nbytes = _workspace(N, V, d, ws, h.device, forward_only=True)
+    _require_device(h, W, t, mask, logprob, lse, ws, err=err)
     _lib.call("slp_lmhead_forward", _ptr(h), _ptr(W), N, V, d, _ptr(t), _ptr(mask), float(T),
-              _ptr(logprob), _ptr(lse), _ptr(ws), nbytes, _ptr(err), _stream_handle(stream))
+              _ptr(logprob), _ptr(lse), _ptr(ws), nbytes, _err_ptr(err), _stream_handle(stream))
     return logprob, lse
 
 
@@ -346,8 +397,9 @@ def slp_lmhead_forward_noalloc(h, W, t, mask, T: float, logprob, lse, err=None, 
         _check_vec("mask", mask, N, torch.uint8)
     _check_vec("logprob", logprob, N, torch.float32)
     _check_vec("lse", lse, N, torch.float32)
+    _require_device(h, W, t, mask, logprob, lse, err=err)
     _lib.call("slp_lmhead_forward_noalloc", _ptr(h), _ptr(W), N, V, d, _ptr(t), _ptr(mask),
-              float(T), _ptr(logprob), _ptr(lse), _ptr(err), _stream_handle(stream))
+              float(T), _ptr(logprob), _ptr(lse), _err_ptr(err), _stream_handle(stream))
     return logprob, lse
 
 
@@ -364,11 +416,14 @@ def slp_lmhead_backward(h, W, t, mask, T: float, lse, grad_out, dh=None, dW=None
         dh = torch.empty((N, d), dtype=torch.bfloat16, device=h.device)
     if dW is None:
         dW = torch.empty((V, d), dtype=torch.bfloat16, device=h.device)
-    ws, nbytes = _workspace(N, V, d, ws, h.device)
-    _check_disjoint("dh", dh, h, W)
+    _check_mat("dh", dh, N, d, torch.bfloat16)
+    _check_mat("dW", dW, V, d, torch.bfloat16)
+    _check_disjoint("dh", dh, h, W, dW)
     _check_disjoint("dW", dW, h, W)
+    ws, nbytes = _workspace(N, V, d, ws, h.device)
+    _require_device(h, W, t, mask, lse, grad_out, dh, dW, ws, err=err)
     _lib.call("slp_lmhead_backward", _ptr(h), _ptr(W), N, V, d, _ptr(t), _ptr(mask), float(T),
-              _ptr(lse), _ptr(grad_out), _ptr(dh), _ptr(dW), _ptr(ws), nbytes, _ptr(err),
+              _ptr(lse), _ptr(grad_out), _ptr(dh), _ptr(dW), _ptr(ws), nbytes, _err_ptr(err),
               _stream_handle(stream))
     return dh, dW
 
@@ -383,14 +438,17 @@ def slp_lmhead_backward_accumulate(h, W, t, mask, T: float, lse, grad_out, dW_ac
         _check_vec("mask", mask, N, torch.uint8)
     _check_vec("lse", lse, N, torch.float32)
     _check_vec("grad_out", grad_out, N, torch.float32)
-    if dW_accum.shape != (V, d) or dW_accum.dtype != torch.float32 or not dW_accum.is_contiguous():
-        raise ValueError("dW_accum must be a contiguous [V, d] float32 tensor")
+    _check_mat("dW_accum", dW_accum, V, d, torch.float32)
     if dh is None:
         dh = torch.empty((N, d), dtype=torch.bfloat16, device=h.device)
+    _check_mat("dh", dh, N, d, torch.bfloat16)
+    _check_disjoint("dh", dh, h, W, dW_accum)
+    _check_disjoint("dW_accum", dW_accum, h, W)
     ws, nbytes = _workspace(N, V, d, ws, h.device)
+    _require_device(h, W, t, mask, lse, grad_out, dh, dW_accum, ws, err=err)
     _lib.call("slp_lmhead_backward_accumulate", _ptr(h), _ptr(W), N, V, d, _ptr(t), _ptr(mask),
               float(T), _ptr(lse), _ptr(grad_out), _ptr(dh), _ptr(dW_accum), _ptr(ws), nbytes,
-              _ptr(err), _stream_handle(stream))
+              _err_ptr(err), _stream_handle(stream))
     return dh
 
 
