@@ -396,11 +396,14 @@ def run_reference(args, world, rank):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1000 / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded generators, CPU)",
-            "config": workload_desc(args.config, inp, na),
+            "config": {**workload_desc(args.config, inp, na),
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": n, "kind": "oracle",
                              "sample": f"{rows} consecutive rows per core per step ({n} threads), "
                                        "fp64 numpy forward+backward including each row's "
-                                       "conversion to fp64"},
+                                       "conversion to fp64; value = rows done / wall time "
+                                       "(a per-core row sample scaled to tokens/s, not the "
+                                       "whole workload)"},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 

@@ -81,6 +81,10 @@ def test_reference_arm_rank0_line(capsys):
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    # the same config keys as the GPU arm's line (workload_desc + parallelism)
+    assert d["config"]["parallelism"] == "single GPU"
+    for k in ("workload", "N", "V", "active_rows", "temperature", "l2"):
+        assert k in d["config"]
 
 
 def test_cpu_baseline_all_cores_runs_every_thread():
