@@ -204,9 +204,11 @@ def lmhead_backward(h, W, t, mask, T: float, lse, grad_out):
 
 
 def lmhead_dh_rows(h, W, t, mask, T: float, lse, grad_out, rows):
-    """Rows `rows` of dh from lmhead_backward, one at a time: for an active row
-    n, dh[n] = dz[n] @ W with dz[n, v] = g_n (1[v = t_n] - exp(h_n.W_v / T -
-    lse_n)) / T; an inactive row is 0.  Needs only row n's own lse."""
+    """Rows `rows` of dh from lmhead_backward: for an active row n,
+    dh[n] = dz[n] @ W with dz[n, v] = g_n (1[v = t_n] - exp(h_n.W_v / T -
+    lse_n)) / T; an inactive row is 0.  Needs only the requested rows' own
+    lse.  The requested active rows are projected together, as one smaller
+    instance of lmhead_backward's products."""
     W = _as_f64(W)
     h = _as_f64(h)
     N = h.shape[0]
@@ -214,13 +216,14 @@ def lmhead_dh_rows(h, W, t, mask, T: float, lse, grad_out, rows):
     t = np.asarray(t).reshape(N).astype(np.int64)
     lse = _as_f64(lse).reshape(N)
     g = _as_f64(grad_out).reshape(N)
-    out = np.zeros((len(rows), W.shape[1]), dtype=np.float64)
-    for k, n in enumerate(rows):
-        if not active[n]:
-            continue
-        x = lmhead_logits(h[n:n + 1], W)
-        dz = selected_logprob_backward(x, t[n:n + 1], None, T, lse[n:n + 1], g[n:n + 1])
-        out[k] = dz[0] @ W
+    rows = np.asarray(rows, dtype=np.int64).reshape(-1)
+    out = np.zeros((rows.size, W.shape[1]), dtype=np.float64)
+    sel = np.nonzero(active[rows])[0]
+    if sel.size:
+        r = rows[sel]
+        x = lmhead_logits(h[r], W)
+        dz = selected_logprob_backward(x, t[r], None, T, lse[r], g[r])
+        out[sel] = dz @ W
     return out
 
 

@@ -70,9 +70,21 @@ def test_small_all_outputs(N, V, d, T, pm):
     assert bool((lp[off] == 0).all()) and bool((lse[off] == 0).all())
 
 
+def grad_rows_ok(got, ref, what):
+    """grad_ok on every row on its own (an all-zero reference row must come
+    back all zeros), then on the rows pooled."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    for k in range(ref.shape[0]):
+        grad_ok(got[k], ref[k], f"{what}, row {k} of the sample")
+    grad_ok(got, ref, f"{what} (pooled)")
+
+
 def test_full_size_sampled():
-    """The lmhead workload at full size (N=8192, V=151936, d=2560): sampled rows
-    of logprob / dh and sampled rows of dW against the oracle."""
+    """The lmhead workload at full size (N=8192, V=151936, d=2560): logprob of
+    every row, 128 rows of dh (120 active, 8 masked) and 256 rows of dW (the
+    targets of the sampled active rows, the first and last vocabulary rows,
+    the rest uniform) against the oracle, each row checked on its own."""
     dev = device()
     a = W.make_lmhead_inputs(device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -81,17 +93,23 @@ def test_full_size_sampled():
     h64, W64 = to64(a.h), to64(a.W)
     t, m, g = a.t.cpu().numpy(), a.mask.cpu().numpy(), to64(a.g)
     act = np.nonzero(m)[0]
+    off_rows = np.nonzero(m == 0)[0]
     gen = np.random.default_rng(5)
-    rows = sorted(set(gen.choice(act, 12, replace=False).tolist()) | {int(act[0]), int(act[-1])})
+    rows = sorted(set(gen.choice(act, 118, replace=False).tolist()) | {int(act[0]), int(act[-1])})
+    rows += sorted(gen.choice(off_rows, 8, replace=False).tolist())
+    assert len(rows) == 128
     # oracle forward for every active row (dW needs every row's lse)
     rlp, rlse = O.lmhead_forward(h64, W64, t, m, a.T)
     assert_close_nan(to64(lp), rlp, TOL_LP, "logprob (all rows)")
     rdh = O.lmhead_dh_rows(h64, W64, t, m, a.T, rlse, g, rows)
-    grad_ok(to64(dh[rows]), rdh, "dh (sampled rows)")
-    vrows = sorted(set(gen.choice(a.W.shape[0], 12, replace=False).tolist()) |
-                   {0, a.W.shape[0] - 1, int(t[act[0]])})
+    grad_rows_ok(to64(dh[rows]), rdh, "dh")
+    V = a.W.shape[0]
+    vset = {int(t[r]) for r in rows if m[r]} | {0, V - 1}
+    while len(vset) < 256:
+        vset.add(int(gen.integers(0, V)))
+    vrows = sorted(vset)
     rdW = O.lmhead_dW_rows(h64, W64, t, m, a.T, rlse, g, vrows)
-    grad_ok(to64(dW[vrows]), rdW, "dW (sampled rows)")
+    grad_rows_ok(to64(dW[vrows]), rdW, "dW")
     off = torch.as_tensor(m == 0, device=dev)
     assert bool((dh[off].view(torch.int16) == 0).all())
     assert bool(torch.isfinite(dW.float()).all()) and bool(torch.isfinite(dh.float()).all())
