@@ -391,8 +391,11 @@ int slp_lmhead_backward(const void* h, const void* W, int64_t N, int64_t V, int6
  * V = 151936 that allows up to N = 1792 rows.
  *
  * The call allocates nothing.  Its first call on a device looks up the
- * array's device address (cudaGetSymbolAddress, with that device current);
- * make that first call before any stream capture.  All calls on a device
+ * array's device address (cudaGetSymbolAddress, with that device current)
+ * and keeps it for the life of the process; make that first call before any
+ * stream capture.  A cudaDeviceReset on that device ends the context that
+ * address belongs to, so the call must not be used on that device after a
+ * reset (unload and reload the library instead).  All calls on a device
  * share the array and leave their contents in it (no part has to start
  * zeroed); calls whose work overlaps on the GPU race on it, so serialise
  * them (for example on one stream).

@@ -12,7 +12,9 @@
 // Nothing here allocates: no cudaMalloc, no cudaFree, no allocating library
 // call.  The first call on a device looks the array up with
 // cudaGetSymbolAddress while that device is current and caches the address;
-// make that first call before any stream capture.  Every call on a device
+// make that first call before any stream capture.  The cached address belongs
+// to the device's current context: after a cudaDeviceReset it is stale, and
+// the call must not be used on that device again.  Every call on a device
 // uses the same array and leaves its contents behind.  No byte of it has to
 // start at zero: every value the kernels read is written earlier in the same
 // call.  Two calls whose work overlaps on the GPU (other streams, or a second
