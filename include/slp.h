@@ -75,8 +75,11 @@ typedef enum {
 /* Bits OR-ed into the optional device error word. */
 #define SLP_DATA_ERR_TARGET 1    /* target outside [0, V) on an active row          */
 #define SLP_DEVICE_ERR_TIMEOUT 2 /* a pipeline wait inside an LM-head kernel gave up
-                                    after about two seconds; that call's outputs are
-                                    undefined (the kernel returned instead of hanging) */
+                                    after its bound (two seconds unless
+                                    slp_lmhead_set_wait_limit_ns set another); that
+                                    call's outputs are undefined (the kernel drained
+                                    its copies and tensor-core work and returned
+                                    instead of hanging) */
 
 /*
  * slp_forward - selected-token log-probability and row log-sum-exp.
@@ -426,6 +429,28 @@ int slp_lmhead_backward_accumulate(const void* h, const void* W, int64_t N, int6
                                    const float* lse, const float* grad_out, void* dh,
                                    float* dW_accum, void* ws, size_t ws_bytes, int32_t* err,
                                    void* stream);
+
+/*
+ * slp_lmhead_set_wait_limit_ns - bound, in nanoseconds, of every pipeline wait
+ * inside the LM-head kernels launched after this call (process-wide, all
+ * devices); ns == 0 restores the default of two seconds.  Returns the bound
+ * that was in force.
+ *
+ * The pages have no counterpart: they only ask that what is not handled be
+ * reported explicitly rather than change results silently (Megatron-LM issue
+ * #6700, "Compatibility and fallbacks"; slime issue #2253, maintainer
+ * analysis: a fail-closed contract).  Every wait in the LM-head GEMMs (a copy
+ * landing in shared memory, tensor-core work finishing, an accumulator being
+ * drained) counts SM cycles at two per nanosecond, so it lasts at least this
+ * long at any clock.  A wait that runs out sets SLP_DEVICE_ERR_TIMEOUT in
+ * *err, lets the CTA wait (with a fixed two-second bound) for the copies and
+ * tensor-core operations it has already issued, frees its tensor memory and
+ * returns; later calls on the stream run normally.  A short bound is for
+ * tests of that path and for callers that want an early watchdog; the
+ * default is far above any single launch.  Not synchronised with launches in
+ * flight: it applies to launches made after it returns.
+ */
+uint64_t slp_lmhead_set_wait_limit_ns(uint64_t ns);
 
 /* Static, human-readable text for a slp_status value. */
 const char* slp_status_string(int status);

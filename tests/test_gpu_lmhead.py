@@ -258,3 +258,43 @@ def test_backward_wider_chunks_from_larger_workspace(extra):
     grad_ok(to64(dW), rdW, "dW")
     grad_ok(to64(dh), to64(dh0), "dh against the default chunking")
     grad_ok(to64(dW), to64(dW0), "dW against the default chunking")
+
+
+def test_wait_that_runs_out_flags_the_call_and_the_stream_recovers():
+    """With the wait bound set to 1 ns, the LM-head GEMMs' pipeline waits run
+    out: the forward and the backward return, SLP_DEVICE_ERR_TIMEOUT is set in
+    the error word, and normal calls right after, on the same stream, match
+    the oracle (the kernels drained their copies and tensor-core work and
+    freed their tensor memory instead of hanging)."""
+    from vocab_selected_token_gb300 import _lib
+    dev = device()
+    a = W.make_lmhead_inputs(device=dev, N=512, V=32768, d=2560, seed=41, p_mask=0.8)
+    flagged = {"forward": False, "backward": False}
+    prev = slp.slp_lmhead_set_wait_limit_ns(1)
+    try:
+        assert prev == 2_000_000_000  # the default bound
+        for _ in range(5):  # every CTA's first few waits may still be met in time
+            err = torch.zeros(1, dtype=torch.int32, device=dev)
+            _, lse = slp.slp_lmhead_forward(a.h, a.W, a.t, a.mask, a.T, err=err)
+            torch.cuda.synchronize()
+            flagged["forward"] |= bool(int(err.item()) & _lib.SLP_DEVICE_ERR_TIMEOUT)
+            err = torch.zeros(1, dtype=torch.int32, device=dev)
+            slp.slp_lmhead_backward(a.h, a.W, a.t, a.mask, a.T, torch.zeros_like(lse), a.g,
+                                    err=err)
+            torch.cuda.synchronize()
+            flagged["backward"] |= bool(int(err.item()) & _lib.SLP_DEVICE_ERR_TIMEOUT)
+            if all(flagged.values()):
+                break
+    finally:
+        assert slp.slp_lmhead_set_wait_limit_ns(0) == 1
+    assert flagged["forward"] and flagged["backward"], flagged
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    lp, lse, dh, dW = run_fwd_bwd(a, err=err)
+    assert int(err.item()) == 0
+    h64, W64 = to64(a.h), to64(a.W)
+    t, m, g = a.t.cpu().numpy(), a.mask.cpu().numpy(), to64(a.g)
+    rlp, rlse = O.lmhead_forward(h64, W64, t, m, a.T)
+    assert_close_nan(to64(lp), rlp, TOL_LP, "logprob after the timed-out calls")
+    rdh, rdW = O.lmhead_backward(h64, W64, t, m, a.T, rlse, g)
+    grad_ok(to64(dh), rdh, "dh after the timed-out calls")
+    grad_ok(to64(dW), rdW, "dW after the timed-out calls")

@@ -30,7 +30,7 @@ __all__ = [
     "slp_topk_kl_forward", "slp_topk_kl_backward",
     "slp_lmhead_workspace_size",
     "slp_lmhead_forward_workspace_size", "slp_lmhead_forward_noalloc",
-    "slp_lmhead_backward_accumulate",
+    "slp_lmhead_backward_accumulate", "slp_lmhead_set_wait_limit_ns",
     "slp_lmhead_forward", "slp_lmhead_backward", "selected_logprob",
     "lmhead_selected_logprob", "library_path",
 ]
@@ -346,6 +346,13 @@ def slp_lmhead_workspace_size_max(N: int, V: int, d: int) -> int:
 def slp_lmhead_forward_workspace_size(N: int, V: int, d: int) -> int:
     """Bytes of workspace slp_lmhead_forward alone needs."""
     return int(_lib.load().slp_lmhead_forward_workspace_size(int(N), int(V), int(d)))
+
+
+def slp_lmhead_set_wait_limit_ns(ns: int) -> int:
+    """Bound (ns) of every pipeline wait in later LM-head launches; 0 restores
+    the two-second default.  Returns the previous bound.  A wait that runs
+    out sets SLP_DEVICE_ERR_TIMEOUT in the call's error word."""
+    return int(_lib.load().slp_lmhead_set_wait_limit_ns(int(ns)))
 
 
 def _lmhead_check(h, W):

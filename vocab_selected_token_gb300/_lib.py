@@ -57,6 +57,7 @@ SIGNATURES = {
                                           _vp, _vp]),
     "slp_lmhead_backward_accumulate": (_int, [_vp, _vp, _i64, _i64, _i64, _vp, _vp, _f32, _vp, _vp,
                                               _vp, _vp, _vp, _sz, _vp, _vp]),
+    "slp_lmhead_set_wait_limit_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
     "slp_status_string": (ctypes.c_char_p, [_int]),
 }
 

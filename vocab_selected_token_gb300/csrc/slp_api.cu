@@ -273,6 +273,8 @@ int slp_lmhead_backward_accumulate(const void* h, const void* W, int64_t N, int6
                                                  static_cast<cudaStream_t>(stream), true));
 }
 
+uint64_t slp_lmhead_set_wait_limit_ns(uint64_t ns) { return slp::lmhead_set_wait_limit(ns); }
+
 const char* slp_status_string(int status) {
   switch (status) {
     case SLP_OK: return "ok";

@@ -73,6 +73,9 @@ cudaError_t launch_topk_kl_backward(const void* x, int dtype, int64_t N, int64_t
 size_t lmhead_workspace_size(int64_t N, int64_t V, int64_t d);
 size_t lmhead_workspace_size_max(int64_t N, int64_t V, int64_t d);
 size_t lmhead_forward_workspace_size(int64_t N, int64_t V, int64_t d);
+// Sets the bound of every pipeline wait in later LM-head launches (0: the
+// default of two seconds); returns the previous bound.
+uint64_t lmhead_set_wait_limit(uint64_t ns);
 
 cudaError_t launch_lmhead_forward(const void* h, const void* W, int64_t N, int64_t V, int64_t d,
                                   const int32_t* t, const uint8_t* mask, float T,

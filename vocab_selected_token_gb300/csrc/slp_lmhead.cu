@@ -42,20 +42,37 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace slp {
 namespace lmh {
 
-constexpr int BM = 128;   // rows of a tile (TMEM lanes)
+constexpr int BM = 128;   // rows of one CTA's tile (TMEM lanes)
 constexpr int BN = 256;   // columns of a tile (TMEM columns per accumulator)
 constexpr int BK = 64;    // K per stage: 64 bf16 = one 128-byte swizzle row
-constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = BN * BK * 2;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int kThreads = 256;
 constexpr uint32_t kTmemCols = 2 * BN;
-constexpr int kSmemBytes = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr int kRowRound = 2 * BM;  // compact rows are padded to whole pair tiles
+
+// Tile geometry of the two GEMM forms.  One CTA: a 128 x 256 tile per CTA.
+// CTA pair (cta_group::2): a 256 x 256 tile per pair of CTAs on two SMs, one
+// MMA instruction covering both; each CTA holds its 128 rows of A and half of
+// B (128 tile columns), and its TMEM holds its 128 rows of the accumulator.
+// For the same MMA work per SM a stage then carries 32 KB instead of 48 KB,
+// which leaves room for more stages in flight.
+template <bool kPair>
+struct Tile {
+  static constexpr int kCtas = kPair ? 2 : 1;
+  static constexpr int kRows = BM * kCtas;        // rows of the (pair's) tile
+  static constexpr int kBRows = BN / kCtas;       // B rows (tile columns) in one CTA
+  static constexpr int kBBytes = kBRows * BK * 2;
+  static constexpr int kStageBytes = A_BYTES + kBBytes;
+  static constexpr int kStages = kPair ? 6 : 4;
+  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+};
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // default bound of a pipeline wait
+constexpr uint64_t kDrainLimitNs = 2000000000ull;  // bound of the waits after a give-up
 constexpr int kSlabCap = 256;  // most vocabulary slabs per row (forward partials)
 constexpr int kKSplitCap = 24;  // most K splits of the dh GEMM
 constexpr int kVChunk = 65536;  // vocabulary columns per backward chunk
@@ -68,6 +85,7 @@ __host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
 // the grid, evaluated identically by every CTA and by the follow-up kernels.
 struct Sched {
   int m_tiles, n_tiles, k_blocks, S, units;
+  int bm;  // rows of one tile (128 for one CTA, 256 for a CTA pair)
 };
 
 // Slabs of vocabulary tiles per row block: the S minimising the tile count of
@@ -113,32 +131,34 @@ __host__ __device__ inline int ksplit_min(int V, int d) {
   return static_cast<int>((bytes + (48ll << 20) - 1) / (48ll << 20));
 }
 
+// bm: rows of one tile.  G: tiles in flight at once (CTAs, or CTA pairs).
 // f32_cap: floats of split-K partial storage available to the dh GEMM; the
 // split count is clamped to it (fewer splits are still a correct schedule).
-__host__ __device__ inline Sched make_sched(int epi, int Na, int V, int d, int G,
+__host__ __device__ inline Sched make_sched(int epi, int Na, int V, int d, int G, int bm,
                                             long long f32_cap = -1) {
   Sched s{};
+  s.bm = bm;
   if (epi == EPI_LSE || epi == EPI_DZ) {
-    s.m_tiles = cdiv(Na, BM);
+    s.m_tiles = cdiv(Na, bm);
     s.n_tiles = cdiv(V, BN);
     s.k_blocks = d / BK;
     s.S = choose_slabs(s.m_tiles, s.n_tiles, G);
     s.units = s.m_tiles * s.S;
   } else if (epi == EPI_F32) {
-    s.m_tiles = cdiv(Na, BM);
+    s.m_tiles = cdiv(Na, bm);
     s.n_tiles = cdiv(d, BN);
     s.k_blocks = cdiv(V, BK);
     s.S = choose_ksplits(s.m_tiles * s.n_tiles, s.k_blocks, G, ksplit_min(V, d));
     if (f32_cap >= 0 && s.m_tiles > 0) {
-      const long long per_split = static_cast<long long>(s.m_tiles) * BM * d;
+      const long long per_split = static_cast<long long>(s.m_tiles) * bm * d;
       const long long smax = f32_cap / per_split;
       if (s.S > smax) s.S = smax < 1 ? 1 : static_cast<int>(smax);
     }
     s.units = s.m_tiles * s.n_tiles * s.S;
   } else {
-    s.m_tiles = cdiv(V, BM);
+    s.m_tiles = cdiv(V, bm);
     s.n_tiles = cdiv(d, BN);
-    s.k_blocks = cdiv(Na, BM) * (BM / BK);
+    s.k_blocks = cdiv(Na, BM) * (BM / BK);  // compact rows Na..roundup(Na, 128) are zero
     s.S = 1;
     s.units = s.m_tiles * s.n_tiles;
   }
@@ -208,6 +228,7 @@ struct Params {
   float* out_lp;              // forward results [N] (original rows)
   float* out_lse;
   float T;
+  unsigned long long wait_ns;  // bound of every pipeline wait (after it: give up, flag, drain)
 };
 
 __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float (&v)[32]) {
@@ -236,17 +257,21 @@ __device__ __forceinline__ float select32(const float (&v)[32], int i) {
   return (i & 1) ? d[1] : d[0];
 }
 
-template <int kEpi, bool kAmn, bool kBmn>
+template <int kEpi, bool kAmn, bool kBmn, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     lmh_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB, const Params p) {
   using namespace sm100;
+  using TL = Tile<kPair>;
+  constexpr int STAGES = TL::kStages;
+  constexpr int STAGE_BYTES = TL::kStageBytes;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 4);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  volatile int* peer_fills = reinterpret_cast<volatile int*>(tmem_holder + 2);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -254,7 +279,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_empty = bar_full + 8 * STAGES;
   const uint32_t bar_accf = bar_full + 16 * STAGES;
   const uint32_t bar_acce = bar_accf + 16;
+  const uint32_t bar_done = bar_acce + 16;  // the MMA thread's last commit
   const uint32_t ring = smem_u32(smem);
+  // The pair: rank 0 issues the MMAs and owns the barriers the MMA thread
+  // waits on (full, accumulator-empty); both CTAs load, and both drain their
+  // own TMEM rows.  Without a pair the same code runs with rank 0 alone.
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+  const int tile0 = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int tiles_in_flight = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  const uint32_t lead_full = kPair ? mapa_rank(bar_full, 0) : bar_full;
+  const uint32_t lead_acce = kPair ? mapa_rank(bar_acce, 0) : bar_acce;
+  const uint32_t peer_abort =
+      kPair ? mapa_rank(smem_u32(const_cast<int*>(abort_flag)), rank ^ 1u) : 0u;
+  // a wait that gave up here ends the other CTA's waits too
+  auto give_up = [&]() {
+    *abort_flag = 1;
+    if (kPair) st_cluster_u32(peer_abort, 1u);
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -263,80 +304,111 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_accf + 8 * b, 1);
-      mbar_init(bar_acce + 8 * b, 4);  // one arrival per epilogue warp
+      mbar_init(bar_acce + 8 * b, 4 * TL::kCtas);  // one arrival per epilogue warp of the pair
     }
+    mbar_init(bar_done, 1);
     *abort_flag = 0;
+    *peer_fills = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
   }
-  if (warp == 2) tmem_alloc(smem_u32(tmem_holder), kTmemCols);
+  if (warp == 2) {
+    if (kPair)
+      tmem_alloc_pair(smem_u32(tmem_holder), kTmemCols);
+    else
+      tmem_alloc(smem_u32(tmem_holder), kTmemCols);
+  }
   tc_fence_before();
-  __syncthreads();
+  if (kPair) {
+    __syncwarp();
+    pair_sync();  // both CTAs' barriers exist before either signals the other's
+  } else {
+    __syncthreads();
+  }
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
   const int Na = p.counters[0];
-  const Sched sc = make_sched(kEpi, Na, p.V, p.d, p.G, p.pf32_cap);
+  const Sched sc = make_sched(kEpi, Na, p.V, p.d, p.G, TL::kRows, p.pf32_cap);
+  int fills = 0;  // stage fills this CTA's producer issued
 
   if (warp == 0) {
-    // ---------------- TMA producer ----------------
+    // ---------------- TMA producer (both CTAs) ----------------
     if (lane == 0) {
       int it = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < sc.units && ok; u += gridDim.x) {
+      for (int u = tile0; u < sc.units && ok; u += tiles_in_flight) {
         const Unit w = decode(sc, kEpi, u);
+        const int arow = w.m * TL::kRows + static_cast<int>(rank) * BM;  // this CTA's A rows
         for (int n = w.n0; n < w.n1 && ok; ++n) {
+          const int bcol = n * BN + static_cast<int>(rank) * TL::kBRows;  // this CTA's B rows
           for (int kb = w.k0; kb < w.k1; ++kb, ++it) {
             const int s = it % STAGES;
             const uint32_t ph = (it / STAGES) & 1;
-            if (!mbar_wait_bounded(bar_empty + 8 * s, ph ^ 1, abort_flag, kWaitLimitNs)) {
+            if (!mbar_wait_bounded(bar_empty + 8 * s, ph ^ 1, abort_flag, p.wait_ns)) {
+              give_up();
               ok = false;
               break;
             }
-            const uint32_t fb = bar_full + 8 * s;
-            mbar_arrive_expect_tx(fb, STAGE_BYTES);
+            // rank 0 expects the bytes of both CTAs on its own full barrier
+            if (rank == 0) mbar_arrive_expect_tx(bar_full + 8 * s, STAGE_BYTES * TL::kCtas);
+            const uint32_t fb = lead_full + 8 * s;
             const uint32_t a_dst = ring + s * STAGE_BYTES;
             const uint32_t b_dst = a_dst + A_BYTES;
+            auto load = [&](uint32_t dst, const CUtensorMap* m, int c0, int c1) {
+              if (kPair)
+                tma_load_2d_pair(dst, m, c0, c1, fb);
+              else
+                tma_load_2d(dst, m, c0, c1, fb);
+            };
             if (!kAmn) {
-              tma_load_2d(a_dst, &tmA, kb * BK, w.m * BM, fb);
+              load(a_dst, &tmA, kb * BK, arow);
             } else {
 #pragma unroll
-              for (int j = 0; j < BM / 64; ++j)
-                tma_load_2d(a_dst + j * 8192, &tmA, w.m * BM + 64 * j, kb * BK, fb);
+              for (int j = 0; j < BM / 64; ++j) load(a_dst + j * 8192, &tmA, arow + 64 * j, kb * BK);
             }
             if (!kBmn) {
-              tma_load_2d(b_dst, &tmB, kb * BK, n * BN, fb);
+              load(b_dst, &tmB, kb * BK, bcol);
             } else {
 #pragma unroll
-              for (int j = 0; j < BN / 64; ++j)
-                tma_load_2d(b_dst + j * 8192, &tmB, n * BN + 64 * j, kb * BK, fb);
+              for (int j = 0; j < TL::kBRows / 64; ++j)
+                load(b_dst + j * 8192, &tmB, bcol + 64 * j, kb * BK);
             }
           }
         }
       }
-      if (!ok) {
-        // drain: wait (bounded, ignoring the abort flag) for the copies issued
-        // into the last STAGES slots before the CTA may exit
+      fills = it;
+      if (!kPair) {
+        // Drain: wait (bounded, ignoring the abort flag) for the copies issued
+        // into the last STAGES slots, so no copy lands in shared memory after
+        // the CTA has exited.  Earlier copies were consumed: their slots were
+        // refilled only after the MMAs reading them finished.  After a normal
+        // run these phases have completed already (the MMA thread waited on
+        // them); after a give-up anywhere in the CTA some may still be landing.
         for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
           mbar_wait_bounded(bar_full + 8 * (j % STAGES), (j / STAGES) & 1, nullptr,
-                            kWaitLimitNs);
+                            kDrainLimitNs);
+      } else if (rank == 1) {
+        // tell rank 0, which drains the pair's copies after the cluster barrier
+        st_cluster_u32(mapa_rank(smem_u32(const_cast<int*>(peer_fills)), 0), static_cast<uint32_t>(it));
       }
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
-      constexpr uint32_t idesc = umma_idesc_bf16(BM, BN, kAmn, kBmn);
+    // ---------------- MMA issuer (rank 0 only) ----------------
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = umma_idesc_bf16(TL::kRows, BN, kAmn, kBmn);
       int it = 0, tc = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < sc.units && ok; u += gridDim.x) {
+      for (int u = tile0; u < sc.units && ok; u += tiles_in_flight) {
         const Unit w = decode(sc, kEpi, u);
         for (int n = w.n0; n < w.n1 && ok; ++n, ++tc) {
           const int buf = tc & 1;
           if (!mbar_wait_bounded(bar_acce + 8 * buf, ((tc >> 1) & 1) ^ 1, abort_flag,
-                                 kWaitLimitNs)) {
+                                 p.wait_ns)) {
+            give_up();
             ok = false;
             break;
           }
@@ -345,7 +417,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kb = w.k0; kb < w.k1; ++kb, ++it) {
             const int s = it % STAGES;
             if (!mbar_wait_bounded(bar_full + 8 * s, (it / STAGES) & 1, abort_flag,
-                                   kWaitLimitNs)) {
+                                   p.wait_ns)) {
+              give_up();
               ok = false;
               break;
             }
@@ -358,13 +431,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        : umma_desc_sw128(a_addr + k * 32, 16, 1024);
               const uint64_t bd = kBmn ? umma_desc_sw128(b_addr + k * 2048, 8192, 1024)
                                        : umma_desc_sw128(b_addr + k * 32, 16, 1024);
-              mma_bf16(d_tmem, ad, bd, idesc, (kb > w.k0 || k > 0) ? 1u : 0u);
+              if (kPair)
+                mma_bf16_pair(d_tmem, ad, bd, idesc, (kb > w.k0 || k > 0) ? 1u : 0u);
+              else
+                mma_bf16(d_tmem, ad, bd, idesc, (kb > w.k0 || k > 0) ? 1u : 0u);
             }
-            mma_commit(bar_empty + 8 * s);  // frees the stage once these MMAs finish
+            // frees the stage (in both CTAs) once these MMAs finish
+            if (kPair)
+              mma_commit_pair_mc(bar_empty + 8 * s, 3);
+            else
+              mma_commit(bar_empty + 8 * s);
           }
           if (!ok) break;
-          mma_commit(bar_accf + 8 * buf);  // accumulator ready for the epilogue
+          // accumulator ready for the epilogue (of both CTAs)
+          if (kPair)
+            mma_commit_pair_mc(bar_accf + 8 * buf, 3);
+          else
+            mma_commit(bar_accf + 8 * buf);
         }
+      }
+      // Every MMA this thread issued has completed before the CTA barrier
+      // below, so none still writes TMEM when warp 2 frees it.  After a
+      // normal run the epilogue has waited for all of them already; after a
+      // give-up (here or in the epilogue) some may still be running.
+      if (it > 0) {
+        if (kPair)
+          mma_commit_pair(bar_done);
+        else
+          mma_commit(bar_done);
+        mbar_wait_bounded(bar_done, 0, nullptr, kDrainLimitNs);
       }
     }
   } else if ((kEpi == EPI_BF16 || kEpi == EPI_ACC32) && warp < 4) {
@@ -373,8 +468,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // GEMM that ran just before, in split order, for every compact row i < Na.
     // The dW GEMM does not touch dh_acc or the partials, so the two overlap.
     if (p.dh_fold) {
-      const Sched sf = make_sched(EPI_F32, Na, p.V, p.d, p.G, p.pf32_cap);
-      const long long mpad = static_cast<long long>(sf.m_tiles) * BM;
+      const Sched sf = make_sched(EPI_F32, Na, p.V, p.d, p.G, TL::kRows, p.pf32_cap);
+      const long long mpad = static_cast<long long>(sf.m_tiles) * sf.bm;
       const bool first = p.v0 == 0;
       const int nw = static_cast<int>(gridDim.x) * 2;
       for (int i = static_cast<int>(blockIdx.x) * 2 + (warp - 2); i < Na; i += nw) {
@@ -406,14 +501,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp >= 4) {
-    // ---------------- epilogue ----------------
+    // ---------------- epilogue (both CTAs: each drains its own TMEM rows) ----------------
     const int q = warp & 3;
-    const int rit = q * 32 + lane;  // row within the tile = TMEM lane
+    const int rit = q * 32 + lane;  // row within this CTA's 128 rows = TMEM lane
     int tc = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < sc.units && ok; u += gridDim.x) {
+    for (int u = tile0; u < sc.units && ok; u += tiles_in_flight) {
       const Unit w = decode(sc, kEpi, u);
-      const int row = w.m * BM + rit;
+      const int rblk = w.m * TL::kCtas + static_cast<int>(rank);  // 128-row block of this CTA
+      const int row = rblk * BM + rit;
       // per-row constants
       bool valid = false;
       int tr = -1;
@@ -442,8 +538,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // every lane waits; the warp then agrees, so no lane reaches the
         // warp-wide tcgen05.ld alone
         const bool got = mbar_wait_bounded(bar_accf + 8 * buf, (tc >> 1) & 1, abort_flag,
-                                           kWaitLimitNs);
+                                           p.wait_ns);
         if (!__all_sync(0xFFFFFFFFu, got)) {
+          if (lane == 0) give_up();
           ok = false;
           break;
         }
@@ -487,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           } else if (kEpi == EPI_F32) {
             if (row < Na && col0 < p.d) {
-              const long long mpad = static_cast<long long>(sc.m_tiles) * BM;
+              const long long mpad = static_cast<long long>(sc.m_tiles) * sc.bm;
               float* dst = p.part_f32 + (static_cast<long long>(w.slab) * mpad + row) * p.d + col0;
               float4* d4 = reinterpret_cast<float4*>(dst);
 #pragma unroll
@@ -514,7 +611,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_acce + 8 * buf);
+        if (lane == 0) {
+          if (kPair)
+            mbar_arrive_cluster(lead_acce + 8 * buf);
+          else
+            mbar_arrive(bar_acce + 8 * buf);
+        }
       }
       if (kEpi == EPI_LSE && ok) {
         if (valid) {
@@ -529,7 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // each row in slab order and writes the row's results.
         __threadfence();
         __syncwarp();
-        int* cnt = p.row_cnt + w.m * 4 + q;
+        int* cnt = p.row_cnt + rblk * 4 + q;
         int old = 0;
         if (lane == 0) old = atomicAdd(cnt, 1);
         old = __shfl_sync(0xFFFFFFFFu, old, 0);
@@ -556,10 +658,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  if (kPair) {
+    // Both CTAs are done issuing.  Rank 0 then drains every copy of the pair
+    // still landing: each CTA's copies count on rank 0's full barriers, and
+    // neither CTA may exit while a copy into either's shared memory, or onto
+    // rank 0's barriers, is in flight.
+    __syncwarp();
+    pair_sync();
+    if (rank == 0 && warp == 0 && lane == 0) {
+      const int mine = fills;
+      const int peer = *peer_fills;
+      const int hi = mine > peer ? mine : peer;
+      for (int j = (hi > STAGES ? hi - STAGES : 0); j < hi; ++j) {
+        const uint32_t fb = bar_full + 8 * (j % STAGES);
+        if (j >= mine)
+          mbar_arrive_expect_tx(fb, STAGE_BYTES);  // the peer's half only: rank 0 never armed it
+        else if (j >= peer)
+          mbar_complete_tx(fb, STAGE_BYTES);  // armed for both halves; the peer's never comes
+        mbar_wait_bounded(fb, (j / STAGES) & 1, nullptr, kDrainLimitNs);
+      }
+    }
+    __syncwarp();
+    pair_sync();
+  } else {
+    __syncthreads();
+  }
   if (warp == 2) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    if (kPair)
+      tmem_dealloc_pair(tmem_base, kTmemCols);
+    else
+      tmem_dealloc(tmem_base, kTmemCols);
   }
   if (threadIdx.x == 0 && *abort_flag && p.err != nullptr) atomicOr(p.err, SLP_DEVICE_ERR_TIMEOUT);
 }
@@ -633,7 +762,7 @@ __global__ void __launch_bounds__(1024)
 }
 
 // Warp w of the grid copies active row w of h to its compact slot; warps
-// N .. N+BM-1 zero compact rows Na .. roundup(Na, BM)-1.
+// N .. N+255 zero compact rows Na .. roundup(Na, 256)-1 (whole pair tiles).
 constexpr int kGatherWarps = 8;
 __global__ void __launch_bounds__(32 * kGatherWarps)
     lmh_gather_kernel(const __nv_bfloat16* __restrict__ h, int N, int d,
@@ -648,10 +777,10 @@ __global__ void __launch_bounds__(32 * kGatherWarps)
     dst_row = pos[w];
     if (dst_row < 0) return;
     src = reinterpret_cast<const uint4*>(h + static_cast<long long>(w) * d);
-  } else if (w < N + BM) {
+  } else if (w < N + kRowRound) {
     const int Na = counters[0];
     dst_row = Na + (w - N);
-    if (dst_row >= cdiv(Na, BM) * BM) return;
+    if (dst_row >= cdiv(Na, kRowRound) * kRowRound) return;
   } else {
     return;
   }
@@ -731,7 +860,75 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, 
 
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+template <int kEpi, bool kAmn, bool kBmn, bool kPair>
+cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const Params& p,
+                        cudaStream_t stream) {
+  using TL = Tile<kPair>;
+  auto k = lmh_gemm_kernel<kEpi, kAmn, kBmn, kPair>;
+  cudaError_t e =
+      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, TL::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  if (!kPair) {
+    k<<<p.G, kThreads, TL::kSmemBytes, stream>>>(a, b, p);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(2 * p.G);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = TL::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, a, b, p);
+}
+
+// How the GEMMs run on the current device: as CTA pairs (cta_group::2),
+// one pair per two SMs that the device can co-schedule as a cluster, or as
+// one CTA per SM when it cannot.  G = tiles in flight (pairs or CTAs), bm =
+// rows of one tile.  Queried once per device; the workspace layout and every
+// launch use the same answer.
+struct Geometry {
+  bool pair;
+  int G;
+  int bm;
+};
+
+Geometry geometry() {
+  static int cached[64] = {0};  // pairs that fit, or -1: none
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  if (cached[dev] == 0) {
+    int n = 0;
+    auto k = lmh_gemm_kernel<EPI_LSE, false, false, true>;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Tile<true>::kSmemBytes) == cudaSuccess) {
+      cudaLaunchConfig_t cfg{};
+      cfg.gridDim = dim3(2 * (sm_count() / 2));
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = Tile<true>::kSmemBytes;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess) n = 0;
+    }
+    cudaGetLastError();  // a failed query leaves no sticky error behind
+    cached[dev] = n > 0 ? n : -1;
+  }
+  if (cached[dev] > 0) return Geometry{true, cached[dev], Tile<true>::kRows};
+  return Geometry{false, sm_count(), Tile<false>::kRows};
+}
+
 struct Layout {
+  Geometry geo;
   int Mcap;
   int vchunk;          // vocabulary columns per backward chunk
   long long ld_dz;     // row stride of the dz chunk buffer
@@ -739,16 +936,16 @@ struct Layout {
   size_t off_dz, off_pf32, off_acc, bwd_end;
 };
 
-// Largest split-K partial footprint S * roundup(Na,128) * d over every Na <= N
-// and both chunk widths, for the grid the kernels will use.
-size_t max_partial_floats(int Mcap, int V, int vchunk, int d, int G) {
+// Largest split-K partial footprint S * roundup(Na, bm) * d over every
+// Na <= N and both chunk widths, for the geometry the kernels will use.
+size_t max_partial_floats(int Mcap, int V, int vchunk, int d, const Geometry& g) {
   size_t best = 0;
   const int widths[2] = {vchunk < V ? vchunk : V, V % vchunk == 0 ? (vchunk < V ? vchunk : V)
                                                                  : V % vchunk};
   for (int w = 0; w < 2; ++w)
-    for (int mt = 1; mt * BM <= Mcap; ++mt) {
-      const Sched sc = make_sched(EPI_F32, mt * BM, widths[w], d, G);
-      const size_t f = static_cast<size_t>(sc.S) * mt * BM * d;
+    for (int mt = 1; mt * g.bm <= Mcap; ++mt) {
+      const Sched sc = make_sched(EPI_F32, mt * g.bm, widths[w], d, g.G, g.bm);
+      const size_t f = static_cast<size_t>(sc.S) * mt * g.bm * d;
       if (f > best) best = f;
     }
   return best;
@@ -758,7 +955,8 @@ size_t max_partial_floats(int Mcap, int V, int vchunk, int d, int G) {
 // V is smaller).
 Layout layout(int64_t N, int64_t V, int64_t d, int64_t vchunk = kVChunk) {
   Layout L{};
-  L.Mcap = static_cast<int>(cdiv(static_cast<int>(N), BM) * BM);
+  L.geo = geometry();
+  L.Mcap = static_cast<int>(cdiv(static_cast<int>(N), kRowRound) * kRowRound);
   L.vchunk = V < vchunk ? static_cast<int>(V) : static_cast<int>(vchunk);
   L.ld_dz = (L.vchunk + 63) / 64 * 64;
   size_t o = 0;
@@ -777,21 +975,22 @@ Layout layout(int64_t N, int64_t V, int64_t d, int64_t vchunk = kVChunk) {
   o = align256(L.off_dz + 2 * static_cast<size_t>(L.Mcap) * L.ld_dz);
   L.off_pf32 = o;
   o = align256(o + 4 * max_partial_floats(L.Mcap, static_cast<int>(V), L.vchunk,
-                                         static_cast<int>(d), sm_count()));
+                                         static_cast<int>(d), L.geo));
   L.off_acc = o; o = align256(o + 4 * static_cast<size_t>(L.Mcap) * d);
   L.bwd_end = o > L.fwd_end ? o : L.fwd_end;
   return L;
 }
 
+// One GEMM launch in the layout's geometry.
 template <int kEpi, bool kAmn, bool kBmn>
-cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const Params& p,
-                        cudaStream_t stream) {
-  auto k = lmh_gemm_kernel<kEpi, kAmn, kBmn>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (e != cudaSuccess) return e;
-  k<<<p.G, kThreads, kSmemBytes, stream>>>(a, b, p);
-  return cudaGetLastError();
+cudaError_t launch(const Layout& L, const CUtensorMap& a, const CUtensorMap& b, const Params& p,
+                   cudaStream_t stream) {
+  return L.geo.pair ? launch_gemm<kEpi, kAmn, kBmn, true>(a, b, p, stream)
+                    : launch_gemm<kEpi, kAmn, kBmn, false>(a, b, p, stream);
 }
+
+// Bound of the pipeline waits for the launches that follow (process-wide).
+std::atomic<unsigned long long> g_wait_ns{kWaitLimitNs};
 
 struct Prepared {
   Layout L;
@@ -830,7 +1029,7 @@ cudaError_t prepare(const void* h, int64_t N, int64_t V, int64_t d, const int32_
   p.d = static_cast<int>(d);
   p.N = static_cast<int>(N);
   p.Mcap = P.L.Mcap;
-  p.G = sm_count();
+  p.G = P.L.geo.G;
   p.counters = counters;
   p.idx = idx;
   p.t = t;
@@ -850,15 +1049,20 @@ cudaError_t prepare(const void* h, int64_t N, int64_t V, int64_t d, const int32_
   p.out_lp = logprob;
   p.out_lse = lse;
   p.T = T;
+  p.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
   lmh_scan_kernel<<<1, 1024, 0, stream>>>(mask, p.N, counters, P.pos, idx, p.row_cnt,
                                           (P.L.Mcap / BM) * 4, logprob, lse);
-  lmh_gather_kernel<<<cdiv(p.N + BM, kGatherWarps), 32 * kGatherWarps, 0, stream>>>(
+  lmh_gather_kernel<<<cdiv(p.N + kRowRound, kGatherWarps), 32 * kGatherWarps, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(h), p.N,
                                                  p.d, counters, P.pos, P.hc);
   return cudaGetLastError();
 }
 
 }  // namespace lmh
+
+uint64_t lmhead_set_wait_limit(uint64_t ns) {
+  return lmh::g_wait_ns.exchange(ns == 0 ? lmh::kWaitLimitNs : ns);
+}
 
 size_t lmhead_forward_workspace_size(int64_t N, int64_t V, int64_t d) {
   return lmh::layout(N, V, d).fwd_end;
@@ -879,11 +1083,12 @@ cudaError_t launch_lmhead_forward(const void* h, const void* W, int64_t N, int64
   Prepared P;
   cudaError_t e = prepare(h, N, V, d, t, mask, T, ws, err, stream, &P, logprob, lse);
   if (e != cudaSuccess) return e;
+  const uint32_t brows = static_cast<uint32_t>(BN / (P.L.geo.pair ? 2 : 1));  // B rows per CTA
   CUtensorMap ma, mb;
   if (!make_map(&ma, P.hc, d, P.L.Mcap, d * 2, BK, BM) ||
-      !make_map(&mb, W, d, V, d * 2, BK, BN))
+      !make_map(&mb, W, d, V, d * 2, BK, brows))
     return cudaErrorInvalidValue;
-  return launch_gemm<EPI_LSE, false, false>(ma, mb, P.p, stream);
+  return launch<EPI_LSE, false, false>(P.L, ma, mb, P.p, stream);
 }
 
 cudaError_t launch_lmhead_backward(const void* h, const void* W, int64_t N, int64_t V, int64_t d,
@@ -915,18 +1120,19 @@ cudaError_t launch_lmhead_backward(const void* h, const void* W, int64_t N, int6
       pc.out = static_cast<__nv_bfloat16*>(dW) + v0 * d;
     const __nv_bfloat16* Wc = Wb + v0 * d;
     CUtensorMap m_w_k, m_dz_k, m_w_mn, m_dz_mn;
-    if (!make_map(&m_w_k, Wc, d, vc, d * 2, BK, BN) ||                // B of recompute
+    const uint32_t brows = static_cast<uint32_t>(BN / (P.L.geo.pair ? 2 : 1));
+    if (!make_map(&m_w_k, Wc, d, vc, d * 2, BK, brows) ||             // B of recompute
         !make_map(&m_dz_k, pc.dz, vc, P.L.Mcap, dz_row, BK, BM) ||    // A of dh (K = chunk)
         !make_map(&m_w_mn, Wc, d, vc, d * 2, 64, BK) ||               // B of dh (N = d)
         !make_map(&m_dz_mn, pc.dz, vc, P.L.Mcap, dz_row, 64, BK))     // A of dW (M = chunk)
       return cudaErrorInvalidValue;
-    e = launch_gemm<EPI_DZ, false, false>(m_hc_k, m_w_k, pc, stream);
+    e = launch<EPI_DZ, false, false>(P.L, m_hc_k, m_w_k, pc, stream);
     if (e != cudaSuccess) return e;
-    e = launch_gemm<EPI_F32, false, true>(m_dz_k, m_w_mn, pc, stream);
+    e = launch<EPI_F32, false, true>(P.L, m_dz_k, m_w_mn, pc, stream);
     if (e != cudaSuccess) return e;
     pc.dh_fold = 1;
-    e = accumulate_f32 ? launch_gemm<EPI_ACC32, true, true>(m_dz_mn, m_hc_mn, pc, stream)
-                       : launch_gemm<EPI_BF16, true, true>(m_dz_mn, m_hc_mn, pc, stream);
+    e = accumulate_f32 ? launch<EPI_ACC32, true, true>(P.L, m_dz_mn, m_hc_mn, pc, stream)
+                       : launch<EPI_BF16, true, true>(P.L, m_dz_mn, m_hc_mn, pc, stream);
     if (e != cudaSuccess) return e;
   }
   lmh_dh_finish_kernel<<<static_cast<int>(N), 256, 0, stream>>>(P.p, P.pos,

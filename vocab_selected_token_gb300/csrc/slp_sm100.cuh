@@ -59,6 +59,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but the thread is suspended for at most about hint_ns
+// nanoseconds while the phase is incomplete (instead of the hardware's own
+// window, which can outlast a short wait bound by itself).
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity,
+                                                   uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounds below this are "short": each try then suspends for at most the bound
+// and the clock is read after every try, so the bound holds to within a try.
+constexpr uint64_t kShortWaitNs = 1000000;
+
 // Wait until the phase with the given parity has completed, giving up after
 // about `limit_ns` (counted in this SM's cycles, at least that long at any
 // clock) or as soon as *abort is set by another thread (abort may be NULL:
@@ -66,12 +86,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // ran out also sets *abort.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   volatile int* abort, uint64_t limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
+  const bool short_bound = limit_ns < kShortWaitNs;
+  const uint32_t hint = static_cast<uint32_t>(limit_ns);
+  if (short_bound ? mbar_try_wait_hint(bar, parity, hint) : mbar_try_wait(bar, parity))
+    return true;
   const uint64_t t0 = sm_cycles();
   const uint64_t limit = limit_ns * kCyclesPerNs;
   for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 0) {
+    if (short_bound ? mbar_try_wait_hint(bar, parity, hint) : mbar_try_wait(bar, parity))
+      return true;
+    if (short_bound || (i & 63u) == 0) {
       if (abort != nullptr && *abort) return false;
       if (sm_cycles() - t0 > limit) {
         if (abort != nullptr) *abort = 1;
@@ -203,6 +227,107 @@ __host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N, bool a_mn, 
   return (1u << 4) | (1u << 7) | (1u << 10) | (a_mn ? (1u << 15) : 0u) |
          (b_mn ? (1u << 16) : 0u) | ((static_cast<uint32_t>(N) >> 3) << 17) |
          ((static_cast<uint32_t>(M) >> 4) << 24);
+}
+
+// ---- CTA pairs: a thread-block cluster of two CTAs on two SMs ----------------
+// The pair-wide MMA (cta_group::2) is issued by one thread of the even CTA and
+// reads A and B from the same shared-memory offsets in both CTAs; its
+// accumulator rows live in both CTAs' TMEM at the same column offset.
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// shared::cluster address of the same shared-memory offset in CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_rank(uint32_t smem_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+  return r;
+}
+
+// Every thread of both CTAs: arrive (release) and wait (acquire) at the
+// cluster barrier.  Callers reconverge the warp first (__syncwarp), so all
+// its threads execute the same barrier instruction.
+__device__ __forceinline__ void pair_sync() {
+  asm volatile("barrier.cluster.arrive.release;\n\t"
+               "barrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// Arrive once on an mbarrier that may sit in the other CTA of the pair.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
+// Count `bytes` of the current phase's expected transaction as done, as if
+// they had landed (for copies that will never be issued).
+__device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.complete_tx.relaxed.cluster.shared::cta.b64 [%0], %1;" ::"r"(bar),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.relaxed.cluster.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v)
+               : "memory");
+}
+
+// TMA tiled load into this CTA's shared memory whose completion is counted on
+// an mbarrier of either CTA of the pair (given by its shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap, int32_t c0,
+                                                 int32_t c1, uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(bar_cluster)
+      : "memory");
+}
+
+// Pair-wide TMEM allocation: one warp of each CTA executes it; both CTAs get
+// the same columns.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t holder_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   holder_smem),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+// D[tmem, both CTAs] (+)= A[smem, both CTAs] * B[smem, both CTAs]^T: one
+// 256 x N x 16 instruction (bf16), issued by the even CTA.
+__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive once on the mbarrier at this shared-memory offset in every CTA of
+// `cta_mask` when the pair-wide tcgen05 operations this thread issued so far
+// have completed.
+__device__ __forceinline__ void mma_commit_pair_mc(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(cta_mask)
+      : "memory");
+}
+
+// Same, on this CTA's mbarrier only.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
 }
 
 }  // namespace sm100
