@@ -80,6 +80,9 @@ typedef enum {
                                     call's outputs are undefined (the kernel drained
                                     its copies and tensor-core work and returned
                                     instead of hanging) */
+#define SLP_DEVICE_ERR_BOUNDS 4  /* only in a library built with -DSLP_DEBUG_BOUNDS: a
+                                    kernel refused a global access outside every buffer
+                                    its call was given (the access was skipped)     */
 
 /*
  * slp_forward - selected-token log-probability and row log-sum-exp.
@@ -451,6 +454,22 @@ int slp_lmhead_backward_accumulate(const void* h, const void* W, int64_t N, int6
  * flight: it applies to launches made after it returns.
  */
 uint64_t slp_lmhead_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * slp_bounds_check_selftest - shows that a library built with
+ * -DSLP_DEBUG_BOUNDS checks its kernels' global accesses.  No page has a
+ * counterpart: this build stands in for a memory checker, which this library's
+ * tests cannot use.
+ *
+ * buf: device array of at least 8 floats; err: device error word.  In the
+ * checked build one kernel is launched whose table of permitted ranges holds
+ * buf[0..4) only; it loads and stores buf[4] (inside the caller's array, so
+ * nothing is touched that the caller does not own) and stores 1.0f to buf[0].
+ * The access to buf[4] must be refused: SLP_DEVICE_ERR_BOUNDS is ORed into
+ * *err, buf[4] is left as it was and buf[0] becomes 1.0f.  In a normal build
+ * nothing is launched and SLP_ERR_UNSUPPORTED is returned.
+ */
+int slp_bounds_check_selftest(float* buf, int32_t* err, void* stream);
 
 /* Static, human-readable text for a slp_status value. */
 const char* slp_status_string(int status);

@@ -19,6 +19,7 @@ SLP_ERR_WORKSPACE = 4
 SLP_ERR_CUDA = 5
 SLP_DATA_ERR_TARGET = 1
 SLP_DEVICE_ERR_TIMEOUT = 2
+SLP_DEVICE_ERR_BOUNDS = 4
 
 _vp = ctypes.c_void_p
 _i64 = ctypes.c_int64
@@ -58,6 +59,7 @@ SIGNATURES = {
     "slp_lmhead_backward_accumulate": (_int, [_vp, _vp, _i64, _i64, _i64, _vp, _vp, _f32, _vp, _vp,
                                               _vp, _vp, _vp, _sz, _vp, _vp]),
     "slp_lmhead_set_wait_limit_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
+    "slp_bounds_check_selftest": (_int, [_vp, _vp, _vp]),
     "slp_status_string": (ctypes.c_char_p, [_int]),
 }
 

@@ -1,7 +1,11 @@
 """Build step for libslp.so: compiles every CUDA source under csrc/ for
 sm_103a (in parallel, one process per translation unit) and links the shared
 library in-tree, next to this file.  Used by ``__graft_entry__.build()``;
-run directly with ``python -m vocab_selected_token_gb300.build``."""
+run directly with ``python -m vocab_selected_token_gb300.build``.
+
+``build_checked()`` builds the bounds-checked variant, libslp_checked.so
+(-DSLP_DEBUG_BOUNDS: every global access of every kernel is checked against
+the buffers its call was given), in its own build folder."""
 
 from __future__ import annotations
 
@@ -15,6 +19,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libslp.so")
+BUILD_CHECKED = os.path.join(PKG, "_build_checked")
+LIB_CHECKED = os.path.join(PKG, "libslp_checked.so")
 INCLUDE = os.path.join(ROOT, "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -39,17 +45,18 @@ def _newest_input() -> float:
     return max(os.path.getmtime(f) for f in files)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile and link libslp.so; returns its path.  Skips the work when the
-    library is newer than every source."""
-    if (not force and not extra_flags and os.path.exists(LIB)
-            and os.path.getmtime(LIB) >= _newest_input()):
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), lib: str = LIB,
+          build_dir: str = BUILD) -> str:
+    """Compile and link libslp.so (or `lib`, with `extra_flags`, objects in
+    `build_dir`); returns its path.  Skips the work when the library is newer
+    than every source."""
+    if not force and os.path.exists(lib) and os.path.getmtime(lib) >= _newest_input():
+        return lib
+    os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
     procs, objs = [], []
     for src in sources():
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         cmd = [cc, *NVCC_FLAGS, *extra_flags, "-c", src, "-o", obj]
         if verbose:
@@ -64,16 +71,22 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
             failed.append(src)
     if failed:
         raise RuntimeError(f"nvcc failed on {failed}")
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     link = [cc, "-shared", *ARCH, "-o", tmp, *objs, "-lcudart_static", "-ldl", "-lrt", "-lpthread"]
     if verbose:
         print(" ".join(link), file=sys.stderr)
     r = subprocess.run(link, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)
     if r.returncode != 0:
         sys.stderr.write(r.stdout.decode(errors="replace"))
-        raise RuntimeError("linking libslp.so failed")
-    os.replace(tmp, LIB)
-    return LIB
+        raise RuntimeError(f"linking {os.path.basename(lib)} failed")
+    os.replace(tmp, lib)
+    return lib
+
+
+def build_checked(force: bool = False, verbose: bool = False) -> str:
+    """The bounds-checked library (a test tool, not the product path)."""
+    return build(force=force, verbose=verbose, extra_flags=("-DSLP_DEBUG_BOUNDS",),
+                 lib=LIB_CHECKED, build_dir=BUILD_CHECKED)
 
 
 if __name__ == "__main__":

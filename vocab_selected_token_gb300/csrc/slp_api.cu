@@ -3,6 +3,7 @@
 // launchers.  The library allocates nothing and never synchronises.
 
 #include "slp.h"
+#include "slp_bounds.cuh"
 #include "slp_internal.h"
 
 #include <cuda_runtime.h>
@@ -27,6 +28,18 @@ int sm_count() {
 }  // namespace slp
 
 namespace {
+
+// One CTA whose bounds table holds buf[0..4) only: it loads and stores
+// buf[4], which the bounds-checked build must refuse, and stores buf[0],
+// which it must make.
+__global__ void bounds_selftest_kernel(float* buf SLP_DBG_PARAM) {
+  SLP_DBG_ENTER();
+  if (threadIdx.x == 0) {
+    const float v = slp::dbg::ld(buf + 4);
+    slp::dbg::st(buf + 4, v + 1.0f);
+    slp::dbg::st(buf, 1.0f);
+  }
+}
 
 bool temperature_ok(float T) { return isfinite(T) && T > 0.f; }
 
@@ -274,6 +287,20 @@ int slp_lmhead_backward_accumulate(const void* h, const void* W, int64_t N, int6
 }
 
 uint64_t slp_lmhead_set_wait_limit_ns(uint64_t ns) { return slp::lmhead_set_wait_limit(ns); }
+
+int slp_bounds_check_selftest(float* buf, int32_t* err, void* stream) {
+#ifdef SLP_DEBUG_BOUNDS
+  if (buf == nullptr || err == nullptr) return SLP_ERR_INVALID_ARG;
+  bounds_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      buf SLP_DBG_ARG(err, {{buf, 16ull}}));
+  return cuda_status(cudaGetLastError());
+#else
+  (void)buf;
+  (void)err;
+  (void)stream;
+  return SLP_ERR_UNSUPPORTED;
+#endif
+}
 
 const char* slp_status_string(int status) {
   switch (status) {

@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include "slp.h"
+#include "slp_bounds.cuh"
 
 namespace slp {
 
@@ -22,6 +23,7 @@ __device__ __forceinline__ float ex2(float x) {
 
 // 128-bit streaming load: read once, do not keep in L1.
 __device__ __forceinline__ uint4 ld_stream(const void* p) {
+  if (!dbg::ok(p, 16)) return make_uint4(0u, 0u, 0u, 0u);
   uint4 r;
   asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
       : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
@@ -31,6 +33,7 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) {
 
 // 128-bit streaming store (evict-first).
 __device__ __forceinline__ void st_stream(void* p, const uint4& v) {
+  if (!dbg::ok(p, 16)) return;
   asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
                "r"(v.z), "r"(v.w)
                : "memory");
@@ -62,10 +65,10 @@ struct Elem<__nv_bfloat16> {
     return make_uint4(w[0], w[1], w[2], w[3]);
   }
   __device__ static __forceinline__ float load1(const __nv_bfloat16* p) {
-    return __bfloat162float(*p);
+    return __bfloat162float(dbg::ld(p));
   }
   __device__ static __forceinline__ void store1(__nv_bfloat16* p, float v) {
-    *p = __float2bfloat16_rn(v);
+    dbg::st(p, __float2bfloat16_rn(v));
   }
 };
 
@@ -83,8 +86,8 @@ struct Elem<float> {
     return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
                       __float_as_uint(f[3]));
   }
-  __device__ static __forceinline__ float load1(const float* p) { return *p; }
-  __device__ static __forceinline__ void store1(float* p, float v) { *p = v; }
+  __device__ static __forceinline__ float load1(const float* p) { return dbg::ld(p); }
+  __device__ static __forceinline__ void store1(float* p, float v) { dbg::st(p, v); }
 };
 
 // Running log-sum-exp state of a set of logits, kept in base 2.
@@ -167,8 +170,8 @@ __device__ __forceinline__ void write_row_result(const Lse2& a, float xt, bool t
     l = a.m / T + ln_s;
     lp = (xt - a.m) / T - ln_s;
   }
-  if (logprob != nullptr) logprob[row] = lp;  // NULL: log-sum-exp only
-  lse[row] = l;
+  if (logprob != nullptr) dbg::st(logprob + row, lp);  // NULL: log-sum-exp only
+  dbg::st(lse + row, l);
 }
 
 // Log-sum-exp state with the entropy accumulator, in the base-2 frame of the
@@ -261,7 +264,7 @@ __device__ __forceinline__ void write_row_result(const Lse3& a, float xt, bool t
   } else {
     H = (log2f(a.s) - a.w / a.s) * kLn2;
   }
-  entropy[row] = H;
+  dbg::st(entropy + row, H);
 }
 
 // ---- paired (f32x2) arithmetic on raw 16-byte vectors ----------------------

@@ -238,7 +238,7 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float (&
     float f[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) f[j] = v[q * 8 + j];
-    d4[q] = Elem<__nv_bfloat16>::pack(f);
+    dbg::st(d4 + q, Elem<__nv_bfloat16>::pack(f));
   }
 }
 
@@ -260,7 +260,8 @@ __device__ __forceinline__ float select32(const float (&v)[32], int i) {
 template <int kEpi, bool kAmn, bool kBmn, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     lmh_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                    const __grid_constant__ CUtensorMap tmB, const Params p) {
+                    const __grid_constant__ CUtensorMap tmB, const Params p SLP_DBG_PARAM) {
+  SLP_DBG_ENTER();
   using namespace sm100;
   using TL = Tile<kPair>;
   constexpr int STAGES = TL::kStages;
@@ -331,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
-  const int Na = p.counters[0];
+  const int Na = dbg::ld(p.counters);
   const Sched sc = make_sched(kEpi, Na, p.V, p.d, p.G, TL::kRows, p.pf32_cap);
   int fills = 0;  // stage fills this CTA's producer issued
 
@@ -480,14 +481,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < 4; ++k) {
             a[k] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (j0 + 128 * k < p.d && !first)
-              a[k] = *reinterpret_cast<const float4*>(acc + j0 + 128 * k);
+              a[k] = dbg::ld(reinterpret_cast<const float4*>(acc + j0 + 128 * k));
           }
           for (int sp = 0; sp < sf.S; ++sp) {
             const float* src = p.part_f32 + (sp * mpad + i) * p.d + j0;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               if (j0 + 128 * k >= p.d) continue;
-              const float4 v = *reinterpret_cast<const float4*>(src + 128 * k);
+              const float4 v = dbg::ld(reinterpret_cast<const float4*>(src + 128 * k));
               a[k].x += v.x;
               a[k].y += v.y;
               a[k].z += v.z;
@@ -496,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            if (j0 + 128 * k < p.d) *reinterpret_cast<float4*>(acc + j0 + 128 * k) = a[k];
+            if (j0 + 128 * k < p.d) dbg::st(reinterpret_cast<float4*>(acc + j0 + 128 * k), a[k]);
         }
       }
     }
@@ -519,16 +520,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (kEpi == EPI_LSE || kEpi == EPI_DZ) {
         valid = row < Na;
         if (valid) {
-          const int orig = p.idx[row];
-          tr = p.t[orig];
+          const int orig = dbg::ld(p.idx + row);
+          tr = dbg::ld(p.t + orig);
           if (tr < 0 || tr >= p.Vtot) {
             tr = -1;  // invalid target: no gradient contribution, flagged elsewhere
             valid = kEpi == EPI_LSE;
           } else {
             tr -= p.v0;  // column within this launch (may fall outside it)
             if (kEpi == EPI_DZ) {
-              coef = p.g[orig] * p.invT;
-              L2 = p.lse[orig] * kLog2e;
+              coef = dbg::ld(p.g + orig) * p.invT;
+              L2 = dbg::ld(p.lse + orig) * kLog2e;
             }
           }
         }
@@ -579,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               } else {
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
-                  if (col0 + j < p.V) dst[j] = __float2bfloat16_rn(o[j]);
+                  if (col0 + j < p.V) dbg::st(dst + j, __float2bfloat16_rn(o[j]));
               }
             }
           } else if (kEpi == EPI_F32) {
@@ -589,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               float4* d4 = reinterpret_cast<float4*>(dst);
 #pragma unroll
               for (int j = 0; j < 8; ++j)
-                d4[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                dbg::st(d4 + j, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
             }
           } else if (kEpi == EPI_BF16) {
             if (row < p.V && col0 < p.d)
@@ -599,12 +600,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               float4* d4 = reinterpret_cast<float4*>(p.out_acc + static_cast<long long>(row) * p.d + col0);
 #pragma unroll
               for (int j = 0; j < 8; ++j) {
-                float4 o = d4[j];
+                float4 o = dbg::ld(d4 + j);
                 o.x += v[4 * j];
                 o.y += v[4 * j + 1];
                 o.z += v[4 * j + 2];
                 o.w += v[4 * j + 3];
-                d4[j] = o;
+                dbg::st(d4 + j, o);
               }
             }
           }
@@ -621,10 +622,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (kEpi == EPI_LSE && ok) {
         if (valid) {
           const long long o = static_cast<long long>(w.slab) * p.Mcap + row;
-          p.part_m[o] = st.m;
-          p.part_mc[o] = st.mc;
-          p.part_s[o] = st.s;
-          p.part_xt[o] = xt;
+          dbg::st(p.part_m + o, st.m);
+          dbg::st(p.part_mc + o, st.mc);
+          dbg::st(p.part_s + o, st.s);
+          dbg::st(p.part_xt + o, xt);
         }
         // Each epilogue warp counts its 32 rows' slabs; the warp completing
         // the count (the last slab to store them) merges the S partials of
@@ -633,23 +634,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         int* cnt = p.row_cnt + rblk * 4 + q;
         int old = 0;
-        if (lane == 0) old = atomicAdd(cnt, 1);
+        if (lane == 0 && dbg::ok(cnt, 4)) old = atomicAdd(cnt, 1);
         old = __shfl_sync(0xFFFFFFFFu, old, 0);
         if (old == sc.S - 1 && row < Na) {
           __threadfence();
-          const int orig = p.idx[row];
-          const int tt = p.t[orig];
+          const int orig = dbg::ld(p.idx + row);
+          const int tt = dbg::ld(p.t + orig);
           const bool tvalid = tt >= 0 && tt < p.Vtot;
           const int ttile = tvalid ? tt / BN : -1;
           Lse2 acc = lse2_empty();
           float xtr = 0.f;
           for (int sl = 0; sl < sc.S; ++sl) {
             const long long o = static_cast<long long>(sl) * p.Mcap + row;
-            acc = lse2_merge(acc, Lse2{__ldcg(p.part_m + o), __ldcg(p.part_mc + o),
-                                       __ldcg(p.part_s + o)});
+            acc = lse2_merge(acc, Lse2{dbg::ldcg(p.part_m + o), dbg::ldcg(p.part_mc + o),
+                                       dbg::ldcg(p.part_s + o)});
             const int n0 = static_cast<int>(static_cast<long long>(sl) * sc.n_tiles / sc.S);
             const int n1 = static_cast<int>(static_cast<long long>(sl + 1) * sc.n_tiles / sc.S);
-            if (ttile >= n0 && ttile < n1) xtr = __ldcg(p.part_xt + o);
+            if (ttile >= n0 && ttile < n1) xtr = dbg::ldcg(p.part_xt + o);
           }
           write_row_result(acc, xtr, tvalid, p.T, p.c, p.out_lp, p.out_lse, p.err, orig);
         }
@@ -699,14 +700,15 @@ __global__ void __launch_bounds__(1024)
     lmh_scan_kernel(const uint8_t* __restrict__ mask, int N, int32_t* __restrict__ counters,
                     int32_t* __restrict__ pos, int32_t* __restrict__ idx,
                     int32_t* __restrict__ row_cnt, int n_row_cnt, float* __restrict__ lp0,
-                    float* __restrict__ lse0) {
+                    float* __restrict__ lse0 SLP_DBG_PARAM) {
+  SLP_DBG_ENTER();
   // One CTA; each thread takes kRows consecutive rows per pass, so a pass
   // covers 8192 rows with one block-wide scan of the per-thread counts.
   constexpr int kRows = 8;
   __shared__ int warp_sums[32];
   __shared__ int carry;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int j = threadIdx.x; j < n_row_cnt; j += blockDim.x) row_cnt[j] = 0;
+  for (int j = threadIdx.x; j < n_row_cnt; j += blockDim.x) dbg::st(row_cnt + j, 0);
   if (threadIdx.x == 0) carry = 0;
   __syncthreads();
   for (int base = 0; base < N; base += 1024 * kRows) {
@@ -716,7 +718,7 @@ __global__ void __launch_bounds__(1024)
 #pragma unroll
     for (int e = 0; e < kRows; ++e) {
       const int r = r0 + e;
-      f[e] = (r < N) && (mask == nullptr || mask[r] != 0) ? 1 : 0;
+      f[e] = (r < N) && (mask == nullptr || dbg::ld(mask + r) != 0) ? 1 : 0;
       cnt += f[e];
     }
     int v = cnt;  // inclusive scan of the counts across the warp
@@ -743,14 +745,14 @@ __global__ void __launch_bounds__(1024)
       const int r = r0 + e;
       if (r >= N) break;
       if (f[e]) {
-        pos[r] = excl;
-        idx[excl] = r;
+        dbg::st(pos + r, excl);
+        dbg::st(idx + excl, r);
         ++excl;
       } else {
-        pos[r] = -1;
+        dbg::st(pos + r, -1);
         if (lp0 != nullptr) {  // forward: inactive rows give zeros
-          lp0[r] = 0.f;
-          lse0[r] = 0.f;
+          dbg::st(lp0 + r, 0.f);
+          dbg::st(lse0 + r, 0.f);
         }
       }
     }
@@ -758,7 +760,7 @@ __global__ void __launch_bounds__(1024)
     if (threadIdx.x == 0) carry += warp_sums[31];
     __syncthreads();
   }
-  if (threadIdx.x == 0) counters[0] = carry;
+  if (threadIdx.x == 0) dbg::st(counters, static_cast<int32_t>(carry));
 }
 
 // Warp w of the grid copies active row w of h to its compact slot; warps
@@ -767,18 +769,19 @@ constexpr int kGatherWarps = 8;
 __global__ void __launch_bounds__(32 * kGatherWarps)
     lmh_gather_kernel(const __nv_bfloat16* __restrict__ h, int N, int d,
                       const int32_t* __restrict__ counters, const int32_t* __restrict__ pos,
-                      __nv_bfloat16* __restrict__ hc) {
+                      __nv_bfloat16* __restrict__ hc SLP_DBG_PARAM) {
+  SLP_DBG_ENTER();
   const int w = static_cast<int>(blockIdx.x) * kGatherWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   const int nv = d / 8;  // 16-byte vectors per row
   int dst_row;
   const uint4* src = nullptr;
   if (w < N) {
-    dst_row = pos[w];
+    dst_row = dbg::ld(pos + w);
     if (dst_row < 0) return;
     src = reinterpret_cast<const uint4*>(h + static_cast<long long>(w) * d);
   } else if (w < N + kRowRound) {
-    const int Na = counters[0];
+    const int Na = dbg::ld(counters);
     dst_row = Na + (w - N);
     if (dst_row >= cdiv(Na, kRowRound) * kRowRound) return;
   } else {
@@ -790,11 +793,11 @@ __global__ void __launch_bounds__(32 * kGatherWarps)
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int i = i0 + 32 * u;
-      v[u] = (src != nullptr && i < nv) ? src[i] : make_uint4(0u, 0u, 0u, 0u);
+      v[u] = (src != nullptr && i < nv) ? dbg::ld(src + i) : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u)
-      if (i0 + 32 * u < nv) dst[i0 + 32 * u] = v[u];
+      if (i0 + 32 * u < nv) dbg::st(dst + i0 + 32 * u, v[u]);
   }
 }
 
@@ -803,23 +806,24 @@ __global__ void __launch_bounds__(32 * kGatherWarps)
 // dh[r] = bf16(dh_acc[pos[r]]); inactive rows 0; rows with a bad target NaN.
 __global__ void __launch_bounds__(256)
     lmh_dh_finish_kernel(const Params p, const int32_t* __restrict__ pos,
-                         __nv_bfloat16* __restrict__ dh) {
+                         __nv_bfloat16* __restrict__ dh SLP_DBG_PARAM) {
+  SLP_DBG_ENTER();
   const int r = blockIdx.x;
-  const int i = pos[r];
+  const int i = dbg::ld(pos + r);
   __nv_bfloat16* out = dh + static_cast<long long>(r) * p.d;
-  const int tt = p.t[r];
+  const int tt = dbg::ld(p.t + r);
   const bool bad = i >= 0 && (tt < 0 || tt >= p.Vtot);
   if (bad && threadIdx.x == 0 && p.err != nullptr) atomicOr(p.err, SLP_DATA_ERR_TARGET);
   for (int j = threadIdx.x * 4; j < p.d; j += blockDim.x * 4) {
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (i >= 0) a = *reinterpret_cast<const float4*>(p.dh_acc + static_cast<long long>(i) * p.d + j);
+    if (i >= 0) a = dbg::ld(reinterpret_cast<const float4*>(p.dh_acc + static_cast<long long>(i) * p.d + j));
     if (bad) a.x = a.y = a.z = a.w = __int_as_float(0x7FC00000);
     __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y);
     __nv_bfloat162 hi = __floats2bfloat162_rn(a.z, a.w);
     uint2 w;
     w.x = *reinterpret_cast<uint32_t*>(&lo);
     w.y = *reinterpret_cast<uint32_t*>(&hi);
-    *reinterpret_cast<uint2*>(out + j) = w;
+    dbg::st(reinterpret_cast<uint2*>(out + j), w);
   }
 }
 
@@ -862,14 +866,14 @@ inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255);
 
 template <int kEpi, bool kAmn, bool kBmn, bool kPair>
 cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const Params& p,
-                        cudaStream_t stream) {
+                        cudaStream_t stream SLP_DBG_PARAM) {
   using TL = Tile<kPair>;
   auto k = lmh_gemm_kernel<kEpi, kAmn, kBmn, kPair>;
   cudaError_t e =
       cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, TL::kSmemBytes);
   if (e != cudaSuccess) return e;
   if (!kPair) {
-    k<<<p.G, kThreads, TL::kSmemBytes, stream>>>(a, b, p);
+    k<<<p.G, kThreads, TL::kSmemBytes, stream>>>(a, b, p SLP_DBG_PASS(slp_dbg_bounds));
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg{};
@@ -884,7 +888,7 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const Params
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k, a, b, p);
+  return cudaLaunchKernelEx(&cfg, k, a, b, p SLP_DBG_PASS(slp_dbg_bounds));
 }
 
 // How the GEMMs run on the current device: as CTA pairs (cta_group::2),
@@ -984,9 +988,11 @@ Layout layout(int64_t N, int64_t V, int64_t d, int64_t vchunk = kVChunk) {
 // One GEMM launch in the layout's geometry.
 template <int kEpi, bool kAmn, bool kBmn>
 cudaError_t launch(const Layout& L, const CUtensorMap& a, const CUtensorMap& b, const Params& p,
-                   cudaStream_t stream) {
-  return L.geo.pair ? launch_gemm<kEpi, kAmn, kBmn, true>(a, b, p, stream)
-                    : launch_gemm<kEpi, kAmn, kBmn, false>(a, b, p, stream);
+                   cudaStream_t stream SLP_DBG_PARAM) {
+  return L.geo.pair ? launch_gemm<kEpi, kAmn, kBmn, true>(a, b, p, stream
+                                                         SLP_DBG_PASS(slp_dbg_bounds))
+                    : launch_gemm<kEpi, kAmn, kBmn, false>(a, b, p, stream
+                                                          SLP_DBG_PASS(slp_dbg_bounds));
 }
 
 // Bound of the pipeline waits for the launches that follow (process-wide).
@@ -997,7 +1003,14 @@ struct Prepared {
   Params p;
   int32_t* pos;
   __nv_bfloat16* hc;
+  SLP_DBG_ONLY(dbg::Bounds bnd;)  // the call's buffers and the workspace sections it uses
 };
+
+#ifdef SLP_DEBUG_BOUNDS
+void dbg_add(dbg::Bounds& b, const void* p, size_t bytes) {
+  if (p != nullptr && bytes > 0 && b.n < dbg::kMaxRanges) b.r[b.n++] = dbg::Range{p, bytes};
+}
+#endif
 
 // The widest backward chunk whose workspace fits in ws_bytes: the whole
 // vocabulary, two default chunks, or the default chunk.
@@ -1050,11 +1063,36 @@ cudaError_t prepare(const void* h, int64_t N, int64_t V, int64_t d, const int32_
   p.out_lse = lse;
   p.T = T;
   p.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+#ifdef SLP_DEBUG_BOUNDS
+  {
+    const uint64_t n = static_cast<uint64_t>(N);
+    P.bnd = dbg::make(err, {{h, 2 * n * d}, {t, 4 * n}, {mask, n}, {logprob, 4 * n},
+                            {lse, 4 * n}});
+    const Layout& L = P.L;
+    auto sec = [&](size_t lo, size_t hi) { dbg_add(P.bnd, w + lo, hi - lo); };
+    sec(L.off_counters, L.off_rcnt);
+    sec(L.off_rcnt, L.off_pos);
+    sec(L.off_pos, L.off_idx);
+    sec(L.off_idx, L.off_hc);
+    sec(L.off_hc, L.off_pm);
+    if (logprob != nullptr) {  // forward: the slab partials
+      sec(L.off_pm, L.off_pmc);
+      sec(L.off_pmc, L.off_ps);
+      sec(L.off_ps, L.off_pxt);
+      sec(L.off_pxt, L.fwd_end);
+    } else {  // backward: dz chunk, split-K partials, dh accumulator
+      sec(L.off_dz, L.off_pf32);
+      sec(L.off_pf32, L.off_acc);
+      sec(L.off_acc, L.bwd_end);
+    }
+  }
+#endif
   lmh_scan_kernel<<<1, 1024, 0, stream>>>(mask, p.N, counters, P.pos, idx, p.row_cnt,
-                                          (P.L.Mcap / BM) * 4, logprob, lse);
+                                          (P.L.Mcap / BM) * 4, logprob, lse
+                                          SLP_DBG_PASS(P.bnd));
   lmh_gather_kernel<<<cdiv(p.N + kRowRound, kGatherWarps), 32 * kGatherWarps, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(h), p.N,
-                                                 p.d, counters, P.pos, P.hc);
+      static_cast<const __nv_bfloat16*>(h), p.N, p.d, counters, P.pos, P.hc
+      SLP_DBG_PASS(P.bnd));
   return cudaGetLastError();
 }
 
@@ -1088,7 +1126,8 @@ cudaError_t launch_lmhead_forward(const void* h, const void* W, int64_t N, int64
   if (!make_map(&ma, P.hc, d, P.L.Mcap, d * 2, BK, BM) ||
       !make_map(&mb, W, d, V, d * 2, BK, brows))
     return cudaErrorInvalidValue;
-  return launch<EPI_LSE, false, false>(P.L, ma, mb, P.p, stream);
+  SLP_DBG_ONLY(dbg_add(P.bnd, W, 2ull * V * d);)
+  return launch<EPI_LSE, false, false>(P.L, ma, mb, P.p, stream SLP_DBG_PASS(P.bnd));
 }
 
 cudaError_t launch_lmhead_backward(const void* h, const void* W, int64_t N, int64_t V, int64_t d,
@@ -1103,6 +1142,13 @@ cudaError_t launch_lmhead_backward(const void* h, const void* W, int64_t N, int6
   if (e != cudaSuccess) return e;
   P.p.g = grad_out;
   P.p.lse = lse;
+#ifdef SLP_DEBUG_BOUNDS
+  dbg_add(P.bnd, W, 2ull * V * d);
+  dbg_add(P.bnd, grad_out, 4ull * N);
+  dbg_add(P.bnd, lse, 4ull * N);
+  dbg_add(P.bnd, dh, 2ull * N * d);
+  dbg_add(P.bnd, dW, (accumulate_f32 ? 4ull : 2ull) * V * d);
+#endif
   CUtensorMap m_hc_k, m_hc_mn;
   if (!make_map(&m_hc_k, P.hc, d, P.L.Mcap, d * 2, BK, BM) ||    // A of recompute
       !make_map(&m_hc_mn, P.hc, d, P.L.Mcap, d * 2, 64, BK))     // B of dW (N = d)
@@ -1126,17 +1172,18 @@ cudaError_t launch_lmhead_backward(const void* h, const void* W, int64_t N, int6
         !make_map(&m_w_mn, Wc, d, vc, d * 2, 64, BK) ||               // B of dh (N = d)
         !make_map(&m_dz_mn, pc.dz, vc, P.L.Mcap, dz_row, 64, BK))     // A of dW (M = chunk)
       return cudaErrorInvalidValue;
-    e = launch<EPI_DZ, false, false>(P.L, m_hc_k, m_w_k, pc, stream);
+    e = launch<EPI_DZ, false, false>(P.L, m_hc_k, m_w_k, pc, stream SLP_DBG_PASS(P.bnd));
     if (e != cudaSuccess) return e;
-    e = launch<EPI_F32, false, true>(P.L, m_dz_k, m_w_mn, pc, stream);
+    e = launch<EPI_F32, false, true>(P.L, m_dz_k, m_w_mn, pc, stream SLP_DBG_PASS(P.bnd));
     if (e != cudaSuccess) return e;
     pc.dh_fold = 1;
-    e = accumulate_f32 ? launch<EPI_ACC32, true, true>(P.L, m_dz_mn, m_hc_mn, pc, stream)
-                       : launch<EPI_BF16, true, true>(P.L, m_dz_mn, m_hc_mn, pc, stream);
+    e = accumulate_f32
+            ? launch<EPI_ACC32, true, true>(P.L, m_dz_mn, m_hc_mn, pc, stream SLP_DBG_PASS(P.bnd))
+            : launch<EPI_BF16, true, true>(P.L, m_dz_mn, m_hc_mn, pc, stream SLP_DBG_PASS(P.bnd));
     if (e != cudaSuccess) return e;
   }
-  lmh_dh_finish_kernel<<<static_cast<int>(N), 256, 0, stream>>>(P.p, P.pos,
-                                                                static_cast<__nv_bfloat16*>(dh));
+  lmh_dh_finish_kernel<<<static_cast<int>(N), 256, 0, stream>>>(
+      P.p, P.pos, static_cast<__nv_bfloat16*>(dh) SLP_DBG_PASS(P.bnd));
   return cudaGetLastError();
 }
 

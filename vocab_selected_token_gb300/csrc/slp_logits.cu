@@ -61,7 +61,8 @@ __global__ void __launch_bounds__(kFwdThreads)
     slp_fwd_kernel(const Elt* __restrict__ x, int64_t V, int64_t ld,
                    const int32_t* __restrict__ t, const uint8_t* __restrict__ mask, float T,
                    float c, float* __restrict__ logprob, float* __restrict__ lse,
-                   float* __restrict__ entropy, int32_t* __restrict__ err, int splits) {
+                   float* __restrict__ entropy, int32_t* __restrict__ err, int splits SLP_DBG_PARAM) {
+  SLP_DBG_ENTER();
   using E = Elem<Elt>;
   constexpr int kVec = E::kVec;
   constexpr int kWarps = kFwdThreads / 32;
@@ -74,17 +75,17 @@ __global__ void __launch_bounds__(kFwdThreads)
   const int rank = static_cast<int>(blockIdx.x - row * splits);
   // Every CTA of a cluster handles the same row, so all of them leave here
   // together (no cluster barrier is left waiting).
-  if (mask != nullptr && mask[row] == 0) {
+  if (mask != nullptr && dbg::ld(mask + row) == 0) {
     if (rank == 0 && threadIdx.x == 0) {
-      if (logprob != nullptr) logprob[row] = 0.f;
-      lse[row] = 0.f;
-      if (kEnt) entropy[row] = 0.f;
+      if (logprob != nullptr) dbg::st(logprob + row, 0.f);
+      dbg::st(lse + row, 0.f);
+      if (kEnt) dbg::st(entropy + row, 0.f);
     }
     return;
   }
   const Elt* xr = x + row * ld;
   // t == NULL: log-sum-exp only (no target, logprob not written)
-  const int32_t tt = t != nullptr ? t[row] : 0;
+  const int32_t tt = t != nullptr ? dbg::ld(t + row) : 0;
   const bool tvalid = tt >= 0 && static_cast<int64_t>(tt) < V;
   float xt = 0.f;
   if (rank == 0 && threadIdx.x == 0 && tvalid) xt = E::load1(xr + tt);
@@ -254,18 +255,19 @@ __global__ void __launch_bounds__(32 * kRowsWarps)
     slp_fwd_rows_kernel(const Elt* __restrict__ x, int64_t N, int64_t V, int64_t ld,
                         const int32_t* __restrict__ t, const uint8_t* __restrict__ mask, float T,
                         float c, float* __restrict__ logprob, float* __restrict__ lse,
-                        float* __restrict__ entropy, int32_t* __restrict__ err) {
+                        float* __restrict__ entropy, int32_t* __restrict__ err SLP_DBG_PARAM) {
+  SLP_DBG_ENTER();
   using E = Elem<Elt>;
   constexpr int kVec = E::kVec;
   constexpr bool kEnt = sizeof(St) == sizeof(Lse3);
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kRowsWarps + (threadIdx.x >> 5);
   if (row >= N) return;
-  if (mask != nullptr && mask[row] == 0) {
+  if (mask != nullptr && dbg::ld(mask + row) == 0) {
     if (lane == 0) {
-      if (logprob != nullptr) logprob[row] = 0.f;
-      lse[row] = 0.f;
-      if (kEnt) entropy[row] = 0.f;
+      if (logprob != nullptr) dbg::st(logprob + row, 0.f);
+      dbg::st(lse + row, 0.f);
+      if (kEnt) dbg::st(entropy + row, 0.f);
     }
     return;
   }
@@ -293,7 +295,7 @@ __global__ void __launch_bounds__(32 * kRowsWarps)
   }
   st = st_warp_reduce(st);
   if (lane == 0) {
-    const int32_t tt = t != nullptr ? t[row] : 0;
+    const int32_t tt = t != nullptr ? dbg::ld(t + row) : 0;
     const bool tvalid = tt >= 0 && static_cast<int64_t>(tt) < V;
     const float xt = tvalid ? E::load1(xr + tt) : 0.f;
     if constexpr (kEnt)
@@ -323,14 +325,14 @@ struct BwdRow {
                                        float c, const float* lse, const float* g, const float* H,
                                        const float* gH, int32_t* err, bool report) {
     const Elt* tag = nullptr;
-    tt = t[row];
-    gT = (kEnt && g == nullptr) ? 0.f : g[row] * invT;
-    L2 = lse[row] * kLog2e;
+    tt = dbg::ld(t + row);
+    gT = (kEnt && g == nullptr) ? 0.f : dbg::ld(g + row) * invT;
+    L2 = dbg::ld(lse + row) * kLog2e;
     float gHT = 0.f;
     Hl2 = 0.f;
     if (kEnt) {
-      gHT = gH == nullptr ? 0.f : gH[row] * invT;
-      Hl2 = H[row] * kLog2e;  // log p_v + H = ln 2 (log2 p_v + H log2 e)
+      gHT = gH == nullptr ? 0.f : dbg::ld(gH + row) * invT;
+      Hl2 = dbg::ld(H + row) * kLog2e;  // log p_v + H = ln 2 (log2 p_v + H log2 e)
     }
     if (tt < 0 || tt >= V) {
       if (err != nullptr && report) atomicOr(err, SLP_DATA_ERR_TARGET);
@@ -390,14 +392,15 @@ __global__ void __launch_bounds__(kBwdThreads, kEnt ? 6 : 1)
                    float c, const float* __restrict__ lse, const float* __restrict__ g,
                    const float* __restrict__ H, const float* __restrict__ gH,
                    Elt* __restrict__ gx, int64_t ldg, int32_t* __restrict__ err,
-                   int64_t tiles_per_row) {
+                   int64_t tiles_per_row SLP_DBG_PARAM) {
+  SLP_DBG_ENTER();
   using E = Elem<Elt>;
   constexpr int kVec = E::kVec;
   constexpr int64_t kTileElems = static_cast<int64_t>(kBwdThreads) * kBwdUnroll * kVec;
 
   const int64_t row = blockIdx.x / tiles_per_row;
   const int64_t tile = blockIdx.x - row * tiles_per_row;
-  const bool active = mask == nullptr || mask[row] != 0;
+  const bool active = mask == nullptr || dbg::ld(mask + row) != 0;
   const Elt* xr = x + row * ld;
   Elt* gr = gx + row * ldg;
   const int64_t e_tile = tile * kTileElems;
@@ -455,7 +458,8 @@ __global__ void __launch_bounds__(32 * kRowsWarps)
                         float invT, float c, const float* __restrict__ lse,
                         const float* __restrict__ g, const float* __restrict__ H,
                         const float* __restrict__ gH, Elt* __restrict__ gx, int64_t ldg,
-                        int32_t* __restrict__ err) {
+                        int32_t* __restrict__ err SLP_DBG_PARAM) {
+  SLP_DBG_ENTER();
   using E = Elem<Elt>;
   constexpr int kVec = E::kVec;
   const int lane = threadIdx.x & 31;
@@ -464,7 +468,7 @@ __global__ void __launch_bounds__(32 * kRowsWarps)
   const int64_t nvec = V / kVec;
   Elt* gr = gx + row * ldg;
   uint4* gv = reinterpret_cast<uint4*>(gr);
-  if (mask != nullptr && mask[row] == 0) {
+  if (mask != nullptr && dbg::ld(mask + row) == 0) {
     const uint4 z = make_uint4(0u, 0u, 0u, 0u);
     for (int64_t i = lane; i < nvec; i += 32) st_stream(gv + i, z);
     for (int64_t e = nvec * kVec + lane; e < V; e += 32) E::store1(gr + e, 0.f);
@@ -536,7 +540,8 @@ __global__ void __launch_bounds__(kFbThreads, kRV > 0 ? 4 : 1)
                        float c, float invT, const float* __restrict__ g,
                        const float* __restrict__ gH, float* __restrict__ logprob,
                        float* __restrict__ lse, float* __restrict__ entropy,
-                       Elt* __restrict__ gx, int64_t ldg, int32_t* __restrict__ err, int C) {
+                       Elt* __restrict__ gx, int64_t ldg, int32_t* __restrict__ err, int C SLP_DBG_PARAM) {
+  SLP_DBG_ENTER();
   using E = Elem<Elt>;
   using St = typename std::conditional<kEnt, Lse3, Lse2>::type;
   constexpr int kVec = E::kVec;
@@ -562,26 +567,26 @@ __global__ void __launch_bounds__(kFbThreads, kRV > 0 ? 4 : 1)
 
   // Inactive rows: every CTA of the cluster writes zeros and leaves; none of
   // them touches a cluster barrier.
-  if (mask != nullptr && mask[row] == 0) {
+  if (mask != nullptr && dbg::ld(mask + row) == 0) {
     const uint4 z = make_uint4(0u, 0u, 0u, 0u);
     for (int i = threadIdx.x; i < nv; i += kFbThreads) st_stream(gv + i, z);
     if (rank == C - 1)
       for (int64_t e = nvec * kVec + threadIdx.x; e < V; e += kFbThreads)
         E::store1(gx + row * ldg + e, 0.f);
     if (rank == 0 && threadIdx.x == 0) {
-      logprob[row] = 0.f;
-      lse[row] = 0.f;
-      if (kEnt) entropy[row] = 0.f;
+      dbg::st(logprob + row, 0.f);
+      dbg::st(lse + row, 0.f);
+      if (kEnt) dbg::st(entropy + row, 0.f);
     }
     return;
   }
 
   const Elt* xr = x + row * ld;
-  const int32_t tt = t[row];
+  const int32_t tt = dbg::ld(t + row);
   const bool tvalid = tt >= 0 && static_cast<int64_t>(tt) < V;
   float xt = 0.f;
   if (rank == 0 && threadIdx.x == 0 && tvalid) xt = E::load1(xr + tt);
-  const float gT = tvalid ? ((kEnt && g == nullptr) ? 0.f : g[row] * invT)
+  const float gT = tvalid ? ((kEnt && g == nullptr) ? 0.f : dbg::ld(g + row) * invT)
                           : __int_as_float(0x7FC00000);
 
   const int seg_bytes = nv_s * 16;
@@ -729,7 +734,7 @@ __global__ void __launch_bounds__(kFbThreads, kRV > 0 ? 4 : 1)
       Hl20 = H * kLog2e;
     }
     BwdRow<Elt, true> b;
-    b.set(tt, gT, L20, gH != nullptr ? gH[row] * invT : 0.f, Hl20, c);
+    b.set(tt, gT, L20, gH != nullptr ? dbg::ld(gH + row) * invT : 0.f, Hl20, c);
     const int64_t rel0 = static_cast<int64_t>(tt) - v0 * kVec;  // target offset in segment
     const int64_t tvec = rel0 >= 0 ? rel0 / kVec : -1;
     Elt* gr = gx + row * ldg;
@@ -814,7 +819,8 @@ __global__ void __launch_bounds__(32 * kFbRowsWarps, kNV >= 16 ? 4 : (kEnt && kN
                             const float* __restrict__ gH, float* __restrict__ logprob,
                             float* __restrict__ lse, float* __restrict__ entropy,
                             Elt* __restrict__ gx, int64_t ldg, int32_t* __restrict__ err,
-                            int slot_bytes) {
+                            int slot_bytes SLP_DBG_PARAM) {
+  SLP_DBG_ENTER();
   using E = Elem<Elt>;
   using St = typename std::conditional<kEnt, Lse3, Lse2>::type;
   constexpr int kVec = E::kVec;
@@ -826,14 +832,14 @@ __global__ void __launch_bounds__(32 * kFbRowsWarps, kNV >= 16 ? 4 : (kEnt && kN
   const int64_t nvec = V / kVec;
   Elt* gr = gx + row * ldg;
   uint4* gv = reinterpret_cast<uint4*>(gr);
-  if (mask != nullptr && mask[row] == 0) {
+  if (mask != nullptr && dbg::ld(mask + row) == 0) {
     const uint4 z = make_uint4(0u, 0u, 0u, 0u);
     for (int64_t i = lane; i < nvec; i += 32) st_stream(gv + i, z);
     for (int64_t e = nvec * kVec + lane; e < V; e += 32) E::store1(gr + e, 0.f);
     if (lane == 0) {
-      logprob[row] = 0.f;
-      lse[row] = 0.f;
-      if (kEnt) entropy[row] = 0.f;
+      dbg::st(logprob + row, 0.f);
+      dbg::st(lse + row, 0.f);
+      if (kEnt) dbg::st(entropy + row, 0.f);
     }
     return;
   }
@@ -852,9 +858,9 @@ __global__ void __launch_bounds__(32 * kFbRowsWarps, kNV >= 16 ? 4 : (kEnt && kN
     }
     __syncwarp();  // the barrier's initialisation is seen by every lane
   }
-  const int32_t tt = t[row];
+  const int32_t tt = dbg::ld(t + row);
   const bool tvalid = tt >= 0 && static_cast<int64_t>(tt) < V;
-  const float gT = tvalid ? ((kEnt && g == nullptr) ? 0.f : g[row] * invT)
+  const float gT = tvalid ? ((kEnt && g == nullptr) ? 0.f : dbg::ld(g + row) * invT)
                           : __int_as_float(0x7FC00000);
   const uint4 pad = make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord, E::kNegInfWord);
   uint4 rv[kNV];
@@ -915,7 +921,7 @@ __global__ void __launch_bounds__(32 * kFbRowsWarps, kNV >= 16 ? 4 : (kEnt && kN
       Hl20 = H * kLog2e;
     }
     BwdRow<Elt, true> b;
-    b.set(tt, gT, L20, gH != nullptr ? gH[row] * invT : 0.f, Hl20, c);
+    b.set(tt, gT, L20, gH != nullptr ? dbg::ld(gH + row) * invT : 0.f, Hl20, c);
     const int64_t tvec = tvalid ? static_cast<int64_t>(tt) / kVec : -1;
     auto put = [&](int64_t i, const uint4& v) {
       st_stream(gv + i, b.vec(v));
@@ -989,7 +995,9 @@ cudaError_t fwd_typed(const Elt* x, int64_t N, int64_t V, int64_t ld, const int3
     if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
     const float c = static_cast<float>(1.4426950408889634 / static_cast<double>(T));
     slp_fwd_rows_kernel<Elt, St><<<static_cast<unsigned>(blocks), 32 * kRowsWarps, 0, stream>>>(
-        x, N, V, ld, t, mask, T, c, logprob, lse, entropy, err);
+        x, N, V, ld, t, mask, T, c, logprob, lse, entropy, err
+        SLP_DBG_ARG(err, {dbg::rows(x, N, V, ld, sizeof(Elt)), {t, 4ull * N}, {mask, 1ull * N},
+                            {logprob, 4ull * N}, {lse, 4ull * N}, {entropy, 4ull * N}}));
     return cudaGetLastError();
   }
   const int splits = choose_splits(N, V);
@@ -1017,9 +1025,13 @@ cudaError_t fwd_typed(const Elt* x, int64_t N, int64_t V, int64_t ld, const int3
   }
   if (vec)
     return cudaLaunchKernelEx(&cfg, slp_fwd_kernel<Elt, true, St>, x, V, ld, t, mask, T, c,
-                              logprob, lse, entropy, err, splits);
+                              logprob, lse, entropy, err, splits
+                              SLP_DBG_ARG(err, {dbg::rows(x, N, V, ld, sizeof(Elt)), {t, 4ull * N}, {mask, 1ull * N},
+                            {logprob, 4ull * N}, {lse, 4ull * N}, {entropy, 4ull * N}}));
   return cudaLaunchKernelEx(&cfg, slp_fwd_kernel<Elt, false, St>, x, V, ld, t, mask, T, c, logprob,
-                            lse, entropy, err, splits);
+                            lse, entropy, err, splits
+                            SLP_DBG_ARG(err, {dbg::rows(x, N, V, ld, sizeof(Elt)), {t, 4ull * N}, {mask, 1ull * N},
+                            {logprob, 4ull * N}, {lse, 4ull * N}, {entropy, 4ull * N}}));
 }
 
 // Rows of at most 64 KB that fill less than 90 % of their tiles of the
@@ -1050,15 +1062,24 @@ cudaError_t bwd_typed(const Elt* x, int64_t N, int64_t V, int64_t ld, const int3
   if (vec && use_bwd_rows_kernel(N, V * static_cast<int64_t>(sizeof(Elt)))) {
     const int64_t rblocks = (N + kRowsWarps - 1) / kRowsWarps;
     slp_bwd_rows_kernel<Elt, kEnt><<<static_cast<unsigned>(rblocks), 32 * kRowsWarps, 0, stream>>>(
-        x, N, V, ld, t, mask, invT, c, lse, g, H, gH, gx, ldg, err);
+        x, N, V, ld, t, mask, invT, c, lse, g, H, gH, gx, ldg, err
+        SLP_DBG_ARG(err, {dbg::rows(x, N, V, ld, sizeof(Elt)), {t, 4ull * N}, {mask, 1ull * N},
+                            {lse, 4ull * N}, {g, 4ull * N}, {H, 4ull * N}, {gH, 4ull * N},
+                            dbg::rows(gx, N, V, ldg, sizeof(Elt))}));
     return cudaGetLastError();
   }
   if (vec)
     slp_bwd_kernel<Elt, true, kEnt><<<static_cast<unsigned>(blocks), kBwdThreads, 0, stream>>>(
-        x, V, ld, t, mask, invT, c, lse, g, H, gH, gx, ldg, err, tiles);
+        x, V, ld, t, mask, invT, c, lse, g, H, gH, gx, ldg, err, tiles
+        SLP_DBG_ARG(err, {dbg::rows(x, N, V, ld, sizeof(Elt)), {t, 4ull * N}, {mask, 1ull * N},
+                            {lse, 4ull * N}, {g, 4ull * N}, {H, 4ull * N}, {gH, 4ull * N},
+                            dbg::rows(gx, N, V, ldg, sizeof(Elt))}));
   else
     slp_bwd_kernel<Elt, false, kEnt><<<static_cast<unsigned>(blocks), kBwdThreads, 0, stream>>>(
-        x, V, ld, t, mask, invT, c, lse, g, H, gH, gx, ldg, err, tiles);
+        x, V, ld, t, mask, invT, c, lse, g, H, gH, gx, ldg, err, tiles
+        SLP_DBG_ARG(err, {dbg::rows(x, N, V, ld, sizeof(Elt)), {t, 4ull * N}, {mask, 1ull * N},
+                            {lse, 4ull * N}, {g, 4ull * N}, {H, 4ull * N}, {gH, 4ull * N},
+                            dbg::rows(gx, N, V, ldg, sizeof(Elt))}));
   return cudaGetLastError();
 }
 
@@ -1090,7 +1111,9 @@ cudaError_t fwd_bwd_rows_launch(const Elt* x, int64_t N, int64_t V, int64_t ld, 
   slp_fwd_bwd_rows_kernel<Elt, kNV, kEnt>
       <<<static_cast<unsigned>(blocks), 32 * kFbRowsWarps, smem, stream>>>(
           x, N, V, ld, t, mask, T, c, 1.0f / T, g, gH, logprob, lse, entropy, gx, ldg, err,
-          slot_bytes);
+          slot_bytes SLP_DBG_ARG(err, {dbg::rows(x, N, V, ld, sizeof(Elt)), {t, 4ull * N}, {mask, 1ull * N},
+                            {g, 4ull * N}, {gH, 4ull * N}, {logprob, 4ull * N}, {lse, 4ull * N},
+                            {entropy, 4ull * N}, dbg::rows(gx, N, V, ldg, sizeof(Elt))}));
   return cudaGetLastError();
 }
 
@@ -1161,7 +1184,10 @@ cudaError_t fwd_bwd_typed(const Elt* x, int64_t N, int64_t V, int64_t ld, const 
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, x, V, ld, t, mask, T, c, invT, g, gH, logprob, lse,
-                            entropy, gx, ldg, err, static_cast<int>(C));
+                            entropy, gx, ldg, err, static_cast<int>(C)
+                            SLP_DBG_ARG(err, {dbg::rows(x, N, V, ld, sizeof(Elt)), {t, 4ull * N}, {mask, 1ull * N},
+                            {g, 4ull * N}, {gH, 4ull * N}, {logprob, 4ull * N}, {lse, 4ull * N},
+                            {entropy, 4ull * N}, dbg::rows(gx, N, V, ldg, sizeof(Elt))}));
 }
 
 }  // namespace

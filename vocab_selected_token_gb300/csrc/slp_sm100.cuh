@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "slp_bounds.cuh"
+
 namespace slp {
 namespace sm100 {
 
@@ -125,9 +127,18 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int3
 }
 
 // Plain bulk copy global -> shared (both 16-byte aligned, size a multiple of
-// 16), completing on an mbarrier of this CTA.
+// 16), completing on an mbarrier of this CTA.  In the bounds-checked build a
+// copy whose source is outside the call's buffers is not issued; its bytes
+// are counted as landed so the waiters go on (with stale data, and the error
+// bit set).
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
                                           uint32_t bar) {
+  if (!dbg::ok(src, bytes)) {
+    asm volatile("mbarrier.complete_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar),
+                 "r"(bytes)
+                 : "memory");
+    return;
+  }
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
           dst),

@@ -50,27 +50,32 @@ __global__ void __launch_bounds__(256)
                             const uint8_t* __restrict__ mask, float invT, float clamp_min,
                             const float* __restrict__ lse, float* __restrict__ kl,
                             float* __restrict__ smass, float* __restrict__ tmass,
-                            int32_t* __restrict__ err) {
+                            int32_t* __restrict__ err SLP_DBG_PARAM) {
+  SLP_DBG_ENTER();
   using E = Elem<Elt>;
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
   if (row >= N) return;
-  if (mask != nullptr && mask[row] == 0) {
-    if (lane == 0) kl[row] = smass[row] = tmass[row] = 0.f;
+  if (mask != nullptr && dbg::ld(mask + row) == 0) {
+    if (lane == 0) {
+      dbg::st(kl + row, 0.f);
+      dbg::st(smass + row, 0.f);
+      dbg::st(tmass + row, 0.f);
+    }
     return;
   }
-  const float L = lse[row];
+  const float L = dbg::ld(lse + row);
   const Elt* xr = x + row * ld;
   float a_kl = 0.f, a_sm = 0.f, a_tm = 0.f;
   bool bad = false;
   for (int k = lane; k < K; k += 32) {
-    const int id = ids[row * K + k];
+    const int id = dbg::ld(ids + row * K + k);
     if (id < 0 || static_cast<int64_t>(id) >= V) {
       bad = true;
       continue;
     }
     const float ls = fmaf(E::load1(xr + id), invT, -L);
-    const float tk = lt[row * K + k];
+    const float tk = dbg::ld(lt + row * K + k);
     const float p = expf(tk);
     a_kl = fmaf(p, tk - fmaxf(ls, clamp_min), a_kl);
     a_sm += expf(ls);
@@ -85,9 +90,9 @@ __global__ void __launch_bounds__(256)
       if (err != nullptr) atomicOr(err, SLP_DATA_ERR_TARGET);
       a_kl = a_sm = a_tm = __int_as_float(0x7FC00000);
     }
-    kl[row] = a_kl;
-    smass[row] = a_sm;
-    tmass[row] = a_tm;
+    dbg::st(kl + row, a_kl);
+    dbg::st(smass + row, a_sm);
+    dbg::st(tmass + row, a_tm);
   }
 }
 
@@ -98,7 +103,8 @@ __global__ void __launch_bounds__(kTkThreads)
                            const uint8_t* __restrict__ mask, float invT, float c,
                            float clamp_min, const float* __restrict__ lse,
                            const float* __restrict__ g, Elt* __restrict__ gx, int64_t ldg,
-                           int32_t* __restrict__ err) {
+                           int32_t* __restrict__ err SLP_DBG_PARAM) {
+  SLP_DBG_ENTER();
   using E = Elem<Elt>;
   constexpr int kVec = E::kVec;
   extern __shared__ __align__(128) uint8_t tk_smem[];
@@ -108,7 +114,7 @@ __global__ void __launch_bounds__(kTkThreads)
   Elt* gr = gx + row * ldg;
   const int64_t nvec = kVecPath ? V / kVec : 0;
 
-  if (mask != nullptr && mask[row] == 0) {
+  if (mask != nullptr && dbg::ld(mask + row) == 0) {
     if (kVecPath) {
       uint4* gv = reinterpret_cast<uint4*>(gr);
       for (int64_t i = threadIdx.x; i < nvec; i += kTkThreads) st_stream(gv + i, make_uint4(0, 0, 0, 0));
@@ -121,20 +127,20 @@ __global__ void __launch_bounds__(kTkThreads)
   uint8_t* ring = tk_smem;                                        // kTkRing bytes (vector path)
   int* sid = reinterpret_cast<int*>(tk_smem + (kVecPath ? kTkRing : 0));
   float* sp = reinterpret_cast<float*>(sid + K);
-  const float L = lse[row];
+  const float L = dbg::ld(lse + row);
   const float L2 = L * kLog2e;
-  float gT = g[row] * invT;
+  float gT = dbg::ld(g + row) * invT;
   float pl = 0.f;
   bool bad = false;
   for (int k = threadIdx.x; k < K; k += kTkThreads) {
-    const int id = ids[row * K + k];
+    const int id = dbg::ld(ids + row * K + k);
     float p = 0.f;
     if (id < 0 || static_cast<int64_t>(id) >= V) {
       bad = true;
       sid[k] = -1;
     } else {
       const float ls = fmaf(E::load1(xr + id), invT, -L);
-      p = ls >= clamp_min ? expf(lt[row * K + k]) : 0.f;
+      p = ls >= clamp_min ? expf(dbg::ld(lt + row * K + k)) : 0.f;
       sid[k] = id;
     }
     sp[k] = p;
@@ -266,7 +272,8 @@ __global__ void __launch_bounds__(32 * kTkRowsWarps)
                                 int K, const uint8_t* __restrict__ mask, float invT, float c,
                                 float clamp_min, const float* __restrict__ lse,
                                 const float* __restrict__ g, Elt* __restrict__ gx, int64_t ldg,
-                                int32_t* __restrict__ err) {
+                                int32_t* __restrict__ err SLP_DBG_PARAM) {
+  SLP_DBG_ENTER();
   using E = Elem<Elt>;
   constexpr int kVec = E::kVec;
   extern __shared__ __align__(16) int tk_rows_smem[];
@@ -277,7 +284,7 @@ __global__ void __launch_bounds__(32 * kTkRowsWarps)
   Elt* gr = gx + row * ldg;
   uint4* gv = reinterpret_cast<uint4*>(gr);
   const int64_t nvec = V / kVec;
-  if (mask != nullptr && mask[row] == 0) {
+  if (mask != nullptr && dbg::ld(mask + row) == 0) {
     for (int64_t i = lane; i < nvec; i += 32) st_stream(gv + i, make_uint4(0, 0, 0, 0));
     for (int64_t e = nvec * kVec + lane; e < V; e += 32) E::store1(gr + e, 0.f);
     return;
@@ -298,20 +305,20 @@ __global__ void __launch_bounds__(32 * kTkRowsWarps)
     const int64_t i = lane + 32 * u;
     if (i < nvec) v[u] = ld_stream(xv + i);
   }
-  const float L = lse[row];
+  const float L = dbg::ld(lse + row);
   const float L2 = L * kLog2e;
-  float gT = g[row] * invT;
+  float gT = dbg::ld(g + row) * invT;
   float pl = 0.f;
   bool bad = false;
   for (int k = lane; k < K; k += 32) {
-    const int id = ids[row * K + k];
+    const int id = dbg::ld(ids + row * K + k);
     float p = 0.f;
     if (id < 0 || static_cast<int64_t>(id) >= V) {
       bad = true;
       sid[k] = -1;
     } else {
       const float ls = fmaf(E::load1(xr + id), invT, -L);
-      p = ls >= clamp_min ? expf(lt[row * K + k]) : 0.f;
+      p = ls >= clamp_min ? expf(dbg::ld(lt + row * K + k)) : 0.f;
       sid[k] = id;
     }
     sp[k] = p;
@@ -401,7 +408,10 @@ cudaError_t topk_bwd_typed(const Elt* x, int64_t N, int64_t V, int64_t ld, const
     const size_t smem = static_cast<size_t>(kTkRowsWarps) * ((K + 3) & ~3) * 8;
     slp_topk_kl_bwd_rows_kernel<Elt><<<static_cast<unsigned>(blocks), 32 * kTkRowsWarps, smem,
                                        stream>>>(x, N, V, ld, ids, lt, K, mask, invT, c,
-                                                 clamp_min, lse, g, gx, ldg, err);
+                                                 clamp_min, lse, g, gx, ldg, err
+                                                 SLP_DBG_ARG(err, {dbg::rows(x, N, V, ld, sizeof(Elt)), {ids, 4ull * N * K},
+                                  {lt, 4ull * N * K}, {mask, 1ull * N}, {lse, 4ull * N},
+                                  {g, 4ull * N}, dbg::rows(gx, N, V, ldg, sizeof(Elt))}));
     return cudaGetLastError();
   }
   auto k = vec ? slp_topk_kl_bwd_kernel<Elt, true> : slp_topk_kl_bwd_kernel<Elt, false>;
@@ -410,7 +420,10 @@ cudaError_t topk_bwd_typed(const Elt* x, int64_t N, int64_t V, int64_t ld, const
                                        kTkMaxSmem + kTkRing);
   if (e != cudaSuccess) return e;
   k<<<static_cast<unsigned>(N), kTkThreads, static_cast<size_t>(smem), stream>>>(
-      x, V, ld, ids, lt, K, mask, invT, c, clamp_min, lse, g, gx, ldg, err);
+      x, V, ld, ids, lt, K, mask, invT, c, clamp_min, lse, g, gx, ldg, err
+      SLP_DBG_ARG(err, {dbg::rows(x, N, V, ld, sizeof(Elt)), {ids, 4ull * N * K},
+                                  {lt, 4ull * N * K}, {mask, 1ull * N}, {lse, 4ull * N},
+                                  {g, 4ull * N}, dbg::rows(gx, N, V, ldg, sizeof(Elt))}));
   return cudaGetLastError();
 }
 
@@ -430,11 +443,17 @@ cudaError_t launch_topk_kl_forward(const void* x, int dtype, int64_t N, int64_t 
   if (dtype == SLP_BF16)
     slp_topk_kl_rows_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(x), N, V, ld, ids, teacher_logp, static_cast<int>(K),
-        mask, invT, clamp_min, lse, kl, student_mass, teacher_mass, err);
+        mask, invT, clamp_min, lse, kl, student_mass, teacher_mass, err
+        SLP_DBG_ARG(err, {dbg::rows(x, N, V, ld, 2), {ids, 4ull * N * K},
+                          {teacher_logp, 4ull * N * K}, {mask, 1ull * N}, {lse, 4ull * N},
+                          {kl, 4ull * N}, {student_mass, 4ull * N}, {teacher_mass, 4ull * N}}));
   else
     slp_topk_kl_rows_kernel<float><<<blocks, 256, 0, stream>>>(
         static_cast<const float*>(x), N, V, ld, ids, teacher_logp, static_cast<int>(K), mask,
-        invT, clamp_min, lse, kl, student_mass, teacher_mass, err);
+        invT, clamp_min, lse, kl, student_mass, teacher_mass, err
+        SLP_DBG_ARG(err, {dbg::rows(x, N, V, ld, 4), {ids, 4ull * N * K},
+                          {teacher_logp, 4ull * N * K}, {mask, 1ull * N}, {lse, 4ull * N},
+                          {kl, 4ull * N}, {student_mass, 4ull * N}, {teacher_mass, 4ull * N}}));
   return cudaGetLastError();
 }
 
