@@ -130,8 +130,9 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, device):
+    def __init__(self, device, interval_ms=200):
         self.proc = None
+        self.interval_ms = int(interval_ms)
         try:
             uuid = str(torch.cuda.get_device_properties(device).uuid)
             ident = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
@@ -143,7 +144,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", self.ident, f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.interval_ms)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -693,11 +694,12 @@ def time_fused(device, hbm, steps=30, warmup=3):
     return out
 
 
-def time_lmhead(device, steps=10, warmup=3, N=None):
+def time_lmhead(device, steps=40, warmup=3, N=None):
     """Fused LM-head forward and backward on the lmhead workload (N=8192,
     d=2560, V=151936, Bernoulli(0.5) mask), each call timed whole with CUDA
     events; TFLOP/s counts 2*Na*V*d for the forward and 6*Na*V*d for the
-    backward (logits recompute, dh and dW GEMMs)."""
+    backward (logits recompute, dh and dW GEMMs).  SM clocks are sampled
+    every 50 ms during the timed steps (about 0.3 s of back-to-back GEMMs)."""
     from vocab_selected_token_gb300 import _lib
     from vocab_selected_token_gb300 import workloads as W
     lib = _lib.load()
@@ -721,6 +723,8 @@ def time_lmhead(device, steps=10, warmup=3, N=None):
         assert lib.slp_lmhead_forward(*fa) == 0
         assert lib.slp_lmhead_backward(*ba) == 0
     torch.cuda.synchronize(device)
+    clocks = ClockSampler(device, interval_ms=50)
+    clocks.start()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
     for i in range(steps):
         ev[i][0].record(s)
@@ -729,6 +733,7 @@ def time_lmhead(device, steps=10, warmup=3, N=None):
         assert lib.slp_lmhead_backward(*ba) == 0
         ev[i][2].record(s)
     torch.cuda.synchronize(device)
+    clk = clocks.stop()
     f_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
     b_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / steps
     flop_f = 2.0 * na * V * d
@@ -738,7 +743,7 @@ def time_lmhead(device, steps=10, warmup=3, N=None):
            "bwd_tflops": 3 * flop_f / (b_ms * 1e-3) / 1e12,
            "step_tflops": 4 * flop_f / ((f_ms + b_ms) * 1e-3) / 1e12,
            "peak_bf16_tflops": peak, "peak_bf16_tflops_sustained": peak_sus, "peak_source": src,
-           "workspace_bytes": int(ws_b)}
+           "workspace_bytes": int(ws_b), "clocks": clk}
     # the forward (~2 ms) is a burst against the burst peak; the backward and
     # the whole step (6-8 ms of back-to-back GEMMs under the power cap) are
     # also given against the sustained peak
