@@ -302,19 +302,27 @@ int slp_forward_backward_host(const void* x_host, int dtype, int64_t N, int64_t 
                               void* ws, size_t ws_bytes, int32_t* err, void* stream);
 
 /*
- * slp_lmhead_workspace_size - bytes of device workspace that
- * slp_lmhead_backward needs for these sizes (enough for slp_lmhead_forward
- * too; a larger workspace is fine).  Returns 0 for invalid sizes.
+ * slp_lmhead_workspace_size - the recommended device workspace of
+ * slp_lmhead_backward for these sizes (enough for slp_lmhead_forward too):
+ * the backward then runs in vocabulary chunks of 65536 columns.  Returns 0
+ * for invalid sizes.
+ *
+ * slp_lmhead_workspace_size_min - the least workspace slp_lmhead_backward
+ * accepts: chunks of 16384 columns, a quarter of the default dz buffer and
+ * fewer split-K partials, for more GEMM launches.  Between the two, the
+ * backward uses the widest chunk that fits (65536, 32768 or 16384 columns).
  *
  * slp_lmhead_forward_workspace_size - the smaller amount slp_lmhead_forward
  * alone needs (compacted hidden rows and per-slab log-sum-exp partials).
  *
  * The backward workspace holds the compacted rows, a bf16 dz buffer of
- * roundup(N,128) x min(V, 65536) elements (the backward runs in vocabulary
- * chunks of at most 65536 columns), float32 split-K partials of dh and a
- * float32 dh accumulator.
+ * roundup(N,256) x chunk elements, float32 split-K partials of dh and a
+ * float32 dh accumulator.  Workspaces of different chunk widths give results
+ * that agree within the LM-head tolerances, not bit for bit: the dh sums are
+ * regrouped.
  */
 size_t slp_lmhead_workspace_size(int64_t N, int64_t V, int64_t d);
+size_t slp_lmhead_workspace_size_min(int64_t N, int64_t V, int64_t d);
 size_t slp_lmhead_forward_workspace_size(int64_t N, int64_t V, int64_t d);
 
 /*
@@ -367,8 +375,10 @@ int slp_lmhead_forward(const void* h, const void* W, int64_t N, int64_t V, int64
  *   lse       [N] float32 from slp_lmhead_forward.
  *   grad_out  [N] float32.
  *   dh        [N, d] bf16 out.      dW  [V, d] bf16 out (overwritten).
- *   ws, ws_bytes  at least slp_lmhead_workspace_size(N, V, d) bytes,
- *             256-byte aligned; contents on entry do not matter.
+ *   ws, ws_bytes  at least slp_lmhead_workspace_size_min(N, V, d) bytes
+ *             (slp_lmhead_workspace_size recommended), 256-byte aligned;
+ *             contents on entry do not matter.  The chunk width follows
+ *             ws_bytes (see slp_lmhead_workspace_size).
  *   err, stream   as for slp_lmhead_forward.
  * A row whose target is outside [0, V) is flagged in *err, gets a NaN dh row
  * and contributes nothing to dW.

@@ -123,8 +123,10 @@ def test_lmhead_argument_errors(lib):
              None) == _lib.SLP_ERR_INVALID_ARG
     assert b(FAKE, FAKE, N, V, d, FAKE, None, 1.0, FAKE, FAKE, ctypes.c_void_p(0x1002), FAKE,
              FAKE, need_b, None, None) == _lib.SLP_ERR_MISALIGNED
-    # the backward needs the larger workspace
-    assert b(FAKE, FAKE, N, V, d, FAKE, None, 1.0, FAKE, FAKE, FAKE, FAKE, FAKE, need_b - 1,
+    # the backward needs at least its minimum workspace (16384-column chunks)
+    need_min = lib.slp_lmhead_workspace_size_min(N, V, d)
+    assert need <= need_min <= need_b
+    assert b(FAKE, FAKE, N, V, d, FAKE, None, 1.0, FAKE, FAKE, FAKE, FAKE, FAKE, need_min - 1,
              None, None) == _lib.SLP_ERR_WORKSPACE
 
 
@@ -379,3 +381,16 @@ def test_lmhead_workspace_size_max(lib):
         lib.slp_lmhead_workspace_size(300, 60000, 256)
     assert lib.slp_lmhead_workspace_size_max(-1, 100, 64) == 0
     assert lib.slp_lmhead_workspace_size_max(10, 100, 0) == 0
+
+
+def test_lmhead_workspace_size_min(lib):
+    """The 16384-column workspace is below the default one once the vocabulary
+    is wider than a minimum chunk, equal to it otherwise, still holds the
+    forward's workspace, and is 0 for invalid sizes."""
+    small = lib.slp_lmhead_workspace_size_min(8192, 151936, 2560)
+    dflt = lib.slp_lmhead_workspace_size(8192, 151936, 2560)
+    assert lib.slp_lmhead_forward_workspace_size(8192, 151936, 2560) <= small < dflt
+    assert small < 0.4 * dflt  # a quarter of the dz buffer, fewer split-K partials
+    assert lib.slp_lmhead_workspace_size_min(300, 16000, 256) == \
+        lib.slp_lmhead_workspace_size(300, 16000, 256)
+    assert lib.slp_lmhead_workspace_size_min(-1, 100, 64) == 0

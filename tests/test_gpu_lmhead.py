@@ -233,19 +233,23 @@ def test_lmhead_matches_logits_path():
         assert cos >= 0.9999 and frob <= 1e-2, f"{what}: cosine {cos:.6f} frob {frob:.3e}"
 
 
-@pytest.mark.parametrize("extra", ["max", "middle"])
-def test_backward_wider_chunks_from_larger_workspace(extra):
-    """A workspace of slp_lmhead_workspace_size_max runs the backward as one
-    vocabulary chunk, one a little smaller as 131072 + the rest; both agree
-    with the oracle and with the default chunking."""
+@pytest.mark.parametrize("extra", ["max", "middle", "default-less", "min"])
+def test_backward_chunk_width_follows_the_workspace(extra):
+    """The backward's vocabulary chunk follows the workspace: the whole
+    vocabulary (slp_lmhead_workspace_size_max), 131072 + the rest (a little
+    less), 32768 (a little less than the default 65536) and 16384 columns
+    (slp_lmhead_workspace_size_min).  Each agrees with the oracle and with the
+    default chunking."""
     dev = device()
     N, V, d = 200, 140000, 128
     a = W.make_lmhead_inputs(device=dev, N=N, V=V, d=d, p_mask=0.8, seed=44)
     a.W = (a.W.float() * 5).to(torch.bfloat16)
     lp, lse = slp.slp_lmhead_forward(a.h, a.W, a.t, a.mask, a.T)
     big = slp.slp_lmhead_workspace_size_max(N, V, d)
-    assert big > slp.slp_lmhead_workspace_size(N, V, d)
-    nbytes = big if extra == "max" else big - 256
+    dflt = slp.slp_lmhead_workspace_size(N, V, d)
+    small = slp.slp_lmhead_workspace_size_min(N, V, d)
+    assert big > dflt > small
+    nbytes = {"max": big, "middle": big - 256, "default-less": dflt - 256, "min": small}[extra]
     ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     dh, dW = slp.slp_lmhead_backward(a.h, a.W, a.t, a.mask, a.T, lse, a.g, ws=ws)
     dh0, dW0 = slp.slp_lmhead_backward(a.h, a.W, a.t, a.mask, a.T, lse, a.g)

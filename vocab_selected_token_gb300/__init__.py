@@ -28,7 +28,7 @@ __all__ = [
     "slp_forward_entropy", "slp_backward_entropy", "slp_forward_backward_entropy",
     "selected_logprob_and_entropy",
     "slp_topk_kl_forward", "slp_topk_kl_backward",
-    "slp_lmhead_workspace_size",
+    "slp_lmhead_workspace_size", "slp_lmhead_workspace_size_min", "slp_lmhead_workspace_size_max",
     "slp_lmhead_forward_workspace_size", "slp_lmhead_forward_noalloc",
     "slp_lmhead_backward_accumulate", "slp_lmhead_set_wait_limit_ns",
     "slp_lmhead_forward", "slp_lmhead_backward", "selected_logprob",
@@ -341,6 +341,12 @@ def slp_lmhead_workspace_size_max(N: int, V: int, d: int) -> int:
     """Bytes of workspace with which slp_lmhead_backward runs the whole
     vocabulary as one chunk (fewer launches; the default is 65536 columns)."""
     return int(_lib.load().slp_lmhead_workspace_size_max(int(N), int(V), int(d)))
+
+
+def slp_lmhead_workspace_size_min(N: int, V: int, d: int) -> int:
+    """Least workspace slp_lmhead_backward accepts (vocabulary chunks of 16384
+    columns: a quarter of the default dz buffer, for more GEMM launches)."""
+    return int(_lib.load().slp_lmhead_workspace_size_min(int(N), int(V), int(d)))
 
 
 def slp_lmhead_forward_workspace_size(N: int, V: int, d: int) -> int:

@@ -50,6 +50,7 @@ SIGNATURES = {
     "slp_lmhead_workspace_size": (_sz, [_i64, _i64, _i64]),
     "slp_lmhead_forward_workspace_size": (_sz, [_i64, _i64, _i64]),
     "slp_lmhead_workspace_size_max": (_sz, [_i64, _i64, _i64]),
+    "slp_lmhead_workspace_size_min": (_sz, [_i64, _i64, _i64]),
     "slp_lmhead_forward": (_int, [_vp, _vp, _i64, _i64, _i64, _vp, _vp, _f32, _vp, _vp, _vp,
                                   _sz, _vp, _vp]),
     "slp_lmhead_backward": (_int, [_vp, _vp, _i64, _i64, _i64, _vp, _vp, _f32, _vp, _vp, _vp,

@@ -234,6 +234,11 @@ size_t slp_lmhead_workspace_size_max(int64_t N, int64_t V, int64_t d) {
   return slp::lmhead_workspace_size_max(N, V, d);
 }
 
+size_t slp_lmhead_workspace_size_min(int64_t N, int64_t V, int64_t d) {
+  if (N < 0 || V <= 0 || d <= 0 || V > INT32_MAX || N > INT32_MAX || d > INT32_MAX) return 0;
+  return slp::lmhead_workspace_size_min(N, V, d);
+}
+
 size_t slp_lmhead_forward_workspace_size(int64_t N, int64_t V, int64_t d) {
   if (N < 0 || V <= 0 || d <= 0 || V > INT32_MAX || N > INT32_MAX || d > INT32_MAX) return 0;
   return slp::lmhead_forward_workspace_size(N, V, d);
@@ -256,7 +261,7 @@ int slp_lmhead_backward(const void* h, const void* W, int64_t N, int64_t V, int6
                         const float* grad_out, void* dh, void* dW, void* ws, size_t ws_bytes,
                         int32_t* err, void* stream) {
   int st = check_lmhead_args(h, W, N, V, d, t, T, ws, ws_bytes,
-                             slp::lmhead_workspace_size(N, V, d));
+                             slp::lmhead_workspace_size_min(N, V, d));
   if (st != SLP_OK) return st;
   if (N == 0) return SLP_OK;
   if (lse == nullptr || grad_out == nullptr || dh == nullptr || dW == nullptr)
@@ -274,7 +279,7 @@ int slp_lmhead_backward_accumulate(const void* h, const void* W, int64_t N, int6
                                    float* dW_accum, void* ws, size_t ws_bytes, int32_t* err,
                                    void* stream) {
   int st = check_lmhead_args(h, W, N, V, d, t, T, ws, ws_bytes,
-                             slp::lmhead_workspace_size(N, V, d));
+                             slp::lmhead_workspace_size_min(N, V, d));
   if (st != SLP_OK) return st;
   if (N == 0) return SLP_OK;
   if (lse == nullptr || grad_out == nullptr || dh == nullptr || dW_accum == nullptr)

@@ -72,6 +72,7 @@ cudaError_t launch_topk_kl_backward(const void* x, int dtype, int64_t N, int64_t
 // Fused LM-head path (slp_lmhead.cu).
 size_t lmhead_workspace_size(int64_t N, int64_t V, int64_t d);
 size_t lmhead_workspace_size_max(int64_t N, int64_t V, int64_t d);
+size_t lmhead_workspace_size_min(int64_t N, int64_t V, int64_t d);
 size_t lmhead_forward_workspace_size(int64_t N, int64_t V, int64_t d);
 // Sets the bound of every pipeline wait in later LM-head launches (0: the
 // default of two seconds); returns the previous bound.

@@ -75,7 +75,8 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // default bound of a pipeline
 constexpr uint64_t kDrainLimitNs = 2000000000ull;  // bound of the waits after a give-up
 constexpr int kSlabCap = 256;  // most vocabulary slabs per row (forward partials)
 constexpr int kKSplitCap = 24;  // most K splits of the dh GEMM
-constexpr int kVChunk = 65536;  // vocabulary columns per backward chunk
+constexpr int kVChunk = 65536;     // vocabulary columns per backward chunk (default workspace)
+constexpr int kVChunkMin = 16384;  // the narrowest chunk (smallest workspace)
 
 enum Epi { EPI_LSE = 0, EPI_DZ = 1, EPI_F32 = 2, EPI_BF16 = 3, EPI_ACC32 = 4 };
 
@@ -978,8 +979,15 @@ Layout layout(int64_t N, int64_t V, int64_t d, int64_t vchunk = kVChunk) {
   L.off_dz = L.off_pm;  // the backward does not use the forward partials
   o = align256(L.off_dz + 2 * static_cast<size_t>(L.Mcap) * L.ld_dz);
   L.off_pf32 = o;
-  o = align256(o + 4 * max_partial_floats(L.Mcap, static_cast<int>(V), L.vchunk,
-                                         static_cast<int>(d), L.geo));
+  size_t pf = max_partial_floats(L.Mcap, static_cast<int>(V), L.vchunk, static_cast<int>(d), L.geo);
+  if (vchunk == kVChunkMin) {
+    // the smallest workspace also caps the split-K partials at two splits of
+    // every row; the dh GEMM then takes fewer splits (a correct schedule with
+    // less balance) wherever its best one would need more
+    const size_t cap = 2 * static_cast<size_t>(L.Mcap) * d;
+    if (pf > cap) pf = cap;
+  }
+  o = align256(o + 4 * pf);
   L.off_acc = o; o = align256(o + 4 * static_cast<size_t>(L.Mcap) * d);
   L.bwd_end = o > L.fwd_end ? o : L.fwd_end;
   return L;
@@ -1013,12 +1021,14 @@ void dbg_add(dbg::Bounds& b, const void* p, size_t bytes) {
 #endif
 
 // The widest backward chunk whose workspace fits in ws_bytes: the whole
-// vocabulary, two default chunks, or the default chunk.
+// vocabulary, then 131072, 65536 (the default), 32768 or 16384 columns.  A
+// narrower chunk needs a smaller dz chunk and fewer split-K partials, for
+// more launch boundaries.
 int64_t chunk_for(int64_t N, int64_t V, int64_t d, size_t ws_bytes) {
-  const int64_t widths[2] = {V, 2ll * kVChunk};
+  const int64_t widths[4] = {V, 2ll * kVChunk, kVChunk, kVChunk / 2};
   for (int64_t w : widths)
-    if (w > kVChunk && layout(N, V, d, w).bwd_end <= ws_bytes) return w;
-  return kVChunk;
+    if (layout(N, V, d, w).bwd_end <= ws_bytes) return w;
+  return kVChunkMin;
 }
 
 // logprob / lse: the forward's outputs (their inactive rows are zeroed here),
@@ -1112,6 +1122,10 @@ size_t lmhead_workspace_size(int64_t N, int64_t V, int64_t d) {
 
 size_t lmhead_workspace_size_max(int64_t N, int64_t V, int64_t d) {
   return lmh::layout(N, V, d, V).bwd_end;
+}
+
+size_t lmhead_workspace_size_min(int64_t N, int64_t V, int64_t d) {
+  return lmh::layout(N, V, d, lmh::kVChunkMin).bwd_end;
 }
 
 cudaError_t launch_lmhead_forward(const void* h, const void* W, int64_t N, int64_t V, int64_t d,

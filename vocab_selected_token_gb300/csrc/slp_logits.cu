@@ -972,14 +972,29 @@ bool aligned16(const void* p, int64_t ld, int esize) {
   return (reinterpret_cast<uintptr_t>(p) & 15u) == 0 && ((ld * esize) & 15) == 0;
 }
 
-int choose_splits(int64_t N, int64_t V) {
-  // One CTA per row whenever the rows alone give about two waves of resident
-  // CTAs (three per SM: 64 KB of ring each); splitting a row into a cluster
-  // costs more than it gains there.  Fewer rows: split, giving every CTA at
-  // least 16K elements.
-  const int64_t want = static_cast<int64_t>(sm_count()) * 3 * 2;
-  int64_t s = (want + N - 1) / N;
-  const int64_t by_len = V / 16384;
+// CTAs per row of the ring forward (a cluster of that many CTAs when > 1).
+// `ring` is the bytes one CTA keeps in flight; `per_sm` CTAs are resident per
+// SM.  Measured (bf16, L2 flushed, one CTA per row against splits 2..8):
+//  - When every row's CTA is resident at once, splitting only adds a
+//    cluster's launch and barriers: N = 256, V = 151936: 26.2 us unsplit,
+//    31.2 split 3, 34.0 split 4; V = 32768: 13.9 against 16.0.
+//  - When the rows make a little more than one wave, a split evens out the
+//    last wave for long rows: N = 512, V = 262144: 69.2 us split 2 against
+//    75.3 unsplit; at V = 32768 a split leaves each CTA less than its ring
+//    (18.4 unsplit against 23.0).
+//  - From two waves on, one CTA per row ties or wins (N = 1024 and 2048 at
+//    V = 32768, 151936, 262144).
+// So: below one wave, the largest split that keeps every CTA resident; up to
+// two waves, a split of 2; then none.  A CTA always gets at least one ring's
+// worth of the row, and at most 8 CTAs (the portable cluster size) share it.
+int choose_splits(int64_t N, int64_t row_bytes, int64_t ring, int per_sm) {
+  const int64_t slots = static_cast<int64_t>(sm_count()) * per_sm;
+  int64_t s = 1;
+  if (N <= slots)
+    s = slots / (N > 0 ? N : 1);
+  else if (N < 2 * slots)
+    s = 2;
+  const int64_t by_len = row_bytes / ring;
   if (s > by_len) s = by_len;
   if (s > kMaxSplits) s = kMaxSplits;
   if (s < 1) s = 1;
@@ -1000,7 +1015,9 @@ cudaError_t fwd_typed(const Elt* x, int64_t N, int64_t V, int64_t ld, const int3
                             {logprob, 4ull * N}, {lse, 4ull * N}, {entropy, 4ull * N}}));
     return cudaGetLastError();
   }
-  const int splits = choose_splits(N, V);
+  // 64 KB rings fit three CTAs per SM, 32 KB rings (with the entropy) six
+  const int splits = choose_splits(N, V * static_cast<int64_t>(sizeof(Elt)), fwd_smem<St>(),
+                                   fwd_stages<St>() == 4 ? 3 : 6);
   if (N * splits > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
   const float c = static_cast<float>(1.4426950408889634 / static_cast<double>(T));
   const bool vec = aligned16(x, ld, sizeof(Elt));
