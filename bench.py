@@ -509,9 +509,59 @@ def other_workloads(device, hbm):
         torch.cuda.empty_cache()
     out["fused_fwd_bwd"] = time_fused(device, hbm)
     out["short_rows"] = time_short_rows(device, hbm)
+    out["small_n"] = time_small_n(device, hbm)
     out["entropy"] = time_entropy(device, hbm)
     out["topk_kl"] = time_topk(device, hbm)
     out["lmhead"] = time_lmhead(device)
+    return out
+
+
+def time_small_n(device, hbm, steps=30, warmup=3):
+    """Few rows (c151k recipe, N = 256 and 1024 at V = 32768 and 151936): the
+    separate forward + backward step and the fused call.  Most of these inputs
+    fit in L2, so L2 is flushed (a 256 MB write) before every timed step, and
+    each step is timed on its own with CUDA events (the flush outside them)."""
+    import vocab_selected_token_gb300 as slp
+    from vocab_selected_token_gb300 import workloads as W
+    out = {}
+    s = torch.cuda.current_stream(device)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    for N, V in ((256, 32768), (256, 151936), (1024, 32768), (1024, 151936)):
+        inp = W.make_logits_inputs("c151k", device=device, N=N, V=V)
+        nb = N * V * inp.x.element_size()
+        lp = torch.empty(N, device=device)
+        lse = torch.empty(N, device=device)
+        gx = torch.empty_like(inp.x)
+
+        def sep():
+            slp.slp_forward(inp.x, inp.t, None, inp.T, logprob=lp, lse=lse)
+            slp.slp_backward(inp.x, inp.t, None, inp.T, lse, inp.g, grad_x=gx)
+
+        def fused():
+            slp.slp_forward_backward(inp.x, inp.t, None, inp.T, inp.g, logprob=lp, lse=lse,
+                                     grad_x=gx)
+
+        res = {"N": N, "V": V, "l2": "flushed before every timed step"}
+        for key, fn, passes in (("step", sep, 3), ("fused", fused, 2)):
+            for _ in range(warmup):
+                fn()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(steps)]
+            for e0, e1 in ev:
+                flush.fill_(1)
+                e0.record(s)
+                fn()
+                e1.record(s)
+            torch.cuda.synchronize(device)
+            ms = sum(e0.elapsed_time(e1) for e0, e1 in ev) / steps
+            gbs = passes * nb / (ms * 1e-3) / 1e9
+            res[key] = {"ms": ms, "tokens_per_s": N * 1000.0 / ms, "gbs": gbs,
+                        "frac_of_measured": gbs / hbm}
+        out[f"N{N}_V{V}"] = res
+        del inp, gx
+        torch.cuda.empty_cache()
+    del flush
+    torch.cuda.empty_cache()
     return out
 
 
@@ -755,7 +805,36 @@ def time_lmhead(device, steps=40, warmup=3, N=None):
     # NVIDIA's dense bf16 figure for one GB300 (half its 2:4-sparse figure)
     res["peak_bf16_tflops_datasheet"] = 2250.0
     res["step_frac_datasheet"] = res["step_tflops"] / 2250.0
-    del a, ws, dh, dW
+    # the backward against its workspace: the chunk width follows the bytes
+    # given (16384 columns at the minimum, 65536 by default, the whole
+    # vocabulary at the maximum)
+    del ws
+    torch.cuda.empty_cache()
+    curve = []
+    for name, fn in (("min", lib.slp_lmhead_workspace_size_min),
+                     ("default", lib.slp_lmhead_workspace_size),
+                     ("max", lib.slp_lmhead_workspace_size_max)):
+        nb = int(fn(Nn, V, d))
+        wsx = torch.empty(nb, dtype=torch.uint8, device=device)
+        bx = ba[:12] + (wsx.data_ptr(), nb) + ba[14:]
+        for _ in range(2):
+            assert lib.slp_lmhead_backward(*bx) == 0
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(device)
+        e0.record(s)
+        for _ in range(10):
+            assert lib.slp_lmhead_backward(*bx) == 0
+        e1.record(s)
+        torch.cuda.synchronize(device)
+        ms = e0.elapsed_time(e1) / 10
+        curve.append({"workspace": name, "workspace_bytes": nb, "bwd_ms": ms,
+                      "bwd_tflops": 3 * flop_f / (ms * 1e-3) / 1e12})
+        del wsx
+        torch.cuda.empty_cache()
+    res["bwd_by_workspace"] = curve
+    # for scale: the bf16 logits of every row, which the fused path never stores
+    res["bf16_logits_bytes_all_rows"] = 2 * Nn * V
+    del a, dh, dW
     torch.cuda.empty_cache()
     return res
 
