@@ -181,6 +181,25 @@ def test_split_invariance():
                *slp.slp_forward(big.x[:4], big.t[:4], None, 1.0), None, range(4))
 
 
+def test_split_invariance_long_rows():
+    """Rows of 1 MB (V = 524288 bf16) under every split the forward's rule
+    picks for few rows: 8 CTAs per row (N = 2 and 50), 4 (N = 100), 1
+    (N = 300) and 2 (N = 600, a little more than one wave).  The shared rows
+    agree across the calls and with the oracle."""
+    dev = device()
+    big = W.make_logits_inputs("c151k", device=dev, N=600, V=524288)
+    outs = []
+    for N in (2, 50, 100, 300, 600):
+        lp, lse = slp.slp_forward(big.x[:N], big.t[:N], None, 1.0)
+        torch.cuda.synchronize()
+        outs.append((to64(lp[:2]), to64(lse[:2])))
+    for lp, lse in outs[1:]:
+        assert np.abs(lp - outs[0][0]).max() <= TOL_LP
+        assert np.abs(lse - outs[0][1]).max() <= TOL_LP
+    lp, lse = slp.slp_forward(big.x[:100], big.t[:100], None, 1.0)
+    check_rows(big.x[:100], big.t[:100], None, 1.0, big.g[:100], lp, lse, None, range(100))
+
+
 def test_short_rows_both_forward_kernels():
     """Rows of 60 KB take the warp-per-row forward when there are many rows
     and the ring kernel when there are few; the same rows agree across the
