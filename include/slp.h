@@ -341,6 +341,13 @@ size_t slp_lmhead_workspace_size_max(int64_t N, int64_t V, int64_t d);
  * slp_lmhead_forward - selected-token log-probabilities through the LM head,
  * logits never stored.
  *
+ * The GEMMs run on pairs of CTAs (thread-block clusters of two, one
+ * tcgen05 MMA over both); on a device that cannot co-schedule such pairs, or
+ * with SLP_LMHEAD_CTA_PAIRS=0 in the environment before the first LM-head
+ * call or workspace query, they run one CTA per tile.  The two forms agree
+ * within the LM-head tolerances and need workspaces of different sizes: ask
+ * the workspace functions in the same process that makes the calls.
+ *
  * Defined by: the slp_forward definition applied to x = h W^T (no bias),
  * computing only rows with mask[n] != 0 before the vocabulary projection and
  * scattering the per-row scalars back (slime issue #2253, maintainer

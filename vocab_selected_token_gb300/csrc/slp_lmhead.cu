@@ -42,6 +42,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <stdlib.h>
+
 #include <atomic>
 
 namespace slp {
@@ -904,9 +906,15 @@ struct Geometry {
 };
 
 Geometry geometry() {
-  static int cached[64] = {0};  // pairs that fit, or -1: none
+  static int cached[64] = {0};  // pairs that fit, or -1: none (or not wanted)
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  if (cached[dev] == 0) {
+    // SLP_LMHEAD_CTA_PAIRS=0 in the environment keeps the one-CTA form (read
+    // once per device, at the first LM-head call or workspace query)
+    const char* env = getenv("SLP_LMHEAD_CTA_PAIRS");
+    if (env != nullptr && env[0] == '0') cached[dev] = -1;
+  }
   if (cached[dev] == 0) {
     int n = 0;
     auto k = lmh_gemm_kernel<EPI_LSE, false, false, true>;
