@@ -6,16 +6,17 @@
 // Forward
 //   1. scan    : mask -> pos[N] (compact index or -1), idx[Na], Na     (1 CTA);
 //                inactive rows get logprob = lse = 0
-//   2. gather  : h_c[i] = h[idx[i]], rows Na..roundup(Na,128) zeroed
-//   3. GEMM    : persistent tcgen05 kernel, 128 x 256 tiles of h_c W^T with
-//                fp32 accumulators in TMEM; the epilogue warps keep an online
+//   2. gather  : h_c[i] = h[idx[i]], rows Na..roundup(Na,256) zeroed
+//   3. GEMM    : persistent tcgen05 kernel, 256 x 256 tiles of h_c W^T per
+//                CTA pair with fp32 accumulators in TMEM; the epilogue warps
+//                of each CTA keep an online
 //                (max, sum-exp) per row over a slab of vocabulary tiles and
 //                catch the target logit; one partial per (slab, row).  The
 //                epilogue warp that stores the last slab of its 32 rows merges
 //                their partials in slab order and writes logprob/lse to the
 //                original rows.
-// Backward, per vocabulary chunk of at most kVChunk columns (a bounded
-// workspace instead of a [rows, V] buffer)
+// Backward, per vocabulary chunk of 16384 to V columns, as the caller's
+// workspace allows (a bounded workspace instead of a [rows, V] buffer)
 //   1-2. scan + gather as above (once)
 //   3. GEMM (recompute): the chunk's tiles; the epilogue writes
 //        dz = g/T (1[v == t] - 2^(x*c - lse*log2 e)) as bf16 (rows >= Na: 0)
@@ -24,13 +25,18 @@
 //        warps 2-3 meanwhile fold dh_acc (+)= sum_ks dh_part[ks] (fixed order)
 //   then once: dh[r] = bf16(dh_acc[pos[r]]) (inactive rows 0)
 //
-// GEMM kernel layout (one CTA per SM, 256 threads): warp 0 issues TMA loads
-// into a 4-stage shared-memory ring (128-byte swizzle), warp 1 issues
-// tcgen05.mma (M=128, N=256, K=16) into one of two TMEM accumulators, warp 2
-// owns the TMEM allocation, warps 4-7 are the epilogue (TMEM lane = row, so
-// every row reduction is thread-local).  Every mbarrier wait gives up after
-// about two seconds, sets SLP_DEVICE_ERR_TIMEOUT and lets the CTA drain and
-// free its TMEM instead of hanging.
+// GEMM kernel layout: persistent, 256 threads per CTA, launched as clusters
+// of two CTAs on two SMs (a CTA pair).  In each CTA warp 0 issues TMA loads
+// of its 128 rows of A and its half of B into a 6-stage shared-memory ring
+// (128-byte swizzle); warp 1 of the even CTA issues tcgen05.mma.cta_group::2
+// (M=256 over both CTAs, N=256, K=16) into one of two TMEM accumulators;
+// warp 2 owns the pair-wide TMEM allocation; warps 4-7 are the epilogue of
+// their CTA's 128 rows (TMEM lane = row, so every row reduction is
+// thread-local).  Without pairs (a device that cannot co-schedule them, or
+// SLP_LMHEAD_CTA_PAIRS=0) the same template runs one CTA per 128 x 256 tile
+// with a 4-stage ring.  Every mbarrier wait gives up after its bound (two
+// seconds by default), sets SLP_DEVICE_ERR_TIMEOUT, drains the copies and
+// tensor-core work in flight and frees its TMEM instead of hanging.
 
 #include "slp.h"
 #include "slp_device.cuh"
