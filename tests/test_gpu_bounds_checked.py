@@ -23,7 +23,9 @@ import torch
 import vocab_selected_token_gb300 as slp
 from oracle import slp_oracle as O
 from tests.gpu_util import assert_close_nan, assert_grad_close, check_rows, device, to64
+from tests import test_gpu_lmhead_random as LMR
 from tests.test_gpu_entropy import check_entropy_rows
+from tests.test_gpu_random_shapes import run_shape
 from vocab_selected_token_gb300 import _lib, build
 from vocab_selected_token_gb300 import workloads as W
 
@@ -156,3 +158,28 @@ def test_lmhead_calls_stay_in_bounds(N, V, d, pm):
         cos = float(got @ ref / (np.linalg.norm(got) * np.linalg.norm(ref)))
         frob = float(np.linalg.norm(got - ref) / np.linalg.norm(ref))
         assert cos >= 0.999 and frob <= 1e-2, f"{what}: cosine {cos:.6f} frob {frob:.2e}"
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_logits_shapes_stay_in_bounds(seed):
+    """The seeded sweep of random shapes, strides, dtypes, temperatures and
+    mask densities (V from 1 to 160000, padded rows) through the checked
+    library: clean error words and oracle parity."""
+    dev = device()
+    with checked_library():
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+        run_shape(seed, err=err)
+        clean(err)
+
+
+@pytest.mark.parametrize("case", [LMR._case(s) for s in range(16)] + LMR.EDGES,
+                         ids=lambda v: str(v))
+def test_random_lmhead_shapes_stay_in_bounds(case):
+    """The LM head's random sweep and edge cases (ragged row blocks, V = 1,
+    d not a multiple of the tile, several backward chunks) through the
+    checked library."""
+    dev = device()
+    with checked_library():
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+        LMR._run(*case, seed=500 + sum(int(v) for v in case[:3]), err=err)
+        clean(err)

@@ -70,13 +70,13 @@ def test_lmhead_edges(case):
     _run(*case, seed=400 + EDGES.index(case))
 
 
-def _run(N, V, d, T, pm, scale, seed):
+def _run(N, V, d, T, pm, scale, seed, err=None):
     dev = device()
     a = W.make_lmhead_inputs(device=dev, N=N, V=V, d=d, p_mask=pm, seed=seed)
     a.W = (a.W.float() * scale).to(torch.bfloat16)
     a.T = T
-    lp, lse = slp.slp_lmhead_forward(a.h, a.W, a.t, a.mask, T)
-    dh, dW = slp.slp_lmhead_backward(a.h, a.W, a.t, a.mask, T, lse, a.g)
+    lp, lse = slp.slp_lmhead_forward(a.h, a.W, a.t, a.mask, T, err=err)
+    dh, dW = slp.slp_lmhead_backward(a.h, a.W, a.t, a.mask, T, lse, a.g, err=err)
     torch.cuda.synchronize()
     h64, W64 = to64(a.h), to64(a.W)
     t, m, g = a.t.cpu().numpy(), a.mask.cpu().numpy(), to64(a.g)

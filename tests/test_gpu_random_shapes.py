@@ -33,6 +33,12 @@ def _case(seed):
 
 @pytest.mark.parametrize("seed", range(24))
 def test_random_shape(seed):
+    run_shape(seed)
+
+
+def run_shape(seed, err=None):
+    """Case `seed` through the three calls, every row against the oracle;
+    `err`, when given, is passed to every call as its error word."""
     dev = device()
     N, V, pad, dtype, T, pm, std = _case(seed)
     g = torch.Generator(device=dev).manual_seed(seed)
@@ -41,9 +47,9 @@ def test_random_shape(seed):
     t = torch.randint(0, V, (N,), generator=g, device=dev, dtype=torch.int32)
     mask = None if pm == 1.0 else (torch.rand(N, generator=g, device=dev) < pm).to(torch.uint8)
     grad = torch.rand(N, generator=g, device=dev) * 2 - 1
-    lp, lse = slp.slp_forward(x, t, mask, T)
-    gx = slp.slp_backward(x, t, mask, T, lse, grad)
-    lp2, lse2, gx2 = slp.slp_forward_backward(x, t, mask, T, grad)
+    lp, lse = slp.slp_forward(x, t, mask, T, err=err)
+    gx = slp.slp_backward(x, t, mask, T, lse, grad, err=err)
+    lp2, lse2, gx2 = slp.slp_forward_backward(x, t, mask, T, grad, err=err)
     torch.cuda.synchronize()
     rows = range(N)
     check_rows(x, t, mask, T, grad, lp, lse, gx, rows, fp32_floor=True)
