@@ -844,15 +844,16 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (fn == nullptr) {
+  // looked up once (thread-safe static initialisation); NULL if unavailable
+  static const EncodeTiledFn fn = []() -> EncodeTiledFn {
     void* ptr = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  }
+      return reinterpret_cast<EncodeTiledFn>(ptr);
+    return nullptr;
+  }();
   return fn;
 }
 
@@ -912,37 +913,40 @@ struct Geometry {
 };
 
 Geometry geometry() {
-  static int cached[64] = {0};  // pairs that fit, or -1: none (or not wanted)
+  // per device, filled on first use: pairs that fit, or -1 for none (or not
+  // wanted); threads that race here store the same value
+  static std::atomic<int> cached[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
-  if (cached[dev] == 0) {
+  int pairs = cached[dev].load(std::memory_order_relaxed);
+  if (pairs == 0) {
     // SLP_LMHEAD_CTA_PAIRS=0 in the environment keeps the one-CTA form (read
     // once per device, at the first LM-head call or workspace query)
     const char* env = getenv("SLP_LMHEAD_CTA_PAIRS");
-    if (env != nullptr && env[0] == '0') cached[dev] = -1;
-  }
-  if (cached[dev] == 0) {
     int n = 0;
-    auto k = lmh_gemm_kernel<EPI_LSE, false, false, true>;
-    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Tile<true>::kSmemBytes) == cudaSuccess) {
-      cudaLaunchConfig_t cfg{};
-      cfg.gridDim = dim3(2 * (sm_count() / 2));
-      cfg.blockDim = dim3(kThreads);
-      cfg.dynamicSmemBytes = Tile<true>::kSmemBytes;
-      cudaLaunchAttribute attr[1];
-      attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = 2;
-      attr[0].val.clusterDim.y = 1;
-      attr[0].val.clusterDim.z = 1;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
-      if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess) n = 0;
+    if (env == nullptr || env[0] != '0') {
+      auto k = lmh_gemm_kernel<EPI_LSE, false, false, true>;
+      if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               Tile<true>::kSmemBytes) == cudaSuccess) {
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(2 * (sm_count() / 2));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = Tile<true>::kSmemBytes;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess) n = 0;
+      }
+      cudaGetLastError();  // a failed query leaves no sticky error behind
     }
-    cudaGetLastError();  // a failed query leaves no sticky error behind
-    cached[dev] = n > 0 ? n : -1;
+    pairs = n > 0 ? n : -1;
+    cached[dev].store(pairs, std::memory_order_relaxed);
   }
-  if (cached[dev] > 0) return Geometry{true, cached[dev], Tile<true>::kRows};
+  if (pairs > 0) return Geometry{true, pairs, Tile<true>::kRows};
   return Geometry{false, sm_count(), Tile<false>::kRows};
 }
 
