@@ -31,6 +31,19 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) {
   return r;
 }
 
+// The same load with an L2 evict-first policy, for data read once whose L2
+// room is better left to the write-back of the stores that follow it.
+__device__ __forceinline__ uint4 ld_stream_ef(const void* p) {
+  if (!dbg::ok(p, 16)) return make_uint4(0u, 0u, 0u, 0u);
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  uint4 r;
+  asm("ld.global.nc.L1::no_allocate.L2::cache_hint.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p), "l"(pol));
+  return r;
+}
+
 // 128-bit streaming store (evict-first).
 __device__ __forceinline__ void st_stream(void* p, const uint4& v) {
   if (!dbg::ok(p, 16)) return;

@@ -514,7 +514,9 @@ __global__ void __launch_bounds__(32 * kRowsWarps)
 // HBM read of the active rows plus one write of the gradient, instead of the
 // two reads of a separate forward and backward (NeMo-RL PR #4222, "Changes":
 // recompute the softmax instead of storing it; here the row stays on chip
-// between the two passes).
+// between the two passes).  The row is read with an L2 evict-first policy:
+// it is read once, and L2 is better left to the gradient's write-back
+// (measured on c151k: 402 -> 394 us).
 
 constexpr int kFbThreads = 256;
 constexpr int kFbChunk = 16384;
@@ -606,7 +608,7 @@ __global__ void __launch_bounds__(kFbThreads, kRV > 0 ? 4 : 1)
       const uint32_t bytes = static_cast<uint32_t>(seg_bytes - off < kFbChunk ? seg_bytes - off
                                                                                 : kFbChunk);
       sm100::mbar_arrive_expect_tx(bbase + 8 * k, bytes);
-      sm100::bulk_load(sbase + off, src + off, bytes, bbase + 8 * k);
+      sm100::bulk_load_ef(sbase + off, src + off, bytes, bbase + 8 * k);
     }
   }
 
@@ -617,7 +619,7 @@ __global__ void __launch_bounds__(kFbThreads, kRV > 0 ? 4 : 1)
 #pragma unroll
     for (int u = 0; u < kRV; ++u) {
       const int i = nv_s + u * kFbThreads + threadIdx.x;
-      rv[u] = i < nv ? ld_stream(xv + i) : pad;
+      rv[u] = i < nv ? ld_stream_ef(xv + i) : pad;
     }
   }
 
