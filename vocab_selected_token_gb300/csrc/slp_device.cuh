@@ -52,6 +52,16 @@ __device__ __forceinline__ void st_stream(void* p, const uint4& v) {
                : "memory");
 }
 
+// 128-bit store that skips L1 and takes L2's default policy (the fused
+// kernel's gradient: measured a little faster there than the streaming
+// store above, 395.9 -> 392.6 us on c151k).
+__device__ __forceinline__ void st_global_na(void* p, const uint4& v) {
+  if (!dbg::ok(p, 16)) return;
+  asm volatile("st.global.L1::no_allocate.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x),
+               "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
 // Element traits: how many elements a 16-byte vector holds, how to widen them.
 template <typename Elt>
 struct Elem;

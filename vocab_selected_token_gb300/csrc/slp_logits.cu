@@ -741,7 +741,7 @@ __global__ void __launch_bounds__(kFbThreads, kRV > 0 ? 4 : 1)
     const int64_t tvec = rel0 >= 0 ? rel0 / kVec : -1;
     Elt* gr = gx + row * ldg;
     auto put = [&](int i, const uint4& v) {
-      st_stream(gv + i, b.vec(v));
+      st_global_na(gv + i, b.vec(v));
       if (i == tvec) E::store1(gr + tt, b.one(E::load1(xr + tt), c, true));
     };
     for (int i = threadIdx.x; i < nv_s; i += kFbThreads) put(i, q[i]);
@@ -771,7 +771,7 @@ __global__ void __launch_bounds__(kFbThreads, kRV > 0 ? 4 : 1)
   const int64_t rel0 = static_cast<int64_t>(tt) - v0 * kVec;  // target offset in segment
   const int64_t tvec = rel0 >= 0 ? rel0 / kVec : -1;
   auto put = [&](int i, const uint4& v) {
-    st_stream(gv + i, scaled_exp2_vec(v, cc, no, sgn, tag));
+    st_global_na(gv + i, scaled_exp2_vec(v, cc, no, sgn, tag));
     if (i == tvec) {
       const float p = ex2(fmaf(E::load1(xr + tt), c, -off));
       E::store1(gx + row * ldg + tt, fmaf(a, p, gT));
