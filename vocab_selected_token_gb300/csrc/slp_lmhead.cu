@@ -29,10 +29,16 @@
 // of two CTAs on two SMs (a CTA pair).  In each CTA warp 0 issues TMA loads
 // of its 128 rows of A and its half of B into a 6-stage shared-memory ring
 // (128-byte swizzle); warp 1 of the even CTA issues tcgen05.mma.cta_group::2
-// (M=256 over both CTAs, N=256, K=16) into one of two TMEM accumulators;
-// warp 2 owns the pair-wide TMEM allocation; warps 4-7 are the epilogue of
-// their CTA's 128 rows (TMEM lane = row, so every row reduction is
-// thread-local).  Without pairs (a device that cannot co-schedule them, or
+// (M=256 over both CTAs, N=256, K=16) into one of two TMEM accumulators --
+// the whole warp runs the issue loop with warp-uniform operands and one
+// elected lane issues, which keeps the issue well ahead of the tensor pipe
+// (a one-lane branch issued about 80 cycles per MMA and starved it); warp 2
+// owns the pair-wide TMEM allocation; warps 4-7 are the epilogue of their
+// CTA's 128 rows (TMEM lane = row, so every row reduction is thread-local).
+// Units (a row block's slab of vocabulary tiles, or one output tile) are
+// handed out at run time: each pair claims the next one from a counter in
+// the workspace and publishes it to every role of both CTAs through a small
+// shared-memory ring.  Without pairs (a device that cannot co-schedule them, or
 // SLP_LMHEAD_CTA_PAIRS=0) the same template runs one CTA per 128 x 256 tile
 // with a 4-stage ring.  Every mbarrier wait gives up after its bound (two
 // seconds by default), sets SLP_DEVICE_ERR_TIMEOUT, drains the copies and
@@ -77,11 +83,12 @@ struct Tile {
   static constexpr int kBBytes = kBRows * BK * 2;
   static constexpr int kStageBytes = A_BYTES + kBBytes;
   static constexpr int kStages = kPair ? 6 : 4;
-  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 512 /*barriers*/;
 };
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // default bound of a pipeline wait
 constexpr uint64_t kDrainLimitNs = 2000000000ull;  // bound of the waits after a give-up
 constexpr int kSlabCap = 256;  // most vocabulary slabs per row (forward partials)
+constexpr int kWorkSlots = 8;  // units published ahead of the slowest consumer
 constexpr int kKSplitCap = 24;  // most K splits of the dh GEMM
 constexpr int kVChunk = 65536;     // vocabulary columns per backward chunk (default workspace)
 constexpr int kVChunkMin = 16384;  // the narrowest chunk (smallest workspace)
@@ -213,17 +220,14 @@ struct Params {
   int v0;                     // first vocabulary column of this launch
   int Vtot;                   // whole vocabulary (valid targets are [0, Vtot))
   int G;                      // grid size the schedule was made for
-  const int32_t* counters;    // [0] = Na
+  const int32_t* counters;    // [0] = Na; [1], [2]: unit counters of alternate launches
   const int32_t* idx;         // compact row -> original row
   const int32_t* t;           // [N] targets
   const float* g;             // [N] upstream gradient (backward)
   const float* lse;           // [N] saved lse (backward)
   float c;                    // log2(e) / T
   float invT;
-  float* part_m;              // [kSlabCap][Mcap] forward partials
-  float* part_mc;
-  float* part_s;
-  float* part_xt;
+  float4* part;               // [kSlabCap][Mcap] forward partials {m, mc, s, x_t}
   __nv_bfloat16* dz;          // [Mcap][ld_dz]
   long long ld_dz;
   float* part_f32;            // [S][Mpad][d] split-K partials of dh (Mpad from Na)
@@ -238,6 +242,8 @@ struct Params {
   float* out_lse;
   float T;
   unsigned long long wait_ns;  // bound of every pipeline wait (after it: give up, flag, drain)
+  int32_t* work;               // units claimed so far beyond the first G (zero at launch)
+  int32_t* work_next;          // the next launch's counter, zeroed by this one
 };
 
 __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float (&v)[32]) {
@@ -279,9 +285,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5 + 2 * kWorkSlots);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   volatile int* peer_fills = reinterpret_cast<volatile int*>(tmem_holder + 2);
+  volatile int* work_ring = reinterpret_cast<volatile int*>(tmem_holder + 4);  // [kWorkSlots]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -290,6 +297,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_accf = bar_full + 16 * STAGES;
   const uint32_t bar_acce = bar_accf + 16;
   const uint32_t bar_done = bar_acce + 16;  // the MMA thread's last commit
+  const uint32_t bar_wfull = bar_done + 8;  // [kWorkSlots] a unit published in the slot
+  const uint32_t bar_wempty = bar_wfull + 8 * kWorkSlots;  // [kWorkSlots] slot read by all
   const uint32_t ring = smem_u32(smem);
   // The pair: rank 0 issues the MMAs and owns the barriers the MMA thread
   // waits on (full, accumulator-empty); both CTAs load, and both drain their
@@ -301,6 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t lead_acce = kPair ? mapa_rank(bar_acce, 0) : bar_acce;
   const uint32_t peer_abort =
       kPair ? mapa_rank(smem_u32(const_cast<int*>(abort_flag)), rank ^ 1u) : 0u;
+  const uint32_t lead_wempty = kPair ? mapa_rank(bar_wempty, 0) : bar_wempty;
   // a wait that gave up here ends the other CTA's waits too
   auto give_up = [&]() {
     *abort_flag = 1;
@@ -317,6 +327,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_acce + 8 * b, 4 * TL::kCtas);  // one arrival per epilogue warp of the pair
     }
     mbar_init(bar_done, 1);
+    // Unit hand-out: rank 0's producer publishes each unit into the ring of
+    // both CTAs; every consumer of the pair (the other producer, the MMA
+    // thread, the epilogue warps) frees the slot on rank 0 once it has read it.
+    for (int j = 0; j < kWorkSlots; ++j) {
+      mbar_init(bar_wfull + 8 * j, 1);
+      mbar_init(bar_wempty + 8 * j, 1 + 4 * TL::kCtas + (kPair ? 1 : 0));
+    }
     *abort_flag = 0;
     *peer_fills = 0;
     fence_mbar_init();
@@ -344,13 +361,66 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int Na = dbg::ld(p.counters);
   const Sched sc = make_sched(kEpi, Na, p.V, p.d, p.G, TL::kRows, p.pf32_cap);
   int fills = 0;  // stage fills this CTA's producer issued
+  if (blockIdx.x == 0 && threadIdx.x == 0 && p.work_next != nullptr) dbg::st(p.work_next, 0);
+
+  // Units: each pair starts with unit tile0, then takes the next unclaimed
+  // unit from a global counter whenever it starts one (a claim ahead, so the
+  // atomic's latency hides behind the unit in progress); pairs that run
+  // faster take more units.  Every role of both CTAs walks the same
+  // sequence: work item wi sits in slot wi % kWorkSlots; -1 ends it.  (Waits
+  // on it acquire at cluster scope: the publishing arrival may come from the
+  // other CTA.)
+  auto take_unit = [&](int wi, int& u) -> bool {
+    if (!mbar_wait_bounded<kPair>(bar_wfull + 8 * (wi % kWorkSlots), (wi / kWorkSlots) & 1,
+                                  abort_flag, p.wait_ns))
+      return false;
+    u = work_ring[wi % kWorkSlots];
+    return true;
+  };
+  auto free_slot = [&](int wi) {
+    if (kPair)
+      mbar_arrive_cluster(lead_wempty + 8 * (wi % kWorkSlots));
+    else
+      mbar_arrive(bar_wempty + 8 * (wi % kWorkSlots));
+  };
+  auto claim_unit = [&]() -> int {
+    return dbg::ok(p.work, 4) ? atomicAdd(p.work, 1) + tiles_in_flight : sc.units;
+  };
 
   if (warp == 0) {
     // ---------------- TMA producer (both CTAs) ----------------
     if (lane == 0) {
       int it = 0;
       bool ok = true;
-      for (int u = tile0; u < sc.units && ok; u += tiles_in_flight) {
+      int u = tile0;
+      int claim = sc.units;
+      if (rank == 0 && u < sc.units) claim = claim_unit();
+      for (int wi = 0; ok; ++wi) {
+        const int slot = wi % kWorkSlots;
+        if (rank == 0) {
+          // publish unit u (or the end) once every consumer has read the slot's last one
+          if (!mbar_wait_bounded<kPair>(bar_wempty + 8 * slot, ((wi / kWorkSlots) & 1) ^ 1,
+                                        abort_flag, p.wait_ns)) {
+            give_up();
+            break;
+          }
+          const int item = u < sc.units ? u : -1;
+          work_ring[slot] = item;
+          if (kPair) {
+            st_cluster_u32(mapa_rank(smem_u32(const_cast<int*>(work_ring + slot)), 1),
+                           static_cast<uint32_t>(item));
+            mbar_arrive_cluster(mapa_rank(bar_wfull + 8 * slot, 1));
+          }
+          mbar_arrive(bar_wfull + 8 * slot);
+          u = item;
+        } else {
+          if (!take_unit(wi, u)) {
+            give_up();
+            break;
+          }
+          free_slot(wi);
+        }
+        if (u < 0) break;
         const Unit w = decode(sc, kEpi, u);
         const int arow = w.m * TL::kRows + static_cast<int>(rank) * BM;  // this CTA's A rows
         for (int n = w.n0; n < w.n1 && ok; ++n) {
@@ -389,6 +459,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+        if (rank == 0) {
+          u = claim;
+          if (u < sc.units) claim = claim_unit();
+        }
       }
       fills = it;
       if (!kPair) {
@@ -408,17 +482,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer (rank 0 only) ----------------
-    if (lane == 0 && rank == 0) {
+    // The whole warp runs this loop; every wait is agreed by the warp, and
+    // one elected lane issues each MMA and commit (inside the helpers).
+    if (rank == 0) {
       constexpr uint32_t idesc = umma_idesc_bf16(TL::kRows, BN, kAmn, kBmn);
       int it = 0, tc = 0;
       bool ok = true;
-      for (int u = tile0; u < sc.units && ok; u += tiles_in_flight) {
+      for (int wi = 0; ok; ++wi) {
+        int u = -1;
+        if (!__all_sync(0xFFFFFFFFu, take_unit(wi, u))) {
+          if (lane == 0) give_up();
+          break;
+        }
+        u = __shfl_sync(0xFFFFFFFFu, u, 0);
+        if (lane == 0) free_slot(wi);
+        if (u < 0) break;
         const Unit w = decode(sc, kEpi, u);
         for (int n = w.n0; n < w.n1 && ok; ++n, ++tc) {
           const int buf = tc & 1;
-          if (!mbar_wait_bounded(bar_acce + 8 * buf, ((tc >> 1) & 1) ^ 1, abort_flag,
-                                 p.wait_ns)) {
-            give_up();
+          if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(bar_acce + 8 * buf,
+                                                         ((tc >> 1) & 1) ^ 1, abort_flag,
+                                                         p.wait_ns))) {
+            if (lane == 0) give_up();
             ok = false;
             break;
           }
@@ -426,9 +511,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t d_tmem = tmem_base + buf * BN;
           for (int kb = w.k0; kb < w.k1; ++kb, ++it) {
             const int s = it % STAGES;
-            if (!mbar_wait_bounded(bar_full + 8 * s, (it / STAGES) & 1, abort_flag,
-                                   p.wait_ns)) {
-              give_up();
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(bar_full + 8 * s, (it / STAGES) & 1,
+                                                           abort_flag, p.wait_ns))) {
+              if (lane == 0) give_up();
               ok = false;
               break;
             }
@@ -460,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(bar_accf + 8 * buf);
         }
       }
-      // Every MMA this thread issued has completed before the CTA barrier
+      // Every MMA the warp issued has completed before the CTA barrier
       // below, so none still writes TMEM when warp 2 frees it.  After a
       // normal run the epilogue has waited for all of them already; after a
       // give-up (here or in the epilogue) some may still be running.
@@ -516,7 +601,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rit = q * 32 + lane;  // row within this CTA's 128 rows = TMEM lane
     int tc = 0;
     bool ok = true;
-    for (int u = tile0; u < sc.units && ok; u += tiles_in_flight) {
+    for (int wi = 0; ok; ++wi) {
+      // every lane waits and reads; the warp frees the slot once
+      int u = -1;
+      const bool got = take_unit(wi, u);
+      if (!__all_sync(0xFFFFFFFFu, got)) {
+        if (lane == 0) give_up();
+        break;
+      }
+      __syncwarp();
+      if (lane == 0) free_slot(wi);
+      if (u < 0) break;
       const Unit w = decode(sc, kEpi, u);
       const int rblk = w.m * TL::kCtas + static_cast<int>(rank);  // 128-row block of this CTA
       const int row = rblk * BM + rit;
@@ -629,13 +724,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (kEpi == EPI_LSE && ok) {
-        if (valid) {
-          const long long o = static_cast<long long>(w.slab) * p.Mcap + row;
-          dbg::st(p.part_m + o, st.m);
-          dbg::st(p.part_mc + o, st.mc);
-          dbg::st(p.part_s + o, st.s);
-          dbg::st(p.part_xt + o, xt);
-        }
+        if (valid)
+          dbg::st(p.part + static_cast<long long>(w.slab) * p.Mcap + row,
+                  make_float4(st.m, st.mc, st.s, xt));
         // Each epilogue warp counts its 32 rows' slabs; the warp completing
         // the count (the last slab to store them) merges the S partials of
         // each row in slab order and writes the row's results.
@@ -653,13 +744,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int ttile = tvalid ? tt / BN : -1;
           Lse2 acc = lse2_empty();
           float xtr = 0.f;
-          for (int sl = 0; sl < sc.S; ++sl) {
-            const long long o = static_cast<long long>(sl) * p.Mcap + row;
-            acc = lse2_merge(acc, Lse2{dbg::ldcg(p.part_m + o), dbg::ldcg(p.part_mc + o),
-                                       dbg::ldcg(p.part_s + o)});
-            const int n0 = static_cast<int>(static_cast<long long>(sl) * sc.n_tiles / sc.S);
-            const int n1 = static_cast<int>(static_cast<long long>(sl + 1) * sc.n_tiles / sc.S);
-            if (ttile >= n0 && ttile < n1) xtr = dbg::ldcg(p.part_xt + o);
+          // eight slabs' partials in flight at a time, merged in slab order
+          constexpr int kBatch = 8;
+          for (int s0 = 0; s0 < sc.S; s0 += kBatch) {
+            float4 pv[kBatch];
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j)
+              pv[j] = s0 + j < sc.S
+                          ? dbg::ldcg(p.part + static_cast<long long>(s0 + j) * p.Mcap + row)
+                          : make_float4(-INFINITY, -INFINITY, 0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+              const int sl = s0 + j;
+              if (sl >= sc.S) break;
+              acc = lse2_merge(acc, Lse2{pv[j].x, pv[j].y, pv[j].z});
+              const int n0 = static_cast<int>(static_cast<long long>(sl) * sc.n_tiles / sc.S);
+              const int n1 = static_cast<int>(static_cast<long long>(sl + 1) * sc.n_tiles / sc.S);
+              if (ttile >= n0 && ttile < n1) xtr = pv[j].w;
+            }
           }
           write_row_result(acc, xtr, tvalid, p.T, p.c, p.out_lp, p.out_lse, p.err, orig);
         }
@@ -718,7 +820,11 @@ __global__ void __launch_bounds__(1024)
   __shared__ int carry;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int j = threadIdx.x; j < n_row_cnt; j += blockDim.x) dbg::st(row_cnt + j, 0);
-  if (threadIdx.x == 0) carry = 0;
+  if (threadIdx.x == 0) {
+    carry = 0;
+    dbg::st(counters + 1, 0);  // unit counters of the GEMM launches that follow
+    dbg::st(counters + 2, 0);
+  }
   __syncthreads();
   for (int base = 0; base < N; base += 1024 * kRows) {
     const int r0 = base + threadIdx.x * kRows;
@@ -955,7 +1061,7 @@ struct Layout {
   int Mcap;
   int vchunk;          // vocabulary columns per backward chunk
   long long ld_dz;     // row stride of the dz chunk buffer
-  size_t off_counters, off_rcnt, off_pos, off_idx, off_hc, off_pm, off_pmc, off_ps, off_pxt, fwd_end;
+  size_t off_counters, off_rcnt, off_pos, off_idx, off_hc, off_part, fwd_end;
   size_t off_dz, off_pf32, off_acc, bwd_end;
 };
 
@@ -988,13 +1094,9 @@ Layout layout(int64_t N, int64_t V, int64_t d, int64_t vchunk = kVChunk) {
   L.off_pos = o; o = align256(o + 4 * static_cast<size_t>(N));
   L.off_idx = o; o = align256(o + 4 * static_cast<size_t>(L.Mcap));
   L.off_hc = o; o = align256(o + 2 * static_cast<size_t>(L.Mcap) * d);
-  const size_t part = 4 * static_cast<size_t>(kSlabCap) * L.Mcap;
-  L.off_pm = o; o = align256(o + part);
-  L.off_pmc = o; o = align256(o + part);
-  L.off_ps = o; o = align256(o + part);
-  L.off_pxt = o; o = align256(o + part);
+  L.off_part = o; o = align256(o + 16 * static_cast<size_t>(kSlabCap) * L.Mcap);
   L.fwd_end = o;
-  L.off_dz = L.off_pm;  // the backward does not use the forward partials
+  L.off_dz = L.off_part;  // the backward does not use the forward partials
   o = align256(L.off_dz + 2 * static_cast<size_t>(L.Mcap) * L.ld_dz);
   L.off_pf32 = o;
   size_t pf = max_partial_floats(L.Mcap, static_cast<int>(V), L.vchunk, static_cast<int>(d), L.geo);
@@ -1023,6 +1125,14 @@ cudaError_t launch(const Layout& L, const CUtensorMap& a, const CUtensorMap& b, 
 
 // Bound of the pipeline waits for the launches that follow (process-wide).
 std::atomic<unsigned long long> g_wait_ns{kWaitLimitNs};
+
+// The j-th GEMM launch of a call counts its units on counters[1 + j % 2] and
+// zeroes the other for launch j + 1 (the scan zeroes both first).
+inline void set_launch(Params& p, int j) {
+  int32_t* c = const_cast<int32_t*>(p.counters);
+  p.work = c + 1 + (j & 1);
+  p.work_next = c + 1 + ((j + 1) & 1);
+}
 
 struct Prepared {
   Layout L;
@@ -1076,10 +1186,7 @@ cudaError_t prepare(const void* h, int64_t N, int64_t V, int64_t d, const int32_
   p.t = t;
   p.c = static_cast<float>(1.4426950408889634 / static_cast<double>(T));
   p.invT = 1.0f / T;
-  p.part_m = reinterpret_cast<float*>(w + P.L.off_pm);
-  p.part_mc = reinterpret_cast<float*>(w + P.L.off_pmc);
-  p.part_s = reinterpret_cast<float*>(w + P.L.off_ps);
-  p.part_xt = reinterpret_cast<float*>(w + P.L.off_pxt);
+  p.part = reinterpret_cast<float4*>(w + P.L.off_part);
   p.dz = reinterpret_cast<__nv_bfloat16*>(w + P.L.off_dz);
   p.ld_dz = P.L.ld_dz;
   p.part_f32 = reinterpret_cast<float*>(w + P.L.off_pf32);
@@ -1091,6 +1198,7 @@ cudaError_t prepare(const void* h, int64_t N, int64_t V, int64_t d, const int32_
   p.out_lse = lse;
   p.T = T;
   p.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+  set_launch(p, 0);
 #ifdef SLP_DEBUG_BOUNDS
   {
     const uint64_t n = static_cast<uint64_t>(N);
@@ -1102,12 +1210,9 @@ cudaError_t prepare(const void* h, int64_t N, int64_t V, int64_t d, const int32_
     sec(L.off_rcnt, L.off_pos);
     sec(L.off_pos, L.off_idx);
     sec(L.off_idx, L.off_hc);
-    sec(L.off_hc, L.off_pm);
+    sec(L.off_hc, L.off_part);
     if (logprob != nullptr) {  // forward: the slab partials
-      sec(L.off_pm, L.off_pmc);
-      sec(L.off_pmc, L.off_ps);
-      sec(L.off_ps, L.off_pxt);
-      sec(L.off_pxt, L.fwd_end);
+      sec(L.off_part, L.fwd_end);
     } else {  // backward: dz chunk, split-K partials, dh accumulator
       sec(L.off_dz, L.off_pf32);
       sec(L.off_pf32, L.off_acc);
@@ -1187,6 +1292,7 @@ cudaError_t launch_lmhead_backward(const void* h, const void* W, int64_t N, int6
     return cudaErrorInvalidValue;
   const uint64_t dz_row = static_cast<uint64_t>(P.L.ld_dz) * 2;
   const __nv_bfloat16* Wb = static_cast<const __nv_bfloat16*>(W);
+  int j = 0;  // GEMM launches so far
   for (int64_t v0 = 0; v0 < V; v0 += P.L.vchunk) {
     const int64_t vc = V - v0 < P.L.vchunk ? V - v0 : P.L.vchunk;
     Params pc = P.p;
@@ -1204,10 +1310,13 @@ cudaError_t launch_lmhead_backward(const void* h, const void* W, int64_t N, int6
         !make_map(&m_w_mn, Wc, d, vc, d * 2, 64, BK) ||               // B of dh (N = d)
         !make_map(&m_dz_mn, pc.dz, vc, P.L.Mcap, dz_row, 64, BK))     // A of dW (M = chunk)
       return cudaErrorInvalidValue;
+    set_launch(pc, j++);
     e = launch<EPI_DZ, false, false>(P.L, m_hc_k, m_w_k, pc, stream SLP_DBG_PASS(P.bnd));
     if (e != cudaSuccess) return e;
+    set_launch(pc, j++);
     e = launch<EPI_F32, false, true>(P.L, m_dz_k, m_w_mn, pc, stream SLP_DBG_PASS(P.bnd));
     if (e != cudaSuccess) return e;
+    set_launch(pc, j++);
     pc.dh_fold = 1;
     e = accumulate_f32
             ? launch<EPI_ACC32, true, true>(P.L, m_dz_mn, m_hc_mn, pc, stream SLP_DBG_PASS(P.bnd))

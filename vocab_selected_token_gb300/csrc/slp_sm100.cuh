@@ -49,31 +49,54 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// kCluster: acquire at cluster scope, for a phase completed by an arrival
+// (release.cluster) from the other CTA of a pair that orders the data it
+// published into this CTA's shared memory.
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
+  if (kCluster)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
   return ok != 0;
 }
 
 // As mbar_try_wait, but the thread is suspended for at most about hint_ns
 // nanoseconds while the phase is incomplete (instead of the hardware's own
 // window, which can outlast a short wait bound by itself).
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity,
                                                    uint32_t hint_ns) {
   uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(hint_ns)
-      : "memory");
+  if (kCluster)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
   return ok != 0;
 }
 
@@ -86,16 +109,19 @@ constexpr uint64_t kShortWaitNs = 1000000;
 // clock) or as soon as *abort is set by another thread (abort may be NULL:
 // then only the limit applies).  Returns false when it gave up; a wait that
 // ran out also sets *abort.
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   volatile int* abort, uint64_t limit_ns) {
   const bool short_bound = limit_ns < kShortWaitNs;
   const uint32_t hint = static_cast<uint32_t>(limit_ns);
-  if (short_bound ? mbar_try_wait_hint(bar, parity, hint) : mbar_try_wait(bar, parity))
+  if (short_bound ? mbar_try_wait_hint<kCluster>(bar, parity, hint)
+                  : mbar_try_wait<kCluster>(bar, parity))
     return true;
   const uint64_t t0 = sm_cycles();
   const uint64_t limit = limit_ns * kCyclesPerNs;
   for (uint32_t i = 1;; ++i) {
-    if (short_bound ? mbar_try_wait_hint(bar, parity, hint) : mbar_try_wait(bar, parity))
+    if (short_bound ? mbar_try_wait_hint<kCluster>(bar, parity, hint)
+                    : mbar_try_wait<kCluster>(bar, parity))
       return true;
     if (short_bound || (i & 63u) == 0) {
       if (abort != nullptr && *abort) return false;
@@ -191,22 +217,33 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
+// The MMA and commit helpers below are executed by a whole converged warp with
+// warp-uniform operands; elect.sync picks one lane (the lowest, the same one
+// every time) to issue the instruction.  Keeping the issuing loop warp-wide
+// lets the operands stay warp-uniform values, so the issue costs a few cycles
+// per instruction instead of the per-lane conversions a one-thread branch
+// needs.
+
 // D[tmem] (+)= A[smem] * B[smem]^T, one instruction (M x N x 16 for bf16).
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                          uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
+      "{\n\t.reg .pred e, p;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
 // Arrive once on an mbarrier when every tcgen05 operation issued so far by
-// this thread has completed.
+// the elected lane has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          bar)
       : "memory");
 }
 
@@ -334,9 +371,10 @@ __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols
 __device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                               uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
+      "{\n\t.reg .pred e, p;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
@@ -346,8 +384,10 @@ __device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, u
 // have completed.
 __device__ __forceinline__ void mma_commit_pair_mc(uint32_t bar, uint16_t cta_mask) {
   asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar),
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;\n\t}" ::"r"(bar),
       "h"(cta_mask)
       : "memory");
 }
@@ -355,7 +395,10 @@ __device__ __forceinline__ void mma_commit_pair_mc(uint32_t bar, uint16_t cta_ma
 // Same, on this CTA's mbarrier only.
 __device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
   asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          bar)
       : "memory");
 }
 
