@@ -76,7 +76,8 @@ LOGITS = [
     ("c151k", 48, 151936),         # cluster-split rows
     ("c151k", 33, 151936 - 5),     # ragged vector tail
     ("packed", 3000, 20016),       # masked spans, warp-per-row kernels
-    ("stability", 256, 131072),    # fp32, -inf columns
+    ("stability", 256, 131072),    # fp32, -inf columns; fused: TMEM part, 4 CTAs
+    ("stability", 20, 100000),     # fp32, fused: TMEM part, 3 CTAs per row instead of 6
     ("stability", 64, 4099),
     ("tiny", 300, 2047),           # rows not 16-byte aligned: scalar kernels
 ]

@@ -116,7 +116,9 @@ FB_ENT = [
     ("stability", 40, 3000),       # fp32 short rows
     ("c151k", 48, 151936),         # cluster of 4 CTAs per row
     ("packed", 300, 20016),        # 40 KB rows: cluster
-    ("stability", 256, 131072),    # fp32, rows with -inf columns
+    ("stability", 256, 131072),    # fp32, rows with -inf columns; TMEM part, 4 CTAs
+    ("stability", 24, 65536),      # fp32, TMEM part: 2 CTAs per row instead of 4
+    ("stability", 16, 150000),     # fp32, TMEM part: 5 CTAs per row instead of 8
     ("tiny", 300, 2047),           # unaligned rows: the separate kernels
 ]
 

@@ -338,7 +338,8 @@ FB_SCALED = [
     ("c151k", 48, 151936),            # cluster of 4
     ("c151k", 33, 151936 - 5),        # ragged tail: rows not 16-byte aligned -> separate kernels
     ("packed", 3000, 20016),
-    ("stability", 256, 131072),       # fp32, cluster of 6
+    ("stability", 256, 131072),       # fp32: 4 CTAs with the TMEM part (7 without)
+    ("stability", 40, 75968),         # fp32, 4 CTAs: the TMEM part would save only one
     ("tiny", 300, 2047),              # unaligned rows -> separate kernels
 ]
 
@@ -461,6 +462,30 @@ def test_fused_short_rows_ragged_tail(V):
     torch.cuda.synchronize()
     assert bool((gx[:, V:] == 7.0).all())
     check_rows(x, t, None, a.T, a.g, lp, lse, gx[:, :V], range(48))
+
+
+@pytest.mark.parametrize("V", [65536, 100000, 150000])
+def test_fused_tmem_form_fp32_rows(V):
+    """fp32 rows for which the fused call keeps part of each segment in TMEM
+    (2, 3 and 5 CTAs per row instead of 4, 6 and 8): every row against the
+    oracle, with two masked rows and one bad target, then the same call again
+    bit for bit."""
+    dev = device()
+    a = W.make_logits_inputs("stability", device=dev, N=20, V=V)
+    mask = torch.ones(20, dtype=torch.uint8, device=dev)
+    mask[3] = 0
+    mask[11] = 0
+    t = a.t.clone()
+    t[7] = V + 5
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    lp, lse, gx = slp.slp_forward_backward(a.x, t, mask, a.T, a.g, err=err)
+    lp2, lse2, gx2 = slp.slp_forward_backward(a.x, t, mask, a.T, a.g)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 1  # the bad target's data error, nothing else
+    assert np.isnan(float(lp[7])) and bool(torch.isnan(gx[7]).all())
+    check_rows(a.x, t, mask, a.T, a.g, lp, lse, gx, [r for r in range(20) if r != 7])
+    assert torch.equal(lp.view(torch.int32), lp2.view(torch.int32))
+    assert torch.equal(gx.view(torch.int32), gx2.view(torch.int32))
 
 
 def test_fused_forward_backward_bad_target():

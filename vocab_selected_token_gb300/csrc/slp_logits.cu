@@ -38,7 +38,6 @@
 namespace slp {
 
 constexpr int kFwdThreads = 256;
-constexpr int kFwdUnroll = 4;  // elements per thread per batch on the scalar path
 constexpr int kFwdChunk = 16384;  // bytes per bulk copy (4 vectors per thread)
 // Shared-memory ring of the vector path, in chunks: four (64 KB, three CTAs
 // per SM) for the plain log-sum-exp; two (32 KB, six CTAs per SM) with the
@@ -529,13 +528,49 @@ constexpr int kFbMaxSeg = kFbChunk * kFbMaxChunks;  // 96 KB per CTA
 constexpr int kFbRV = 5;
 constexpr int kFbRegSeg = 233472 / 4 - 1024 - 256 + kFbRV * kFbThreads * 16;
 constexpr int kFbMaxCluster = 8;
+// TMEM part: kFbTV more vectors per thread in tensor memory (tcgen05.st /
+// tcgen05.ld, 32 lanes x 4 kFbTV columns per warp, 128 columns per CTA).  An
+// SM's 512 TMEM columns hold four such CTAs, so the form reserves at least
+// kFbTmMinSmem bytes of shared memory per CTA: a fifth CTA never fits on an
+// SM, and no tcgen05.alloc ever waits for columns.
+constexpr int kFbTV = 16;
+constexpr int kFbTmCols = 128;
+constexpr int kFbTmMinSmem = 233472 / 5 - 1024 - 256 + 1;  // 5 CTAs would need more
+constexpr int kFbTmSeg = kFbRegSeg + kFbTV * kFbThreads * 16;
+
+// The TMEM part in pass 2: kTV vectors of this thread read back four at a
+// time (16 columns per tcgen05.ld), each handed to put(i, v).
+template <int kTV, typename Put>
+__device__ __forceinline__ void put_tmem(uint32_t taddr, int nv_s, int nv, Put& put) {
+#pragma unroll 1
+  for (int b = 0; b < kTV / 4; ++b) {
+    uint4 tv[4];
+    sm100::tmem_ld_4vec(taddr + 16 * b, tv);
+    sm100::tmem_ld_wait();
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = nv_s + (4 * b + u) * kFbThreads + threadIdx.x;
+      if (i < nv) put(i, tv[u]);
+    }
+  }
+}
+
+// Every thread has finished with TMEM: warp 0 frees the CTA's columns.
+__device__ __forceinline__ void free_tmem(uint32_t base) {
+  sm100::tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    sm100::tc_fence_after();
+    sm100::tmem_dealloc(base, kFbTmCols);
+  }
+}
 
 // kEnt adds the entropy: the state carries the entropy accumulator, the row
 // results include H (`entropy`), and the gradient gains the entropy term
 // -gH p (log p + H) / T computed from the lse and H written here, exactly as
 // slp_bwd_kernel computes it from the saved ones (g and gH may then be NULL,
 // meaning zero).
-template <typename Elt, int kRV, bool kEnt>
+template <typename Elt, int kRV, int kTV, bool kEnt>
 __global__ void __launch_bounds__(kFbThreads, kRV > 0 ? 4 : 1)
     slp_fwd_bwd_kernel(const Elt* __restrict__ x, int64_t V, int64_t ld,
                        const int32_t* __restrict__ t, const uint8_t* __restrict__ mask, float T,
@@ -561,9 +596,12 @@ __global__ void __launch_bounds__(kFbThreads, kRV > 0 ? 4 : 1)
   const int64_t v1 = nvec * (rank + 1) / C;
   const int nv = static_cast<int>(v1 - v0);  // vectors of this segment
   // the last kRV * kFbThreads vectors of the segment stay in registers (kRV
-  // per thread), the rest in shared memory
+  // per thread), the kTV * kFbThreads before them in TMEM (kTV per thread),
+  // the rest in shared memory
   constexpr int kRegVec = kRV * kFbThreads;
-  const int nv_s = nv > kRegVec ? nv - kRegVec : 0;
+  constexpr int kTmVec = kTV * kFbThreads;
+  const int nv_s = nv > kRegVec + kTmVec ? nv - kRegVec - kTmVec : 0;
+  const int nv_r = nv_s + kTmVec;  // first vector of the register part
   const Elt* tag = nullptr;
   uint4* gv = reinterpret_cast<uint4*>(gx + row * ldg) + v0;
 
@@ -600,7 +638,19 @@ __global__ void __launch_bounds__(kFbThreads, kRV > 0 ? 4 : 1)
     abort_flag = 0;
     sm100::fence_mbar_init();
   }
+  __shared__ uint32_t tmem_holder;
+  if constexpr (kTV > 0) {
+    if (threadIdx.x < 32) sm100::tmem_alloc(sm100::smem_u32(&tmem_holder), kFbTmCols);
+    sm100::tc_fence_before();
+  }
   __syncthreads();
+  uint32_t taddr = 0;  // this thread's TMEM lane and first column
+  if constexpr (kTV > 0) {
+    sm100::tc_fence_after();
+    const int w = threadIdx.x >> 5;
+    taddr = tmem_holder + (static_cast<uint32_t>((w & 3) * 32) << 16) +
+            static_cast<uint32_t>((w >> 2) * kTV * 4);
+  }
   if (threadIdx.x == 0) {
     const char* src = reinterpret_cast<const char*>(reinterpret_cast<const uint4*>(xr) + v0);
     for (int k = 0; k < nch; ++k) {
@@ -618,7 +668,7 @@ __global__ void __launch_bounds__(kFbThreads, kRV > 0 ? 4 : 1)
     const uint4* xv = reinterpret_cast<const uint4*>(xr) + v0;
 #pragma unroll
     for (int u = 0; u < kRV; ++u) {
-      const int i = nv_s + u * kFbThreads + threadIdx.x;
+      const int i = nv_r + u * kFbThreads + threadIdx.x;
       rv[u] = i < nv ? ld_stream_ef(xv + i) : pad;
     }
   }
@@ -626,6 +676,29 @@ __global__ void __launch_bounds__(kFbThreads, kRV > 0 ? 4 : 1)
   // pass 1: online log-sum-exp over the segment as its chunks land
   St st;
   st_empty(st);
+  if constexpr (kTV > 0) {
+    // TMEM part, four vectors at a time: loaded, folded, stored to this
+    // thread's lane (16 columns per tcgen05.st)
+    const uint4* xv = reinterpret_cast<const uint4*>(xr) + v0;
+    auto load4 = [&](uint4 (&tv)[4], int b) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = nv_s + (4 * b + u) * kFbThreads + threadIdx.x;
+        tv[u] = i < nv ? ld_stream_ef(xv + i) : pad;
+      }
+    };
+#pragma unroll 1
+    for (int b = 0; b < kTV / 4; ++b) {
+      uint4 tv[4];
+      load4(tv, b);
+      if constexpr (kEnt)
+        lse3_fold_vec<4>(st, tv, c, tag);
+      else
+        lse2_fold_vec<4>(st, tv, c, tag);
+      sm100::tmem_st_4vec(taddr + 16 * b, tv);
+    }
+    sm100::tmem_st_wait();
+  }
   const uint4* q = reinterpret_cast<const uint4*>(seg);
   constexpr int kPer = kFbChunk / 16 / kFbThreads;
   bool ok = true;
@@ -745,16 +818,18 @@ __global__ void __launch_bounds__(kFbThreads, kRV > 0 ? 4 : 1)
       if (i == tvec) E::store1(gr + tt, b.one(E::load1(xr + tt), c, true));
     };
     for (int i = threadIdx.x; i < nv_s; i += kFbThreads) put(i, q[i]);
+    if constexpr (kTV > 0) put_tmem<kTV>(taddr, nv_s, nv, put);
     if constexpr (kRV > 0) {
 #pragma unroll
       for (int u = 0; u < kRV; ++u) {
-        const int i = nv_s + u * kFbThreads + threadIdx.x;
+        const int i = nv_r + u * kFbThreads + threadIdx.x;
         if (i < nv) put(i, rv[u]);
       }
     }
     if (rank == C - 1)
       for (int64_t e = nvec * kVec + threadIdx.x; e < V; e += kFbThreads)
         E::store1(gr + e, b.one(E::load1(xr + e), c, e == tt));
+    if constexpr (kTV > 0) free_tmem(tmem_holder);
     asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
     return;
   }
@@ -778,10 +853,11 @@ __global__ void __launch_bounds__(kFbThreads, kRV > 0 ? 4 : 1)
     }
   };
   for (int i = threadIdx.x; i < nv_s; i += kFbThreads) put(i, q[i]);
+  if constexpr (kTV > 0) put_tmem<kTV>(taddr, nv_s, nv, put);
   if constexpr (kRV > 0) {
 #pragma unroll
     for (int u = 0; u < kRV; ++u) {
-      const int i = nv_s + u * kFbThreads + threadIdx.x;
+      const int i = nv_r + u * kFbThreads + threadIdx.x;
       if (i < nv) put(i, rv[u]);
     }
   }
@@ -791,6 +867,7 @@ __global__ void __launch_bounds__(kFbThreads, kRV > 0 ? 4 : 1)
       E::store1(gx + row * ldg + e, (e == tt) ? fmaf(a, p, gT) : a * p);
     }
   }
+  if constexpr (kTV > 0) free_tmem(tmem_holder);
   asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
 }
 
@@ -1155,6 +1232,19 @@ cudaError_t fwd_bwd_rows_typed(const Elt* x, int64_t N, int64_t V, int64_t ld, c
 #undef SLP_FB_ROWS
 }
 
+// Whether the fused call runs the form with a TMEM part (C CTAs per row
+// without it, C_tm with): fp32 rows on which it saves at least two CTAs.
+// Measured (fused call, CUDA events, one box): fp32 rows of 65536 / 100000 /
+// 131072 / 150000 columns (4 -> 2, 6 -> 3, 7 -> 4, 8 -> 5 CTAs) take 8 / 10
+// / 7 / 5 % less time; 75968 columns (4 -> 3) 1 % more.  On bf16 rows, which
+// carry twice the elements per byte, the form lost at every size tried
+// (c151k 4 -> 3 CTAs: 0.414 against 0.396 ms; 248320 columns, 7 -> 4: 1.535
+// against 1.443 ms): there the TMEM part's loads, four vectors per round
+// trip, and its fold come before the shared-memory chunks are consumed.
+inline bool tmem_fused_form(bool regs, int64_t C, int64_t C_tm, size_t esize) {
+  return regs && esize == 4 && C_tm <= C - 2;
+}
+
 // Fused forward + backward: needs 16-byte-aligned rows and rows short enough
 // to fit a cluster of at most 8 CTAs x 96 KB; returns cudaErrorNotSupported
 // otherwise (the caller then runs the separate kernels).  gH and entropy are
@@ -1178,12 +1268,21 @@ cudaError_t fwd_bwd_typed(const Elt* x, int64_t N, int64_t V, int64_t ld, const 
   int64_t C = regs ? (nvec * 16 + kFbRegSeg - 1) / kFbRegSeg
                    : (nvec * 16 + kFbMaxSeg - 1) / kFbMaxSeg;
   if (C < 1) C = 1;
+  // With a TMEM part as well, a segment holds kFbTmSeg bytes: long rows then
+  // need fewer CTAs per cluster.
+  const int64_t C_tm = (nvec * 16 + kFbTmSeg - 1) / kFbTmSeg;
+  const bool tm = tmem_fused_form(regs, C, C_tm, sizeof(Elt));
+  if (tm) C = C_tm;
   if (C > kFbMaxCluster) return cudaErrorNotSupported;
   if (N * C > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
   const int64_t per = (nvec + C - 1) / C;  // vectors of the longest segment
-  const int64_t in_smem = regs ? (per > kFbRV * kFbThreads ? per - kFbRV * kFbThreads : 0) : per;
-  const int smem = static_cast<int>(in_smem * 16);
-  auto kern = regs ? slp_fwd_bwd_kernel<Elt, kFbRV, kEnt> : slp_fwd_bwd_kernel<Elt, 0, kEnt>;
+  const int64_t on_chip = regs ? (kFbRV + (tm ? kFbTV : 0)) * kFbThreads : 0;
+  const int64_t in_smem = per > on_chip ? per - on_chip : 0;
+  int smem = static_cast<int>(in_smem * 16);
+  if (tm && smem < kFbTmMinSmem) smem = kFbTmMinSmem;
+  auto kern = tm     ? slp_fwd_bwd_kernel<Elt, kFbRV, kFbTV, kEnt>
+              : regs ? slp_fwd_bwd_kernel<Elt, kFbRV, 0, kEnt>
+                     : slp_fwd_bwd_kernel<Elt, 0, 0, kEnt>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kFbMaxSeg);
   if (e != cudaSuccess) return e;
   const float c = static_cast<float>(1.4426950408889634 / static_cast<double>(T));

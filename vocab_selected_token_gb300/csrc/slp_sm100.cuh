@@ -266,6 +266,32 @@ __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Four 16-byte vectors of this thread to / from 16 consecutive 32-bit TMEM
+// columns of its warp's lanes (one lane per thread).
+__device__ __forceinline__ void tmem_st_4vec(uint32_t taddr, const uint4 (&v)[4]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(v[0].x), "r"(v[0].y), "r"(v[0].z), "r"(v[0].w), "r"(v[1].x), "r"(v[1].y), "r"(v[1].z),
+      "r"(v[1].w), "r"(v[2].x), "r"(v[2].y), "r"(v[2].z), "r"(v[2].w), "r"(v[3].x), "r"(v[3].y),
+      "r"(v[3].z), "r"(v[3].w)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_4vec(uint32_t taddr, uint4 (&v)[4]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(v[0].x), "=r"(v[0].y), "=r"(v[0].z), "=r"(v[0].w), "=r"(v[1].x), "=r"(v[1].y),
+        "=r"(v[1].z), "=r"(v[1].w), "=r"(v[2].x), "=r"(v[2].y), "=r"(v[2].z), "=r"(v[2].w),
+        "=r"(v[3].x), "=r"(v[3].y), "=r"(v[3].z), "=r"(v[3].w)
+      : "r"(taddr));
+}
+
 // UMMA shared-memory descriptor for a 128-byte-swizzled operand tile.
 //   K-major  : rows of 64 bf16 (128 B); 8-row groups 1024 B apart (SBO);
 //              LBO unused.
