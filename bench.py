@@ -50,6 +50,8 @@ def parse():
     p.add_argument("--lmhead-only", action="store_true",
                    help="time only the fused LM-head path and print its numbers")
     p.add_argument("--lmhead-rows", type=int, default=None)
+    p.add_argument("--fused-only", action="store_true",
+                   help="time only the fused forward+backward on --config (and --rows)")
     p.add_argument("--rows", type=int, default=None,
                    help="override N (same recipe), e.g. for a small profiling case")
     return p.parse_args()
@@ -426,6 +428,12 @@ def main():
         if rank == 0:
             print(json.dumps({"lmhead": r}), flush=True)
         return
+    if args.fused_only:
+        r = time_fused(device, hbm, steps=args.steps, warmup=args.warmup, names=(args.config,),
+                       N=args.rows)
+        if rank == 0:
+            print(json.dumps({"fused_fwd_bwd": r}), flush=True)
+        return
 
     inp = W.make_logits_inputs(args.config, device=device, N=args.rows)
     fwd_b, bwd_b, na = logits_bytes(inp.x, inp.mask)
@@ -704,15 +712,15 @@ def time_topk(device, hbm, steps=20, warmup=3):
     return res
 
 
-def time_fused(device, hbm, steps=30, warmup=3):
+def time_fused(device, hbm, steps=30, warmup=3, names=("c151k", "packed", "stability"), N=None):
     """slp_forward_backward (upstream gradient known at forward time): one
     read of the active rows and one write of the gradient per step."""
     from vocab_selected_token_gb300 import _lib
     from vocab_selected_token_gb300 import workloads as W
     lib = _lib.load()
     out = {}
-    for name in ("c151k", "packed", "stability"):
-        inp = W.make_logits_inputs(name, device=device)
+    for name in names:
+        inp = W.make_logits_inputs(name, device=device, N=N)
         x = inp.x
         N, V = x.shape
         es = x.element_size()
