@@ -233,6 +233,37 @@ def test_lmhead_matches_logits_path():
         assert cos >= 0.9999 and frob <= 1e-2, f"{what}: cosine {cos:.6f} frob {frob:.3e}"
 
 
+def test_dirty_workspace_is_harmless():
+    """Every workspace value a call reads it wrote first: the scan zeroes the
+    counters from which the GEMMs' pairs claim their units (each GEMM zeroes
+    the next launch's) and the forward's slab counters.  A workspace filled
+    with 0xFF before a forward, the backward on the forward's leftovers, then
+    a forward with another mask and temperature on a workspace filled with
+    0x7F: each matches the oracle."""
+    dev = device()
+    N, V, d = 700, 30000, 256
+    a = W.make_lmhead_inputs(device=dev, N=N, V=V, d=d, p_mask=0.6, seed=77)
+    ws = torch.full((slp.slp_lmhead_workspace_size(N, V, d),), 0xFF, dtype=torch.uint8,
+                    device=dev)
+    lp, lse = slp.slp_lmhead_forward(a.h, a.W, a.t, a.mask, a.T, ws=ws)
+    dh, dW = slp.slp_lmhead_backward(a.h, a.W, a.t, a.mask, a.T, lse, a.g, ws=ws)
+    mask2 = (torch.arange(N, device=dev) % 3 != 0).to(torch.uint8)
+    ws.fill_(0x7F)
+    lp2, lse2 = slp.slp_lmhead_forward(a.h, a.W, a.t, mask2, 0.6, ws=ws)
+    torch.cuda.synchronize()
+    h64, W64 = to64(a.h), to64(a.W)
+    t, m, g = a.t.cpu().numpy(), a.mask.cpu().numpy(), to64(a.g)
+    rlp, rlse = O.lmhead_forward(h64, W64, t, m, a.T)
+    assert_close_nan(to64(lp), rlp, TOL_LP, "logprob")
+    assert_close_nan(to64(lse), rlse, TOL_LP, "lse")
+    rdh, rdW = O.lmhead_backward(h64, W64, t, m, a.T, rlse, g)
+    grad_ok(to64(dh), rdh, "dh")
+    grad_ok(to64(dW), rdW, "dW")
+    rlp2, rlse2 = O.lmhead_forward(h64, W64, t, mask2.cpu().numpy(), 0.6)
+    assert_close_nan(to64(lp2), rlp2, TOL_LP, "logprob, second mask")
+    assert_close_nan(to64(lse2), rlse2, TOL_LP, "lse, second mask")
+
+
 @pytest.mark.parametrize("extra", ["max", "middle", "default-less", "min"])
 def test_backward_chunk_width_follows_the_workspace(extra):
     """The backward's vocabulary chunk follows the workspace: the whole
