@@ -464,26 +464,32 @@ def test_fused_short_rows_ragged_tail(V):
     check_rows(x, t, None, a.T, a.g, lp, lse, gx[:, :V], range(48))
 
 
-@pytest.mark.parametrize("V", [65536, 100000, 150000])
-def test_fused_tmem_form_fp32_rows(V):
+@pytest.mark.parametrize("V,Vp", [(65536, 65536), (100000, 100000), (150000, 150000),
+                                  (100001, 100004)])
+def test_fused_tmem_form_fp32_rows(V, Vp):
     """fp32 rows for which the fused call keeps part of each segment in TMEM
-    (2, 3 and 5 CTAs per row instead of 4, 6 and 8): every row against the
+    (2, 3, 5 and 3 CTAs per row instead of 4, 6, 8 and 6; the last with a
+    scalar tail of one element on a padded row stride): every row against the
     oracle, with two masked rows and one bad target, then the same call again
     bit for bit."""
     dev = device()
-    a = W.make_logits_inputs("stability", device=dev, N=20, V=V)
+    a = W.make_logits_inputs("stability", device=dev, N=20, V=Vp)
+    x = a.x[:, :V]
     mask = torch.ones(20, dtype=torch.uint8, device=dev)
     mask[3] = 0
     mask[11] = 0
-    t = a.t.clone()
+    t = a.t % V
     t[7] = V + 5
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    lp, lse, gx = slp.slp_forward_backward(a.x, t, mask, a.T, a.g, err=err)
-    lp2, lse2, gx2 = slp.slp_forward_backward(a.x, t, mask, a.T, a.g)
+    # gradients on the same padded stride, so both row sets stay 16-byte aligned
+    gx = torch.empty((20, Vp), dtype=x.dtype, device=dev)[:, :V]
+    gx2 = torch.empty((20, Vp), dtype=x.dtype, device=dev)[:, :V]
+    lp, lse, _ = slp.slp_forward_backward(x, t, mask, a.T, a.g, grad_x=gx, err=err)
+    lp2, lse2, _ = slp.slp_forward_backward(x, t, mask, a.T, a.g, grad_x=gx2)
     torch.cuda.synchronize()
     assert int(err.item()) == 1  # the bad target's data error, nothing else
     assert np.isnan(float(lp[7])) and bool(torch.isnan(gx[7]).all())
-    check_rows(a.x, t, mask, a.T, a.g, lp, lse, gx, [r for r in range(20) if r != 7])
+    check_rows(x, t, mask, a.T, a.g, lp, lse, gx, [r for r in range(20) if r != 7])
     assert torch.equal(lp.view(torch.int32), lp2.view(torch.int32))
     assert torch.equal(gx.view(torch.int32), gx2.view(torch.int32))
 
