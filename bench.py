@@ -430,7 +430,7 @@ def main():
         return
     if args.fused_only:
         r = time_fused(device, hbm, steps=args.steps, warmup=args.warmup, names=(args.config,),
-                       N=args.rows)
+                       rows=args.rows)
         if rank == 0:
             print(json.dumps({"fused_fwd_bwd": r}), flush=True)
         return
@@ -712,7 +712,8 @@ def time_topk(device, hbm, steps=20, warmup=3):
     return res
 
 
-def time_fused(device, hbm, steps=30, warmup=3, names=("c151k", "packed", "stability"), N=None):
+def time_fused(device, hbm, steps=30, warmup=3, names=("c151k", "packed", "stability"),
+               rows=None):
     """slp_forward_backward (upstream gradient known at forward time): one
     read of the active rows and one write of the gradient per step."""
     from vocab_selected_token_gb300 import _lib
@@ -720,7 +721,7 @@ def time_fused(device, hbm, steps=30, warmup=3, names=("c151k", "packed", "stabi
     lib = _lib.load()
     out = {}
     for name in names:
-        inp = W.make_logits_inputs(name, device=device, N=N)
+        inp = W.make_logits_inputs(name, device=device, N=rows)
         x = inp.x
         N, V = x.shape
         es = x.element_size()

@@ -94,3 +94,54 @@ def test_cpu_baseline_all_cores_runs_every_thread():
     inp = W.make_logits_inputs("tiny", device="cpu", N=64)
     v, rows, secs, cores = bench.oracle_rows_per_second_all_cores(inp, 0.2, rows_per_thread=4)
     assert cores >= 1 and rows >= 4 * cores and v > 0 and secs >= 0.2
+
+
+def test_fused_timing_builds_each_workload_at_its_own_size(monkeypatch):
+    """time_fused builds every workload with its recipe's own row count (or
+    the one override it is given), not with the row count of the workload
+    timed before it."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from vocab_selected_token_gb300 import _lib
+    from vocab_selected_token_gb300 import workloads as W
+
+    seen = []
+
+    class Stop(Exception):
+        pass
+
+    def fake(name, device="cpu", N=None, V=None, seed=None):
+        seen.append((name, N))
+        if len(seen) == 3:
+            raise Stop()
+        x = torch.zeros((W.WORKLOADS[name]["N"] if N is None else N, 8), dtype=torch.bfloat16)
+        return W.LogitsInputs(x=x, t=torch.zeros(x.shape[0], dtype=torch.int32), mask=None,
+                              T=1.0, g=torch.zeros(x.shape[0]), name=name)
+
+    class FakeLib:
+        def slp_forward_backward(self, *a):
+            return 0
+
+    monkeypatch.setattr(W, "make_logits_inputs", fake)
+    monkeypatch.setattr(_lib, "load", lambda: FakeLib())
+    monkeypatch.setattr(torch.cuda, "synchronize", lambda *a, **k: None)
+
+    class Ev:
+        def __init__(self, **k):
+            pass
+
+        def record(self, *a):
+            pass
+
+        def elapsed_time(self, other):
+            return 1.0
+
+    class St:
+        cuda_stream = 0
+
+    monkeypatch.setattr(torch.cuda, "Event", Ev)
+    monkeypatch.setattr(torch.cuda, "current_stream", lambda *a: St())
+    monkeypatch.setattr(torch.cuda, "empty_cache", lambda: None)
+    with pytest.raises(Stop):
+        bench.time_fused(torch.device("cpu"), 1.0, steps=1, warmup=1)
+    assert seen == [("c151k", None), ("packed", None), ("stability", None)]
