@@ -81,10 +81,45 @@ def traffic_table():
     return out
 
 
+def code_text(src):
+    """C++/CUDA source with its comments, trailing blanks and empty lines
+    removed: what a change to the compiled kernels must touch."""
+    out, i, n = [], 0, len(src)
+    quote = None
+    while i < n:
+        ch = src[i]
+        if quote:
+            out.append(ch)
+            if ch == "\\" and i + 1 < n:
+                out.append(src[i + 1])
+                i += 2
+                continue
+            if ch == quote:
+                quote = None
+            i += 1
+        elif ch in "\"'":
+            quote = ch
+            out.append(ch)
+            i += 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(ch)
+            i += 1
+    lines = [ln.rstrip() for ln in "".join(out).split("\n")]
+    return "\n".join(ln for ln in lines if ln.strip())
+
+
 def source_hash(fname):
+    """sha1 (12 hex digits) of a csrc file's code, comments excluded, so the
+    DRAM-traffic record stays tied to the kernels rather than their prose."""
     import hashlib
     p = os.path.join(ROOT, "vocab_selected_token_gb300", "csrc", fname)
-    return hashlib.sha1(open(p, "rb").read()).hexdigest()[:12]
+    return hashlib.sha1(code_text(open(p).read()).encode()).hexdigest()[:12]
 
 
 # ---------------------------------------------------------------- distributed

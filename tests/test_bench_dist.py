@@ -145,3 +145,17 @@ def test_fused_timing_builds_each_workload_at_its_own_size(monkeypatch):
     with pytest.raises(Stop):
         bench.time_fused(torch.device("cpu"), 1.0, steps=1, warmup=1)
     assert seen == [("c151k", None), ("packed", None), ("stability", None)]
+
+
+def test_code_hash_ignores_comments_only():
+    """The DRAM-traffic record is keyed on the kernels' code: comments and
+    blank lines do not change the hash, code and string contents do."""
+    sys.path.insert(0, ROOT)
+    import bench
+    a = 'int f() { return 1; }  // one\n/* block\n comment */\nconst char* s = "x//y";\n'
+    b = '// header\nint f() { return 1; }\n\n\nconst char* s = "x//y";   \n'
+    c = 'int f() { return 2; }\nconst char* s = "x//y";\n'
+    d = 'int f() { return 1; }\nconst char* s = "x/y";\n'
+    assert bench.code_text(a) == bench.code_text(b)
+    assert bench.code_text(a) != bench.code_text(c)
+    assert bench.code_text(a) != bench.code_text(d)

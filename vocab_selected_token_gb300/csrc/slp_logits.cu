@@ -18,8 +18,9 @@
 // g/T * (1[v == t] - p) with streaming stores.  Inactive rows only write zeros.
 //
 // Fused forward + backward (the upstream gradient known at forward time): a
-// cluster of CTAs holds each row on chip between the two passes, so the row
-// is read from HBM once.
+// cluster of CTAs holds each row on chip between the two passes (registers,
+// shared memory and, for long fp32 rows, tensor memory), so the row is read
+// from HBM once.
 //
 // Short rows (a few KB, small vocabularies) take kernels with one warp per
 // row instead, for the forward, the backward and the fused call: one CTA per
@@ -515,7 +516,9 @@ __global__ void __launch_bounds__(32 * kRowsWarps)
 // recompute the softmax instead of storing it; here the row stays on chip
 // between the two passes).  The row is read with an L2 evict-first policy:
 // it is read once, and L2 is better left to the gradient's write-back
-// (measured on c151k: 402 -> 394 us).
+// (measured on c151k: 402 -> 394 us).  Long fp32 rows also keep kFbTV more
+// vectors per thread in tensor memory (the TMEM part, see tmem_fused_form),
+// so their clusters need fewer CTAs.
 
 constexpr int kFbThreads = 256;
 constexpr int kFbChunk = 16384;
