@@ -264,6 +264,36 @@ def test_dirty_workspace_is_harmless():
     assert_close_nan(to64(lse2), rlse2, TOL_LP, "lse, second mask")
 
 
+def test_two_streams_at_once():
+    """Two forward + backward calls issued on two streams at once, each with
+    its own workspace: the second call's CTA pairs start while the first's
+    still hold SMs, and both claim their units from their own counters.  Each
+    matches the oracle."""
+    dev = device()
+    cases = [W.make_lmhead_inputs(device=dev, N=600, V=24000, d=256, p_mask=0.7, seed=s)
+             for s in (81, 82)]
+    streams = [torch.cuda.Stream(device=dev) for _ in cases]
+    outs = []
+    torch.cuda.synchronize()
+    for a, st in zip(cases, streams):
+        N, V, d = a.h.shape[0], a.W.shape[0], a.h.shape[1]
+        ws = torch.empty(slp.slp_lmhead_workspace_size(N, V, d), dtype=torch.uint8, device=dev)
+        with torch.cuda.stream(st):
+            lp, lse = slp.slp_lmhead_forward(a.h, a.W, a.t, a.mask, a.T, ws=ws, stream=st)
+            dh, dW = slp.slp_lmhead_backward(a.h, a.W, a.t, a.mask, a.T, lse, a.g, ws=ws,
+                                             stream=st)
+        outs.append((lp, lse, dh, dW, ws))
+    torch.cuda.synchronize()
+    for a, (lp, lse, dh, dW, _) in zip(cases, outs):
+        h64, W64 = to64(a.h), to64(a.W)
+        t, m, g = a.t.cpu().numpy(), a.mask.cpu().numpy(), to64(a.g)
+        rlp, rlse = O.lmhead_forward(h64, W64, t, m, a.T)
+        assert_close_nan(to64(lp), rlp, TOL_LP, "logprob")
+        rdh, rdW = O.lmhead_backward(h64, W64, t, m, a.T, rlse, g)
+        grad_ok(to64(dh), rdh, "dh")
+        grad_ok(to64(dW), rdW, "dW")
+
+
 @pytest.mark.parametrize("extra", ["max", "middle", "default-less", "min"])
 def test_backward_chunk_width_follows_the_workspace(extra):
     """The backward's vocabulary chunk follows the workspace: the whole
