@@ -225,7 +225,8 @@ int slp_topk_kl_backward(const void* x, int dtype, int64_t N, int64_t V, int64_t
  * between the log-sum-exp and the gradient pass: a row of at most 32 KB by
  * one warp (registers plus a shared-memory slot), a longer one by a
  * thread-block cluster that splits it across up to 8 CTAs' registers and
- * shared memory.  So the row's bytes are read once
+ * shared memory (and, for long float32 rows, tensor memory as well, 64 KB
+ * per CTA).  So the row's bytes are read once
  * instead of twice (NeMo-RL PR #4222, "Changes": recompute the softmax rather
  * than store it).  Rows that are not 16-byte aligned, or longer than
  * 8 x 96 KB, are served by slp_forward followed by slp_backward.
@@ -342,7 +343,9 @@ size_t slp_lmhead_workspace_size_max(int64_t N, int64_t V, int64_t d);
  * logits never stored.
  *
  * The GEMMs run on pairs of CTAs (thread-block clusters of two, one
- * tcgen05 MMA over both); on a device that cannot co-schedule such pairs, or
+ * tcgen05 MMA over both) that claim their tiles from a counter in the
+ * workspace; results do not depend on which pair computes which tile.  On a
+ * device that cannot co-schedule such pairs, or
  * with SLP_LMHEAD_CTA_PAIRS=0 in the environment before the first LM-head
  * call or workspace query, they run one CTA per tile.  The two forms agree
  * within the LM-head tolerances and need workspaces of different sizes: ask
