@@ -836,6 +836,9 @@ def time_lmhead(device, steps=40, warmup=3, N=None):
            "fwd_tflops": flop_f / (f_ms * 1e-3) / 1e12,
            "bwd_tflops": 3 * flop_f / (b_ms * 1e-3) / 1e12,
            "step_tflops": 4 * flop_f / ((f_ms + b_ms) * 1e-3) / 1e12,
+           # the same step counted without the backward's logits recompute
+           # (6 Na V d: the forward, dh and dW GEMMs)
+           "step_tflops_useful": 3 * flop_f / ((f_ms + b_ms) * 1e-3) / 1e12,
            "peak_bf16_tflops": peak, "peak_bf16_tflops_sustained": peak_sus, "peak_source": src,
            "workspace_bytes": int(ws_b), "clocks": clk}
     # the forward (~2 ms) is a burst against the burst peak; the backward and
