@@ -273,6 +273,66 @@ def time_logits(inp, steps, warmup, world, device, clocks=None):
             "outputs": (lp, lse, gx)}
 
 
+def host_topology(device):
+    """Where the host buffers live relative to the GPU: the CPUs this process
+    may run on, the host's NUMA nodes with their CPUs, and the GPU's PCI
+    NUMA node and local CPUs (from sysfs; None where not exposed)."""
+    def read(path):
+        try:
+            with open(path) as f:
+                return f.read().strip()
+        except OSError:
+            return None
+    info = {"process_cpus": len(os.sched_getaffinity(0))}
+    root = "/sys/devices/system/node"
+    nodes = {}
+    try:
+        for n in sorted(os.listdir(root)):
+            if n.startswith("node") and n[4:].isdigit():
+                nodes[n] = read(os.path.join(root, n, "cpulist"))
+    except OSError:
+        pass
+    info["numa_nodes"] = nodes
+    try:
+        pr = torch.cuda.get_device_properties(device)
+        bus = "%04x:%02x:%02x.0" % (pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
+        dev = os.path.join("/sys/bus/pci/devices", bus)
+        info["gpu_pci"] = bus
+        info["gpu_numa_node"] = read(os.path.join(dev, "numa_node"))
+        info["gpu_local_cpus"] = read(os.path.join(dev, "local_cpulist"))
+    except Exception:
+        info["gpu_pci"] = None
+    return info
+
+
+def host_link_rates(device, nbytes=1 << 29, reps=4):
+    """This machine's host link from page-locked memory: GB/s host->device,
+    device->host, and both directions at once (two streams), best of two
+    rounds of `reps` copies of `nbytes`."""
+    hs = [torch.empty(nbytes, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    ds = [torch.empty(nbytes, dtype=torch.uint8, device=device) for _ in range(2)]
+    st = [torch.cuda.Stream(device=device) for _ in range(2)]
+
+    def timed(jobs):
+        best = None
+        for _ in range(2):
+            torch.cuda.synchronize(device)
+            t0 = time.perf_counter()
+            for j, (dst, src) in enumerate(jobs):
+                with torch.cuda.stream(st[j]):
+                    for _ in range(reps):
+                        dst.copy_(src, non_blocking=True)
+            torch.cuda.synchronize(device)
+            dt = time.perf_counter() - t0
+            best = dt if best is None else min(best, dt)
+        return len(jobs) * reps * nbytes / best / 1e9
+
+    out = {"h2d_gbs": timed([(ds[0], hs[0])]), "d2h_gbs": timed([(hs[0], ds[0])]),
+           "both_gbs": timed([(ds[0], hs[0]), (hs[1], ds[1])])}
+    del hs, ds
+    return out
+
+
 def e2e_logits(inp, steps, device):
     """Same metric through the public API for host-resident data:
     vocab_selected_token_gb300.streaming.forward_backward_from_host streams the
@@ -303,10 +363,13 @@ def e2e_logits(inp, steps, device):
     for _ in range(steps):
         step()
     ms = (time.perf_counter() - t0) * 1000.0 / steps
+    link = host_link_rates(device)
+    link["e2e_frac_of_both"] = (h2d + d2h) / (ms * 1e-3) / 1e9 / link["both_gbs"]
     return {"value": N * 1000.0 / ms, "unit": UNIT, "ms_per_step": ms,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "api": "streaming.forward_backward_from_host -> slp_forward_backward_host "
-                   "(native 3-stream pipeline, ~64 MB chunks, fused forward+backward)"}
+                   "(native 3-stream pipeline, ~64 MB chunks, fused forward+backward)",
+            "host": host_topology(device), "host_link": link}
 
 
 # ---------------------------------------------------------------- oracle arm
