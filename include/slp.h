@@ -228,8 +228,9 @@ int slp_topk_kl_backward(const void* x, int dtype, int64_t N, int64_t V, int64_t
  * shared memory (and, for long float32 rows, tensor memory as well, 64 KB
  * per CTA).  So the row's bytes are read once
  * instead of twice (NeMo-RL PR #4222, "Changes": recompute the softmax rather
- * than store it).  Rows that are not 16-byte aligned, or longer than
- * 8 x 96 KB, are served by slp_forward followed by slp_backward.
+ * than store it).  Rows that are not 16-byte aligned, or longer than eight
+ * such CTAs hold (about 1.1 MB), are served by slp_forward followed by
+ * slp_backward.
  *
  *   x, dtype, N, V, ld, t, mask, T   as for slp_forward.
  *   grad_out  [N] float32 upstream gradient of logprob.
@@ -252,7 +253,7 @@ int slp_forward_backward(const void* x, int dtype, int64_t N, int64_t V, int64_t
  * slp_forward_backward, so it is read from HBM once instead of twice.  The
  * gradient is computed from the lse and entropy this call writes, with the
  * same per-element arithmetic as slp_backward_entropy.  Rows that are not
- * 16-byte aligned, or longer than 8 x 96 KB, are served by
+ * 16-byte aligned, or longer than about 1.1 MB, are served by
  * slp_forward_entropy followed by slp_backward_entropy.
  *
  *   x, dtype, N, V, ld, t, mask, T   as for slp_forward.

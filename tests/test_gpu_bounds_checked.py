@@ -78,6 +78,7 @@ LOGITS = [
     ("packed", 3000, 20016),       # masked spans, warp-per-row kernels
     ("stability", 256, 131072),    # fp32, -inf columns; fused: TMEM part, 4 CTAs
     ("stability", 20, 100000),     # fp32, fused: TMEM part, 3 CTAs per row instead of 6
+    ("tiny", 4, 560000),           # 1.09 MB bf16 rows: the fused call's TMEM form, 8 CTAs
     ("stability", 64, 4099),
     ("tiny", 300, 2047),           # rows not 16-byte aligned: scalar kernels
 ]

@@ -173,9 +173,9 @@ def test_fused_entropy_null_weights(V):
     check_entropy_rows(a, gH, lp, lse, H, gx, range(40))
 
 
-@pytest.mark.parametrize("name,V", [("tiny", 350000), ("stability", 175000)])
-def test_fused_entropy_96k_segments(name, V):
-    """~700 KB rows (bf16 and fp32): the cluster kernel's shared-memory-only
+@pytest.mark.parametrize("name,V", [("tiny", 350000), ("stability", 175000), ("tiny", 560000)])
+def test_fused_entropy_tmem_long_rows(name, V):
+    """Rows of 700 KB to 1.09 MB (bf16 and fp32): the cluster kernel's TMEM
     form with the entropy."""
     dev = device()
     a = W.make_logits_inputs(name, device=dev, N=6, V=V)

@@ -386,11 +386,12 @@ def test_fused_forward_backward_deterministic_full_size():
 
 
 @pytest.mark.parametrize("name,V,Vp", [("tiny", 350000, 350000), ("tiny", 349997, 350000),
-                                       ("stability", 175000, 175000)])
-def test_fused_forward_backward_96k_segments(name, V, Vp):
-    """Rows of ~700 KB: too long for eight register-tail segments, so the
-    cluster kernel runs its shared-memory-only form (eight 96 KB segments);
-    one bf16 case with a scalar tail on an aligned stride, one fp32 case."""
+                                       ("stability", 175000, 175000), ("tiny", 400008, 400008),
+                                       ("tiny", 560000, 560000)])
+def test_fused_forward_backward_tmem_long_rows(name, V, Vp):
+    """Rows of 700 KB to 1.09 MB: longer than eight CTAs of the register form
+    hold, so the cluster kernel runs its TMEM form (5 to 8 CTAs per row); one
+    bf16 case with a scalar tail on an aligned stride, one fp32 case."""
     dev = device()
     a = W.make_logits_inputs(name, device=dev, N=6, V=Vp)
     x = a.x[:, :V]
@@ -403,10 +404,10 @@ def test_fused_forward_backward_96k_segments(name, V, Vp):
     check_rows(x, t, None, a.T, a.g, lp, lse, gx, range(6))
 
 
-@pytest.mark.parametrize("V", [400008, 420000])
+@pytest.mark.parametrize("V", [600000, 620008])
 def test_fused_forward_backward_long_rows(V):
-    """Rows longer than one cluster holds (8 x 96 KB) take the separate
-    kernels and still match the oracle."""
+    """Rows longer than one cluster holds (8 CTAs of the TMEM form, about
+    1.1 MB) take the separate kernels and still match the oracle."""
     dev = device()
     a = W.make_logits_inputs("tiny", device=dev, N=5, V=V)
     lp, lse, gx = slp.slp_forward_backward(a.x, a.t, a.mask, a.T, a.g)

@@ -522,14 +522,14 @@ __global__ void __launch_bounds__(32 * kRowsWarps)
 
 constexpr int kFbThreads = 256;
 constexpr int kFbChunk = 16384;
-constexpr int kFbMaxChunks = 6;
-constexpr int kFbMaxSeg = kFbChunk * kFbMaxChunks;  // 96 KB per CTA
 // Register part: kFbRV 16-byte vectors per thread.  With at most 64 registers
-// per thread and 233472 / 4 - 1024 - 256 bytes of shared memory, four CTAs
-// stay resident per SM (228 KB of shared memory per SM, less 1 KB reserved and
-// 256 B static per CTA); kFbRegSeg is the segment that fits.
+// per thread and kFbMaxSmem bytes of shared memory, four CTAs stay resident
+// per SM (228 KB of shared memory per SM, less 1 KB reserved and 256 B static
+// per CTA); kFbRegSeg is the segment that fits.
+constexpr int kFbMaxSmem = 233472 / 4 - 1024 - 256;
+constexpr int kFbMaxChunks = (kFbMaxSmem + kFbChunk - 1) / kFbChunk;
 constexpr int kFbRV = 5;
-constexpr int kFbRegSeg = 233472 / 4 - 1024 - 256 + kFbRV * kFbThreads * 16;
+constexpr int kFbRegSeg = kFbMaxSmem + kFbRV * kFbThreads * 16;
 constexpr int kFbMaxCluster = 8;
 // TMEM part: kFbTV more vectors per thread in tensor memory (tcgen05.st /
 // tcgen05.ld, 32 lanes x 4 kFbTV columns per warp, 128 columns per CTA).  An
@@ -573,8 +573,8 @@ __device__ __forceinline__ void free_tmem(uint32_t base) {
 // -gH p (log p + H) / T computed from the lse and H written here, exactly as
 // slp_bwd_kernel computes it from the saved ones (g and gH may then be NULL,
 // meaning zero).
-template <typename Elt, int kRV, int kTV, bool kEnt>
-__global__ void __launch_bounds__(kFbThreads, kRV > 0 ? 4 : 1)
+template <typename Elt, int kTV, bool kEnt>
+__global__ void __launch_bounds__(kFbThreads, 4)
     slp_fwd_bwd_kernel(const Elt* __restrict__ x, int64_t V, int64_t ld,
                        const int32_t* __restrict__ t, const uint8_t* __restrict__ mask, float T,
                        float c, float invT, const float* __restrict__ g,
@@ -601,6 +601,7 @@ __global__ void __launch_bounds__(kFbThreads, kRV > 0 ? 4 : 1)
   // the last kRV * kFbThreads vectors of the segment stay in registers (kRV
   // per thread), the kTV * kFbThreads before them in TMEM (kTV per thread),
   // the rest in shared memory
+  constexpr int kRV = kFbRV;
   constexpr int kRegVec = kRV * kFbThreads;
   constexpr int kTmVec = kTV * kFbThreads;
   const int nv_s = nv > kRegVec + kTmVec ? nv - kRegVec - kTmVec : 0;
@@ -1236,20 +1237,26 @@ cudaError_t fwd_bwd_rows_typed(const Elt* x, int64_t N, int64_t V, int64_t ld, c
 }
 
 // Whether the fused call runs the form with a TMEM part (C CTAs per row
-// without it, C_tm with): fp32 rows on which it saves at least two CTAs.
-// Measured (fused call, CUDA events, one box): fp32 rows of 65536 / 100000 /
-// 131072 / 150000 columns (4 -> 2, 6 -> 3, 7 -> 4, 8 -> 5 CTAs) take 8 / 10
-// / 7 / 5 % less time; 75968 columns (4 -> 3) 1 % more.  On bf16 rows, which
-// carry twice the elements per byte, the form lost at every size tried
+// without it, C_tm with).  Rows longer than eight CTAs of the register form
+// hold (about 606 KB) always take it: against the shared-memory-only clusters
+// that served rows up to 768 KB, and the separate kernels beyond, it took 24
+// to 29 % less time (703 KB rows: fp32 0.591 -> 0.450 ms, bf16 0.632 ->
+// 0.475 ms; 1000 KB rows: 0.673 -> 0.480 and 0.689 -> 0.496 ms).  Shorter
+// rows take it when they are fp32 and it saves at least two CTAs: fp32 rows
+// of 65536 / 100000 / 131072 / 150000 columns (4 -> 2, 6 -> 3, 7 -> 4,
+// 8 -> 5 CTAs) take 8 / 10 / 7 / 5 % less time, 75968 columns (4 -> 3) 1 %
+// more.  On such bf16 rows, which carry twice the elements per byte, it lost
 // (c151k 4 -> 3 CTAs: 0.414 against 0.396 ms; 248320 columns, 7 -> 4: 1.535
-// against 1.443 ms): there the TMEM part's loads, four vectors per round
-// trip, and its fold come before the shared-memory chunks are consumed.
-inline bool tmem_fused_form(bool regs, int64_t C, int64_t C_tm, size_t esize) {
-  return regs && esize == 4 && C_tm <= C - 2;
+// against 1.443 ms): the TMEM part's loads, four vectors per round trip, and
+// its fold come before the shared-memory chunks are consumed.
+inline bool tmem_fused_form(int64_t C, int64_t C_tm, size_t esize) {
+  if (C > kFbMaxCluster) return true;
+  return esize == 4 && C_tm <= C - 2;
 }
 
 // Fused forward + backward: needs 16-byte-aligned rows and rows short enough
-// to fit a cluster of at most 8 CTAs x 96 KB; returns cudaErrorNotSupported
+// to fit a cluster of at most 8 CTAs of the TMEM form (8 x kFbTmSeg bytes,
+// about 1.1 MB); returns cudaErrorNotSupported
 // otherwise (the caller then runs the separate kernels).  gH and entropy are
 // used with kEnt only.
 template <typename Elt, bool kEnt>
@@ -1265,28 +1272,23 @@ cudaError_t fwd_bwd_typed(const Elt* x, int64_t N, int64_t V, int64_t ld, const 
     return fwd_bwd_rows_typed<Elt, kEnt>(x, N, V, ld, t, mask, T, g, gH, logprob, lse, entropy,
                                          gx, ldg, err, stream);
   // Segments of at most kFbRegSeg bytes (kFbRV vectors per thread in
-  // registers, the rest in shared memory) keep four CTAs resident per SM.
-  // Longer rows take up to kFbMaxSeg of shared memory per CTA (two per SM).
-  const bool regs = (nvec * 16 + kFbRegSeg - 1) / kFbRegSeg <= kFbMaxCluster;
-  int64_t C = regs ? (nvec * 16 + kFbRegSeg - 1) / kFbRegSeg
-                   : (nvec * 16 + kFbMaxSeg - 1) / kFbMaxSeg;
-  if (C < 1) C = 1;
-  // With a TMEM part as well, a segment holds kFbTmSeg bytes: long rows then
+  // registers, the rest in shared memory) keep four CTAs resident per SM;
+  // with a TMEM part as well, a segment holds kFbTmSeg bytes, so long rows
   // need fewer CTAs per cluster.
+  int64_t C = (nvec * 16 + kFbRegSeg - 1) / kFbRegSeg;
+  if (C < 1) C = 1;
   const int64_t C_tm = (nvec * 16 + kFbTmSeg - 1) / kFbTmSeg;
-  const bool tm = tmem_fused_form(regs, C, C_tm, sizeof(Elt));
-  if (tm) C = C_tm;
+  const bool tm = tmem_fused_form(C, C_tm, sizeof(Elt));
+  if (tm) C = C_tm < 1 ? 1 : C_tm;
   if (C > kFbMaxCluster) return cudaErrorNotSupported;
   if (N * C > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
   const int64_t per = (nvec + C - 1) / C;  // vectors of the longest segment
-  const int64_t on_chip = regs ? (kFbRV + (tm ? kFbTV : 0)) * kFbThreads : 0;
+  const int64_t on_chip = (kFbRV + (tm ? kFbTV : 0)) * kFbThreads;
   const int64_t in_smem = per > on_chip ? per - on_chip : 0;
   int smem = static_cast<int>(in_smem * 16);
   if (tm && smem < kFbTmMinSmem) smem = kFbTmMinSmem;
-  auto kern = tm     ? slp_fwd_bwd_kernel<Elt, kFbRV, kFbTV, kEnt>
-              : regs ? slp_fwd_bwd_kernel<Elt, kFbRV, 0, kEnt>
-                     : slp_fwd_bwd_kernel<Elt, 0, 0, kEnt>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kFbMaxSeg);
+  auto kern = tm ? slp_fwd_bwd_kernel<Elt, kFbTV, kEnt> : slp_fwd_bwd_kernel<Elt, 0, kEnt>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kFbMaxSmem);
   if (e != cudaSuccess) return e;
   const float c = static_cast<float>(1.4426950408889634 / static_cast<double>(T));
   const float invT = 1.0f / T;
