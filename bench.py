@@ -52,6 +52,8 @@ def parse():
     p.add_argument("--lmhead-rows", type=int, default=None)
     p.add_argument("--fused-only", action="store_true",
                    help="time only the fused forward+backward on --config (and --rows)")
+    p.add_argument("--vocab", type=int, default=None,
+                   help="override V (same recipe), with --fused-only, e.g. for long-row profiling")
     p.add_argument("--rows", type=int, default=None,
                    help="override N (same recipe), e.g. for a small profiling case")
     return p.parse_args()
@@ -528,7 +530,7 @@ def main():
         return
     if args.fused_only:
         r = time_fused(device, hbm, steps=args.steps, warmup=args.warmup, names=(args.config,),
-                       rows=args.rows)
+                       rows=args.rows, vocab=args.vocab)
         if rank == 0:
             print(json.dumps({"fused_fwd_bwd": r}), flush=True)
         return
@@ -811,7 +813,7 @@ def time_topk(device, hbm, steps=20, warmup=3):
 
 
 def time_fused(device, hbm, steps=30, warmup=3, names=("c151k", "packed", "stability"),
-               rows=None):
+               rows=None, vocab=None):
     """slp_forward_backward (upstream gradient known at forward time): one
     read of the active rows and one write of the gradient per step."""
     from vocab_selected_token_gb300 import _lib
@@ -819,7 +821,7 @@ def time_fused(device, hbm, steps=30, warmup=3, names=("c151k", "packed", "stabi
     lib = _lib.load()
     out = {}
     for name in names:
-        inp = W.make_logits_inputs(name, device=device, N=rows)
+        inp = W.make_logits_inputs(name, device=device, N=rows, V=vocab)
         x = inp.x
         N, V = x.shape
         es = x.element_size()

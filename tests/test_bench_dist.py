@@ -145,6 +145,11 @@ def test_fused_timing_builds_each_workload_at_its_own_size(monkeypatch):
     with pytest.raises(Stop):
         bench.time_fused(torch.device("cpu"), 1.0, steps=1, warmup=1)
     assert seen == [("c151k", None), ("packed", None), ("stability", None)]
+    seen.clear()
+    with pytest.raises(Stop):
+        bench.time_fused(torch.device("cpu"), 1.0, steps=1, warmup=1,
+                         names=("c151k", "packed", "stability"), rows=7, vocab=None)
+    assert seen == [("c151k", 7), ("packed", 7), ("stability", 7)]
 
 
 def test_code_hash_ignores_comments_only():
