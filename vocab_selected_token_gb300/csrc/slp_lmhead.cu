@@ -304,6 +304,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // waits on (full, accumulator-empty); both CTAs load, and both drain their
   // own TMEM rows.  Without a pair the same code runs with rank 0 alone.
   const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+  const int tile0 = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int tiles_in_flight = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
   const uint32_t lead_full = kPair ? mapa_rank(bar_full, 0) : bar_full;
   const uint32_t lead_acce = kPair ? mapa_rank(bar_acce, 0) : bar_acce;
   const uint32_t peer_abort =
@@ -361,11 +363,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   int fills = 0;  // stage fills this CTA's producer issued
   if (blockIdx.x == 0 && threadIdx.x == 0 && p.work_next != nullptr) dbg::st(p.work_next, 0);
 
-  // Units: each pair claims the next unclaimed unit from a global counter,
-  // one ahead of the unit it works on (so the atomic's latency hides behind
-  // the unit in progress); pairs that run faster take more units, and a pair
-  // that starts late (its SMs still busy with other work) finds the units
-  // taken instead of holding one back.  Every role of both CTAs walks the same
+  // Units: each pair starts with unit tile0 (its index), so every pair has
+  // one however few units there are, then claims the next unclaimed unit from
+  // a global counter, one ahead of the unit it works on (so the atomic's
+  // latency hides behind the unit in progress); pairs that run faster take
+  // more units.  (Claiming the first unit as well let the first pairs to
+  // start take two units each when there were about as many units as pairs,
+  // and the last ones none.)  Every role of both CTAs walks the same
   // sequence: work item wi sits in slot wi % kWorkSlots; -1 ends it.  (Waits
   // on it acquire at cluster scope: the publishing arrival may come from the
   // other CTA.)
@@ -383,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(bar_wempty + 8 * (wi % kWorkSlots));
   };
   auto claim_unit = [&]() -> int {
-    return dbg::ok(p.work, 4) ? atomicAdd(p.work, 1) : sc.units;
+    return dbg::ok(p.work, 4) ? atomicAdd(p.work, 1) + tiles_in_flight : sc.units;
   };
 
   if (warp == 0) {
@@ -391,12 +395,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int it = 0;
       bool ok = true;
-      int u = sc.units;  // rank 0: the unit to publish next; rank 1: the one read
+      int u = tile0;  // rank 0: the unit to publish next; rank 1: overwritten by the ring
       int claim = sc.units;
-      if (rank == 0) {
-        u = claim_unit();
-        if (u < sc.units) claim = claim_unit();
-      }
+      if (rank == 0 && u < sc.units) claim = claim_unit();
       for (int wi = 0; ok; ++wi) {
         const int slot = wi % kWorkSlots;
         if (rank == 0) {
