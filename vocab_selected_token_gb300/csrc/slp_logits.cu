@@ -667,8 +667,8 @@ __global__ void __launch_bounds__(kFbThreads, 4)
   }
 
   const uint4 pad = make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord, E::kNegInfWord);
-  uint4 rv[kRV > 0 ? kRV : 1];  // the register part, loaded while the chunks stream in
-  if constexpr (kRV > 0) {
+  uint4 rv[kRV];  // the register part, loaded while the chunks stream in
+  {
     const uint4* xv = reinterpret_cast<const uint4*>(xr) + v0;
 #pragma unroll
     for (int u = 0; u < kRV; ++u) {
@@ -725,12 +725,10 @@ __global__ void __launch_bounds__(kFbThreads, 4)
       lse2_fold_vec<kPer>(st, vv, c, tag);
   }
   ok = !__syncthreads_or(!ok);
-  if constexpr (kRV > 0) {
-    if constexpr (kEnt)
-      lse3_fold_vec<kRV>(st, rv, c, tag);
-    else
-      lse2_fold_vec<kRV>(st, rv, c, tag);
-  }
+  if constexpr (kEnt)
+    lse3_fold_vec<kRV>(st, rv, c, tag);
+  else
+    lse2_fold_vec<kRV>(st, rv, c, tag);
   if (!ok && threadIdx.x == 0) {
     if (err != nullptr) atomicOr(err, SLP_DEVICE_ERR_TIMEOUT);
     for (int k = 0; k < nch; ++k)  // let every copy land before the CTA moves on
@@ -823,12 +821,10 @@ __global__ void __launch_bounds__(kFbThreads, 4)
     };
     for (int i = threadIdx.x; i < nv_s; i += kFbThreads) put(i, q[i]);
     if constexpr (kTV > 0) put_tmem<kTV>(taddr, nv_s, nv, put);
-    if constexpr (kRV > 0) {
 #pragma unroll
-      for (int u = 0; u < kRV; ++u) {
-        const int i = nv_r + u * kFbThreads + threadIdx.x;
-        if (i < nv) put(i, rv[u]);
-      }
+    for (int u = 0; u < kRV; ++u) {
+      const int i = nv_r + u * kFbThreads + threadIdx.x;
+      if (i < nv) put(i, rv[u]);
     }
     if (rank == C - 1)
       for (int64_t e = nvec * kVec + threadIdx.x; e < V; e += kFbThreads)
@@ -858,12 +854,10 @@ __global__ void __launch_bounds__(kFbThreads, 4)
   };
   for (int i = threadIdx.x; i < nv_s; i += kFbThreads) put(i, q[i]);
   if constexpr (kTV > 0) put_tmem<kTV>(taddr, nv_s, nv, put);
-  if constexpr (kRV > 0) {
 #pragma unroll
-    for (int u = 0; u < kRV; ++u) {
-      const int i = nv_r + u * kFbThreads + threadIdx.x;
-      if (i < nv) put(i, rv[u]);
-    }
+  for (int u = 0; u < kRV; ++u) {
+    const int i = nv_r + u * kFbThreads + threadIdx.x;
+    if (i < nv) put(i, rv[u]);
   }
   if (rank == C - 1) {
     for (int64_t e = nvec * kVec + threadIdx.x; e < V; e += kFbThreads) {
